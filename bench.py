@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the RVQ MoE expert-FFN decode layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one whole MoE layer (router logits -> top-k + grouping -> gate/up
+LUT-GEMV -> SwiGLU reduction -> down LUT-GEMV -> combine + residual) over one
+batch.  Default workload: the K3-shaped decode layer (d=7168, f=2048, 256
+experts, top-16, 4.23 GB of RVQ codes resident in HBM) at batch 1; each step
+takes the next token of a seeded pool, so the routed experts change every
+step and the codes stream from HBM (inputs larger than L2).
+
+Prints one JSON line (rank 0).  Multi-GPU (torchrun): independent replicas,
+no collective on the data path; value = all ranks' weights / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import workloads as W  # noqa: E402
+
+METRIC = "RVQ expert-FFN Gweights/s and code-byte HBM GB/s vs ~8 TB/s peak; layer tok/s"
+UNIT = "Gweights/s"
+WORKLOADS = {
+    # name: (config, batch)
+    "k3_decode_b1": (2, 1),
+    "k3_decode_b8": (2, 8),
+    "k3_decode_b64": (2, 64),
+    "decode_d2048_b1": (1, 1),
+    "decode_d2048_b4": (1, 4),
+    "decode_d2048_b16": (1, 16),
+}
+KERNELS = ["router_logits", "route", "lut_gemv_gate_up", "swiglu_reduce", "lut_gemv_down",
+           "combine"]
+DOMINANT = "lut_gemv_gate_up"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (ctypes on the
+    driver's libnvidia-ml) every ~2 ms; reads only."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        self.samples = []
+        self.ok = False
+        self.max_mhz = None
+        try:
+            import torch
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(cuda_index).uuid)
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                return
+            m = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = int(m.value)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _one(self):
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) != 0:
+            return None
+        fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        if fn(self.h, ctypes.byref(r)) != 0:
+            r.value = 0
+        return (time.perf_counter(), int(c.value), int(r.value))
+
+    def start(self):
+        self._stop = threading.Event()
+        if not self.ok:
+            return
+
+        def run():
+            while not self._stop.is_set():
+                s = self._one()
+                if s:
+                    self.samples.append(s)
+                time.sleep(0.002)
+        self.th = threading.Thread(target=run, daemon=True)
+        self.th.start()
+
+    def stop(self):
+        self._stop.set()
+        if self.ok:
+            self.th.join()
+
+    def summary(self, t0, t1):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "note": "NVML unavailable"}
+        win = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples
+        bits = 0
+        for s in win:
+            bits |= s[2]
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if bits & b],
+                "samples": len(win)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def build_layer(config, device, k=None):
+    from moe_expert_ffn_router_gb300.layer import MoeLayer
+    s = W.WORKLOADS[config].shape
+    src = W.ExpertSource(config, 0, s)
+    L = MoeLayer(s.E, s.d, s.f, k or s.k, layer=0, device=device)
+    for e in range(s.E):
+        mats = [(src.codes(e, m), src.codebooks(e, m)) for m in range(3)]
+        L.load_expert(e, mats[0][0], mats[1][0], mats[2][0], np.stack([c for _, c in mats]))
+    L.set_router(src.router_weight())
+    L.validate()
+    return L, src
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import moe_expert_ffn_router_gb300 as rvq
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    config, batch = WORKLOADS[args.workload]
+    s = W.WORKLOADS[config].shape
+    L, src = build_layer(config, dev)
+    pool = max(64, 4 * batch)
+    pool_bits = src.tokens_bf16(pool * batch if batch > 1 else pool)
+    xs = torch.from_numpy(pool_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    xs = xs.reshape(-1, batch, s.d)
+    nsteps = xs.shape[0]
+    bufs = L.buffers(batch)
+    weights_per_expert = 3 * s.d * s.f
+    code_bytes_per_expert = 3 * (3 * s.d * s.f // 8)
+    cb_bytes_per_expert = 3 * rvq.RVQ_CODEBOOK_BYTES
+
+    def step(i, events=None):
+        return L.forward(xs[i % nsteps], bufs, events=events)
+
+    # unique experts per step (from the routing the GPU computed); the pool
+    # is replayed identically in the timed loop, so count once per pool entry
+    uniq = []
+    for i in range(nsteps):
+        step(i)
+        torch.cuda.synchronize()
+        uniq.append(len(set(bufs["idx"].cpu().numpy().reshape(-1).tolist())))
+    rc, bits = L.status(batch)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits:#x}")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    t0w = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record()
+    barrier()
+    t1w = time.perf_counter()
+    ms = e0.elapsed_time(e1)
+    sampler.stop()
+    clocks = sampler.summary(t0w, t1w)
+
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    steps_idx = [(args.warmup + i) % nsteps for i in range(args.steps)]
+    experts_total = sum(uniq[j] for j in steps_idx)
+    weights = experts_total * weights_per_expert * world
+    sec = ms / 1e3
+    value = weights / sec / 1e9
+    code_gbs = experts_total * (code_bytes_per_expert + cb_bytes_per_expert) * world / sec / 1e9
+    tok_s = batch * args.steps * world / sec
+
+    # ---- per-kernel durations (events between kernels, same steps) ----
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(rvq.MOE_LAYER_EVENTS)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    per = {k: [] for k in KERNELS}
+    for i in range(args.steps):
+        step(args.warmup + i, events=evs)
+        torch.cuda.synchronize()
+        for j, name in enumerate(KERNELS):
+            per[name].append(evs[j].elapsed_time(evs[j + 1]))
+    avg = {k: float(np.mean(v)) for k, v in per.items()}
+    # algorithmic bytes of the gate/up launch: gate + up codes and codebooks of
+    # every unique selected expert
+    gu_bytes = np.mean([uniq[j] for j in steps_idx]) * 2 * (
+        3 * s.d * s.f // 8 + rvq.RVQ_CODEBOOK_BYTES)
+    peak, peak_kind = load_peaks()
+    achieved = gu_bytes / (avg[DOMINANT] / 1e3) / 1e9
+    roofline = {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": peak_kind, "traffic": None,
+                "algorithmic_bytes_per_launch": int(gu_bytes),
+                "avg_launch_us": round(avg[DOMINANT] * 1e3, 2)}
+
+    # ---- end to end through host buffers ----
+    pinned_in = torch.from_numpy(pool_bits.view(np.int16).copy()).reshape(-1, batch, s.d)
+    pinned_in = pinned_in.pin_memory()
+    pinned_out = torch.empty((batch, s.d), dtype=torch.float32).pin_memory()
+    xbuf = torch.empty((batch, s.d), dtype=torch.bfloat16, device=dev)
+    for i in range(args.warmup):
+        xbuf.view(torch.int16).copy_(pinned_in[i % nsteps], non_blocking=True)
+        L.forward(xbuf, bufs)
+        pinned_out.copy_(bufs["out"], non_blocking=True)
+    barrier()
+    e0.record()
+    for i in range(args.steps):
+        j = (args.warmup + i) % nsteps
+        xbuf.view(torch.int16).copy_(pinned_in[j], non_blocking=True)
+        L.forward(xbuf, bufs)
+        pinned_out.copy_(bufs["out"], non_blocking=True)
+    e1.record()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_e2e = float(tt.item())
+    e2e = {"value": round(weights / (ms_e2e / 1e3) / 1e9, 2), "unit": UNIT,
+           "h2d_bytes_per_step": batch * s.d * 2, "d2h_bytes_per_step": batch * s.d * 4}
+    rc, bits = L.status(batch)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits:#x}")
+    res = dict(value=value, ms=ms, code_gbs=code_gbs, tok_s=tok_s, roofline=roofline, e2e=e2e,
+               clocks=clocks, kernels_us={k: round(v * 1e3, 2) for k, v in avg.items()},
+               uniq_mean=float(np.mean([uniq[j] for j in steps_idx])),
+               launches=len(KERNELS) * args.steps, config=config, batch=batch, shape=s)
+    del L
+    return res
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(config, batch, tokens, src=None):
+    """Time the oracle (as it stands, one thread) on `tokens` tokens of the
+    workload.  Returns (Gweights/s, seconds, weights)."""
+    import oracle
+    import synth
+    s = W.WORKLOADS[config].shape
+    src = src or W.ExpertSource(config, 0, s)
+    wr = src.router_weight()
+    x64 = synth.bf16_to_f32(src.tokens_bf16(tokens)).astype(np.float64)
+    lg = oracle.router_logits(wr, x64).astype(np.float32)
+    idx, _, _ = oracle.route(lg, s.k)
+    cache = {}
+    for e in sorted(set(idx.reshape(-1).tolist())):
+        cache[e] = tuple((src.codes(e, m), src.codebooks(e, m)) for m in range(3))
+    t0 = time.perf_counter()
+    weights = 0
+    for t in range(tokens):
+        r = oracle.moe_layer(lambda e: cache[e], wr, x64[t:t + 1], s.k, s.d, s.f)
+        weights += len(set(r["idx"].reshape(-1).tolist())) * 3 * s.d * s.f
+    dt = time.perf_counter() - t0
+    return weights / dt / 1e9, dt, weights
+
+
+def reference_arm(args, rank):
+    """The oracle as the reference implementation: each step evaluates m of
+    the experts one token selects (all k when the step budget allows), so the
+    whole --steps/--warmup run stays near a minute of CPU time."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    config, batch = WORKLOADS[args.workload]
+    s = W.WORKLOADS[config].shape
+    src = W.ExpertSource(config, 0, s)
+    per_expert_s = 0.15 * (s.d * s.f) / (7168 * 2048)
+    m = int(max(1, min(s.k, 60.0 / ((args.steps + args.warmup) * per_expert_s))))
+    wr = src.router_weight()
+    ntok = max(1, (args.steps + args.warmup) * m // s.k + 1)
+    x64 = synth.bf16_to_f32(src.tokens_bf16(ntok)).astype(np.float64)
+    idx, _, _ = oracle.route(oracle.router_logits(wr, x64).astype(np.float32), s.k)
+    work = [(t, int(e)) for t in range(ntok) for e in idx[t]]
+    times, weights, pos = 0.0, 0, 0
+    for i in range(args.warmup + args.steps):
+        chunk = work[pos:pos + m]
+        pos += m
+        mats = {e: tuple((src.codes(e, q), src.codebooks(e, q)) for q in range(3))
+                for _, e in chunk}
+        t0 = time.perf_counter()
+        for t, e in chunk:
+            oracle.expert_ffn(*mats[e], s.d, s.f, x64[t])
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times += dt
+            weights += len(chunk) * 3 * s.d * s.f
+    value = weights / times / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(times / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": W.WORKLOADS[config].name, "batch": batch},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"{m} of the {s.k} experts one token selects per step "
+                                       "(oracle expert FFN: explicit dequant + fp64 matmuls)"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="k3_decode_b1", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--oracle-tokens", type=int, default=4)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    r = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        s = r["shape"]
+        cpu = None
+        if world == 1 or rank == 0:
+            v, dt, wts = oracle_sample(r["config"], r["batch"], args.oracle_tokens)
+            cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{args.oracle_tokens} tokens through the whole oracle layer "
+                             f"({wts / 1e9:.2f} G weights, {dt:.1f} s)"}
+        line = {
+            "metric": METRIC, "value": round(r["value"], 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": W.WORKLOADS[r["config"]].name, "batch": r["batch"],
+                       "d": s.d, "f": s.f, "experts": s.E, "top_k": s.k,
+                       "codes_bytes": 3 * (3 * s.d * s.f // 8) * s.E,
+                       "l2": "inputs larger than L2: 4.23 GB code bank, token pool rotates "
+                             "routing every step" if r["config"] == 2 else
+                             "bank 151 MB; token pool rotates routing every step",
+                       "parallelism": f"replicas{world}"},
+            "code_byte_gbs": round(r["code_gbs"], 1),
+            "layer_tok_s": round(r["tok_s"], 1),
+            "unique_experts_per_step": round(r["uniq_mean"], 2),
+            "kernels_us": r["kernels_us"],
+            "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+            "clocks": r["clocks"], "gpu_launches": r["launches"] * world,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

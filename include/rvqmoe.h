@@ -1,0 +1,269 @@
+/*
+ * rvqmoe -- Mixture-of-Experts expert FFN on 3-stage residual-vector-quantised
+ * (RVQ) weights, for NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * Method (sources are public web pages on the WASTE inference engine):
+ *  - Expert weights are coded by 3-stage residual vector quantisation of
+ *    8-dimensional sub-vectors with 256-entry codebooks: one uint8 code per
+ *    stage per sub-vector, 3.00 bits per weight, no entropy coding
+ *    ["WASTE Inference Engine: Running Kimi K3 2.78T on Consumer Hardware",
+ *    section "Residual Vector Quantization (RVQ)"; GeekNews topic 32035,
+ *    section "Quantization and accuracy"].
+ *  - The weight matrix is never materialised: a partial-dot lookup table is
+ *    built per codebook and position, T_s[j][k] = <x[8j..8j+7], C_s[k]>, and
+ *    each output row is a sum over positions j of three table reads
+ *    ["Running a 2.78-Trillion-Parameter Model on a Laptop: Inside WASTE's
+ *    NVMe-Streaming Engine", section "Technical Insight"].
+ *  - An expert is gate, up and down projection matrices stored together in
+ *    one record with its codebooks and a checked header [same page, section
+ *    "Technical Insight"; GeekNews topic 32035, section "Disk streaming
+ *    structure"]; the router picks 16 experts per layer [GeekNews topic
+ *    32035, section "Read-ahead and router prediction"].
+ *  Readings where the pages are silent (sub-vectors along the input
+ *  dimension, one codebook set per matrix, top-k softmax renormalised over
+ *  the selected experts with ties to the lower index, SwiGLU, weighted
+ *  combine plus residual) are stated at the calls below.
+ *
+ * Conventions for every call:
+ *  - Pointers marked (dev) are device memory, (host) host memory.  The caller
+ *    owns every buffer; the library allocates nothing and frees nothing.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream), except where "synchronous" is stated.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns RVQ_EINVAL (shape, null pointer, range) or RVQ_EALIGN
+ *    (a pointer that is not 16-byte aligned) and launches nothing.
+ *  - Conditions only the device can see (an expert index outside the bank, a
+ *    corrupted record header, a non-finite router logit) set bits of the
+ *    status word at the start of the caller's workspace; rvq_ws_status()
+ *    reads them.  No call traps, aborts or exits.
+ *  - rvq_last_error() returns a thread-local message for the last failure.
+ *  - Calls on different streams with different buffers are thread-safe.
+ */
+#ifndef RVQMOE_H
+#define RVQMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *rvq_stream_t; /* identical to cudaStream_t */
+
+typedef enum rvq_status {
+    RVQ_OK = 0,
+    RVQ_EINVAL = 1,   /* invalid argument (shape, range, null pointer)          */
+    RVQ_EALIGN = 2,   /* pointer not 16-byte aligned                             */
+    RVQ_ENOMEM = 3,   /* caller-provided workspace or buffer too small           */
+    RVQ_ECORRUPT = 4, /* bank record header failed validation                    */
+    RVQ_EDEVICE = 5,  /* a kernel flagged a bad index or non-finite input        */
+    RVQ_ETIMEOUT = 6, /* a bounded device-side wait gave up                      */
+    RVQ_ECUDA = 7,    /* a CUDA runtime call failed (message in rvq_last_error)  */
+    RVQ_ENOTIMPL = 8  /* configuration not supported by this build               */
+} rvq_status;
+
+typedef enum rvq_dtype { RVQ_F32 = 0, RVQ_BF16 = 1 } rvq_dtype;
+
+/* Bits of the device status word (first 4 bytes of every workspace). */
+#define RVQ_DEV_ERR_INDEX 0x1u    /* expert index / offsets outside range      */
+#define RVQ_DEV_ERR_NONFINITE 0x2u /* router logit NaN or infinite             */
+#define RVQ_DEV_ERR_CORRUPT 0x4u  /* expert record header mismatch             */
+#define RVQ_DEV_ERR_TIMEOUT 0x8u  /* bounded spin-wait expired                 */
+
+/* Bytes at the start of every workspace reserved for the status block. */
+#define RVQ_WS_STATUS_BYTES 256u
+
+const char *rvq_status_string(rvq_status s);
+const char *rvq_last_error(void);
+/* Library version, e.g. 0x000100 for 0.1.0. */
+uint32_t rvq_version(void);
+
+/* --------------------------------------------------------------------------
+ * Packed code layout ("RVQ tile layout").  A matrix of `rows` x `cols`
+ * weights has cols/8 sub-vectors ("chunks") per row and 3 codes per chunk.
+ * Requirements: rows % 32 == 0, cols % 512 == 0.  Size: exactly
+ * 3 * rows * cols / 8 bytes (3.00 bits per weight).
+ *   tile (g, b), g < cols/256 (32-chunk group), b < rows/32 (32-row block),
+ *   starts at byte ((g * rows/32) + b) * 3072.  Inside a tile, byte
+ *   ((s*2 + h)*32 + l)*16 + i  (stage s < 3, half h < 2, lane l < 32, i < 16)
+ *   holds the stage-s code of row 32b + l, chunk 32g + ((16h + i + l) mod 32).
+ * The per-row rotation (l) makes the 32 lanes of a warp read 32 different
+ * table columns at every step, so shared-memory lookups never conflict.
+ *
+ * Packed codebook layout: fp32 [3][128][8][2]; element (stage s, entry k,
+ * dimension i) sits at ((s*128 + k/2)*8 + i)*2 + (k & 1), i.e. entries are
+ * interleaved in pairs so that two table entries are built per packed
+ * fp32x2 FMA.  Size RVQ_CODEBOOK_BYTES.
+ * ------------------------------------------------------------------------ */
+#define RVQ_CODEBOOK_BYTES 24576u
+
+/* 3 * rows * cols / 8; 0 if rows/cols do not satisfy the layout rules. */
+size_t rvq_code_bytes(int32_t rows, int32_t cols);
+
+/* Canonical codes (dev) uint8 [rows][cols/8][3] -> packed codes (dev).
+ * dst_bytes must be >= rvq_code_bytes(rows, cols).  src and dst must not
+ * overlap.  EINVAL on shape, ENOMEM if dst_bytes is short. */
+rvq_status rvq_pack(const uint8_t *codes_dev, int32_t rows, int32_t cols,
+                    uint8_t *packed_dev, size_t dst_bytes, rvq_stream_t stream);
+
+/* Inverse of rvq_pack (used by round-trip tests). */
+rvq_status rvq_unpack(const uint8_t *packed_dev, int32_t rows, int32_t cols,
+                      uint8_t *codes_dev, size_t dst_bytes, rvq_stream_t stream);
+
+/* Canonical codebooks (dev) fp32 [3][256][8] -> packed codebooks (dev). */
+rvq_status rvq_pack_codebooks(const float *cb_dev, float *cb_packed_dev, rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * Partial-dot lookup table, "per codebook and position" [starlog page,
+ * "Technical Insight"]: lut[t][j][s][k] = sum_{i<8} x[t][8j+i] * C_s[k][i]
+ * for every token t < n, chunk j < cols/8, stage s < 3, entry k < 256, fp32.
+ * codebooks: canonical fp32 [3][256][8] (dev); x: [n][cols] of xdt (dev);
+ * lut: fp32 [n][cols/8][3][256] (dev).  cols % 8 == 0.  The fused GEMV and
+ * FFN calls build the same table tile by tile in shared memory and never
+ * write it out; this call exists to expose and test that step on its own.
+ * ------------------------------------------------------------------------ */
+rvq_status rvq_lut_build(const float *codebooks_dev, const void *x_dev, rvq_dtype xdt,
+                         int32_t n, int32_t cols, float *lut_dev, rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * One RVQ matrix times n input vectors, on the codes directly:
+ * y[t][r] = sum_j sum_s T^t_s[j][code(r,j,s)] (== W x with W the residual
+ * decode) [agentlenshq page, "Residual Vector Quantization (RVQ)"].
+ * packed codes + packed codebooks (dev); x [n][cols] of xdt (dev); y fp32
+ * [n][rows] (dev).  Workspace (dev) of at least
+ * rvq_gemv_workspace_bytes(rows, cols, n) bytes, 256-byte aligned; its
+ * status block must have been cleared once with rvq_ws_clear().
+ * ------------------------------------------------------------------------ */
+size_t rvq_gemv_workspace_bytes(int32_t rows, int32_t cols, int32_t n);
+rvq_status rvq_gemv(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
+                    int32_t rows, int32_t cols, const void *x_dev, rvq_dtype xdt, int32_t n,
+                    float *y_dev, void *ws_dev, size_t ws_bytes, rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * Expert bank: n_experts records of record_bytes each, contiguous in HBM.
+ * Record = [rvq_expert_header, 128 B][packed codebooks gate, up, down]
+ *          [packed codes gate f x d][up f x d][down d x f]; every part starts
+ * on a 128-byte boundary, records on a 256-byte boundary.  gate, up and down
+ * of one expert are adjacent, as in the pages' one-read expert record.
+ * ------------------------------------------------------------------------ */
+#define RVQ_BANK_MAGIC 0x31515652u /* "RVQ1" little-endian */
+
+typedef struct rvq_expert_header {
+    uint32_t magic;        /* RVQ_BANK_MAGIC                                  */
+    uint32_t version;      /* 1                                               */
+    int32_t layer;         /* layer id given to moe_bank_init                 */
+    int32_t expert;        /* expert id == record index                       */
+    int32_t d, f;          /* hidden and intermediate size                    */
+    uint32_t flags;        /* 0                                               */
+    uint32_t crc32;        /* 0 (payload checksum not computed)               */
+    uint64_t cb_off;       /* byte offsets from the record start             */
+    uint64_t gate_off, up_off, down_off;
+    uint64_t record_bytes;
+    uint8_t pad[56];
+} rvq_expert_header;       /* 128 bytes */
+
+typedef struct rvq_moe_bank {
+    uint8_t *base;         /* (dev) first record, 256-byte aligned            */
+    uint64_t record_bytes; /* moe_bank_record_bytes(d, f)                     */
+    int32_t n_experts, d, f, layer;
+} rvq_moe_bank;
+
+uint64_t moe_bank_record_bytes(int32_t d, int32_t f);
+
+/* Fill *bank for a device buffer of `bytes` bytes (host-side only, launches
+ * nothing).  d % 512 == 0, f % 512 == 0, 1 <= n_experts <= 256.  ENOMEM if
+ * bytes < n_experts * record_bytes. */
+rvq_status moe_bank_init(rvq_moe_bank *bank, uint8_t *base_dev, uint64_t bytes,
+                         int32_t n_experts, int32_t d, int32_t f, int32_t layer);
+
+/* Write one expert record: packs canonical codes (dev) gate/up [f][d/8][3],
+ * down [d][f/8][3] and canonical codebooks (dev) fp32 [3 matrices][3][256][8]
+ * (gate, up, down), and writes the header. */
+rvq_status moe_bank_write_expert(const rvq_moe_bank *bank, int32_t expert,
+                                 const uint8_t *gate_codes_dev, const uint8_t *up_codes_dev,
+                                 const uint8_t *down_codes_dev, const float *codebooks_dev,
+                                 rvq_stream_t stream);
+
+/* Synchronous: copies every record header to the host and checks magic,
+ * version, layer, expert id, shape and offset ranges.  ECORRUPT on mismatch
+ * (message names the first bad record). */
+rvq_status moe_bank_validate(const rvq_moe_bank *bank, rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * Router.  logits[t][e] = sum_c Wr[e][c] * x[t][c] (+ bias[e]), fp32
+ * accumulate.  Wr fp32 [E][d] (dev); bias fp32 [E] (dev) or NULL; x [n][d]
+ * of xdt (dev); logits fp32 [n][E] (dev).  1 <= E <= 256, d % 8 == 0.
+ * ------------------------------------------------------------------------ */
+rvq_status moe_router_logits(const float *wr_dev, const float *bias_dev, const void *x_dev,
+                             rvq_dtype xdt, int32_t n, int32_t E, int32_t d,
+                             float *logits_dev, rvq_stream_t stream);
+
+/* Top-k selection, weights and token grouping.
+ * Selection: the k largest fp32 logits of each token, equal logits ordered by
+ * the lower expert index; slots are written in that order.  Weights:
+ * w = exp(l - l_max) / sum over the k selected (softmax renormalised over
+ * the selection).  Grouping: offsets[E+1] = exclusive prefix of per-expert
+ * counts; pairs[n*k] sorted by (expert, token), entry = t*k + slot.
+ * topk_idx int32 [n][k], topk_w fp32 [n][k], offsets int32 [E+1], pairs int32
+ * [n*k] (all dev).  1 <= k <= min(E, 32), E <= 256, 1 <= n <= moe_route_max_tokens(E).
+ * A non-finite logit sets RVQ_DEV_ERR_NONFINITE in the workspace status word
+ * (ws >= RVQ_WS_STATUS_BYTES); outputs are then unspecified but in range. */
+int32_t moe_route_max_tokens(int32_t E);
+rvq_status moe_route(const float *logits_dev, int32_t n, int32_t E, int32_t k,
+                     int32_t *topk_idx_dev, float *topk_w_dev, int32_t *offsets_dev,
+                     int32_t *pairs_dev, void *ws_dev, size_t ws_bytes, rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * Expert FFN on the grouped pairs: for every pair entry p = t*k + slot with
+ * expert e, y_pair[p] = Wd_e (silu(Wg_e x_t) * (Wu_e x_t)), silu(g) =
+ * g / (1 + exp(-g)), all matrices evaluated on their RVQ codes through
+ * shared-memory lookup tables with fp32 accumulation.  Reads offsets [E+1]
+ * and pairs [n*k] from moe_route (dev); x [n][d] of xdt (dev); y_pair fp32
+ * [n*k][d] (dev).  Each block checks its expert's record header on read and
+ * sets RVQ_DEV_ERR_CORRUPT / RVQ_DEV_ERR_INDEX instead of computing with a bad
+ * record.  ws >= moe_workspace_bytes(bank, n, k), 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t moe_workspace_bytes(const rvq_moe_bank *bank, int32_t n, int32_t k);
+rvq_status moe_expert_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
+                          int32_t n, int32_t k, const int32_t *offsets_dev,
+                          const int32_t *pairs_dev, float *y_pair_dev, void *ws_dev,
+                          size_t ws_bytes, rvq_stream_t stream);
+
+/* Weighted combine plus residual: out[t][c] = residual[t][c] +
+ * sum_slot topk_w[t][slot] * y_pair[t*k + slot][c], fp32.  residual [n][d]
+ * of rdt (dev), out fp32 [n][d] (dev); out may alias residual only if rdt is
+ * RVQ_F32. */
+rvq_status moe_combine(const float *y_pair_dev, const float *topk_w_dev, int32_t n, int32_t k,
+                       int32_t d, const void *residual_dev, rvq_dtype rdt, float *out_dev,
+                       rvq_stream_t stream);
+
+/* One whole MoE layer: router logits, routing and grouping, expert FFN and
+ * combine, with the last reduction of the FFN fused into the combine.
+ * Outputs as the separate calls (logits, topk_idx, topk_w, offsets, pairs,
+ * out; all dev).  x is also the residual.  bias may be NULL.
+ * ws >= moe_workspace_bytes(bank, n, k).  If `events` is not NULL it must
+ * hold MOE_LAYER_EVENTS cudaEvent_t handles, recorded on `stream` before
+ * the first kernel and after each kernel (for per-kernel timing). */
+#define MOE_LAYER_EVENTS 7
+rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, const float *bias_dev,
+                             const void *x_dev, rvq_dtype xdt, int32_t n, int32_t k,
+                             float *logits_dev, int32_t *topk_idx_dev, float *topk_w_dev,
+                             int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
+                             void *ws_dev, size_t ws_bytes, void **events,
+                             rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * Workspace status block.
+ * rvq_ws_clear: zero the status block (async).  Call once per workspace.
+ * rvq_ws_status: synchronous; waits for `stream`, reads the status word,
+ * returns RVQ_OK, RVQ_EDEVICE (index / non-finite), RVQ_ECORRUPT or
+ * RVQ_ETIMEOUT, stores the raw bits in *bits_out if not NULL, and clears it.
+ * ------------------------------------------------------------------------ */
+rvq_status rvq_ws_clear(void *ws_dev, rvq_stream_t stream);
+rvq_status rvq_ws_status(void *ws_dev, uint32_t *bits_out, rvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RVQMOE_H */

@@ -1,0 +1,249 @@
+"""Python binding of librvqmoe (RVQ MoE expert FFN for GB300, sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Functions carry the C names of include/rvqmoe.h and take torch tensors (device
+memory) plus the current CUDA stream.  Importing fails loudly when the
+compiled library is missing; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librvqmoe.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "rvqmoe.h")
+
+RVQ_F32, RVQ_BF16 = 0, 1
+RVQ_WS_STATUS_BYTES = 256
+RVQ_CODEBOOK_BYTES = 24576
+RVQ_BANK_MAGIC = 0x31515652
+MOE_LAYER_EVENTS = 7
+DEV_ERR_INDEX, DEV_ERR_NONFINITE, DEV_ERR_CORRUPT, DEV_ERR_TIMEOUT = 1, 2, 4, 8
+STATUS = {0: "RVQ_OK", 1: "RVQ_EINVAL", 2: "RVQ_EALIGN", 3: "RVQ_ENOMEM", 4: "RVQ_ECORRUPT",
+          5: "RVQ_EDEVICE", 6: "RVQ_ETIMEOUT", 7: "RVQ_ECUDA", 8: "RVQ_ENOTIMPL"}
+
+
+class RvqError(RuntimeError):
+    def __init__(self, name, code, msg):
+        super().__init__(f"{name}: {STATUS.get(code, code)}: {msg}")
+        self.code = code
+        self.status = STATUS.get(code, str(code))
+
+
+class RvqMoeBank(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("record_bytes", ctypes.c_uint64),
+                ("n_experts", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("f", ctypes.c_int32), ("layer", ctypes.c_int32)]
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; "
+                      "g.build()'` (nvcc, sm_103a)")
+
+_vp, _i32, _u32, _u64, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32,
+                              ctypes.c_uint64, ctypes.c_size_t)
+_lib = ctypes.CDLL(LIB_PATH)
+_BANKP = ctypes.POINTER(RvqMoeBank)
+_SIGS = {
+    "rvq_status_string": (ctypes.c_char_p, [_i32]),
+    "rvq_last_error": (ctypes.c_char_p, []),
+    "rvq_version": (_u32, []),
+    "rvq_code_bytes": (_sz, [_i32, _i32]),
+    "rvq_pack": (_i32, [_vp, _i32, _i32, _vp, _sz, _vp]),
+    "rvq_unpack": (_i32, [_vp, _i32, _i32, _vp, _sz, _vp]),
+    "rvq_pack_codebooks": (_i32, [_vp, _vp, _vp]),
+    "rvq_lut_build": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "rvq_gemv_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "rvq_gemv": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "moe_bank_record_bytes": (_u64, [_i32, _i32]),
+    "moe_bank_init": (_i32, [_BANKP, _vp, _u64, _i32, _i32, _i32, _i32]),
+    "moe_bank_write_expert": (_i32, [_BANKP, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_bank_validate": (_i32, [_BANKP, _vp]),
+    "moe_router_logits": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "moe_route_max_tokens": (_i32, [_i32]),
+    "moe_route": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_workspace_bytes": (_sz, [_BANKP, _i32, _i32]),
+    "moe_expert_ffn": (_i32, [_BANKP, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),
+    "moe_layer_forward": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                 _vp, _vp, _vp, _sz, _vp, _vp]),
+    "rvq_ws_clear": (_i32, [_vp, _vp]),
+    "rvq_ws_status": (_i32, [_vp, ctypes.POINTER(_u32), _vp]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def header_functions() -> list[str]:
+    """Names of every function declared in include/rvqmoe.h."""
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(\w+)\s*\([^;{]*\)\s*;", txt)) - {"if", "while"})
+
+
+def lib_has(name: str) -> bool:
+    return hasattr(_lib, name)
+
+
+# ------------------------------------------------------------------ helpers
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dt(t) -> int:
+    if t.dtype == torch.bfloat16:
+        return RVQ_BF16
+    if t.dtype == torch.float32:
+        return RVQ_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _check(name, rc):
+    if rc != 0:
+        raise RvqError(name, rc, last_error())
+
+
+def status_string(code: int) -> str:
+    return _lib.rvq_status_string(code).decode()
+
+
+def last_error() -> str:
+    return _lib.rvq_last_error().decode()
+
+
+def rvq_version() -> int:
+    return int(_lib.rvq_version())
+
+
+# ------------------------------------------------------------------ RVQ calls
+
+def rvq_code_bytes(rows: int, cols: int) -> int:
+    return int(_lib.rvq_code_bytes(rows, cols))
+
+
+def rvq_pack(codes, rows, cols, packed, stream=None):
+    _check("rvq_pack", _lib.rvq_pack(_p(codes), rows, cols, _p(packed), _nbytes(packed),
+                                     _stream(stream)))
+
+
+def rvq_unpack(packed, rows, cols, codes, stream=None):
+    _check("rvq_unpack", _lib.rvq_unpack(_p(packed), rows, cols, _p(codes), _nbytes(codes),
+                                         _stream(stream)))
+
+
+def rvq_pack_codebooks(cb, cb_packed, stream=None):
+    _check("rvq_pack_codebooks", _lib.rvq_pack_codebooks(_p(cb), _p(cb_packed), _stream(stream)))
+
+
+def rvq_lut_build(codebooks, x, n, cols, lut, stream=None):
+    _check("rvq_lut_build", _lib.rvq_lut_build(_p(codebooks), _p(x), _dt(x), n, cols, _p(lut),
+                                               _stream(stream)))
+
+
+def rvq_gemv_workspace_bytes(rows, cols, n) -> int:
+    return int(_lib.rvq_gemv_workspace_bytes(rows, cols, n))
+
+
+def rvq_gemv(packed_codes, packed_cb, rows, cols, x, n, y, ws, stream=None):
+    _check("rvq_gemv", _lib.rvq_gemv(_p(packed_codes), _p(packed_cb), rows, cols, _p(x), _dt(x),
+                                     n, _p(y), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+# ------------------------------------------------------------------ bank
+
+def moe_bank_record_bytes(d: int, f: int) -> int:
+    return int(_lib.moe_bank_record_bytes(d, f))
+
+
+def moe_bank_init(buffer, n_experts, d, f, layer=0) -> RvqMoeBank:
+    bank = RvqMoeBank()
+    _check("moe_bank_init", _lib.moe_bank_init(ctypes.byref(bank), _p(buffer), _nbytes(buffer),
+                                               n_experts, d, f, layer))
+    return bank
+
+
+def moe_bank_write_expert(bank, expert, gate_codes, up_codes, down_codes, codebooks, stream=None):
+    _check("moe_bank_write_expert",
+           _lib.moe_bank_write_expert(ctypes.byref(bank), expert, _p(gate_codes), _p(up_codes),
+                                      _p(down_codes), _p(codebooks), _stream(stream)))
+
+
+def moe_bank_validate(bank, stream=None):
+    _check("moe_bank_validate", _lib.moe_bank_validate(ctypes.byref(bank), _stream(stream)))
+
+
+# ------------------------------------------------------------------ MoE calls
+
+def moe_router_logits(wr, bias, x, n, E, d, logits, stream=None):
+    _check("moe_router_logits",
+           _lib.moe_router_logits(_p(wr), _p(bias), _p(x), _dt(x), n, E, d, _p(logits),
+                                  _stream(stream)))
+
+
+def moe_route_max_tokens(E: int) -> int:
+    return int(_lib.moe_route_max_tokens(E))
+
+
+def moe_route(logits, n, E, k, topk_idx, topk_w, offsets, pairs, ws, stream=None):
+    _check("moe_route", _lib.moe_route(_p(logits), n, E, k, _p(topk_idx), _p(topk_w),
+                                       _p(offsets), _p(pairs), _p(ws), _nbytes(ws),
+                                       _stream(stream)))
+
+
+def moe_workspace_bytes(bank, n, k) -> int:
+    return int(_lib.moe_workspace_bytes(ctypes.byref(bank), n, k))
+
+
+def moe_expert_ffn(bank, x, n, k, offsets, pairs, y_pair, ws, stream=None):
+    _check("moe_expert_ffn",
+           _lib.moe_expert_ffn(ctypes.byref(bank), _p(x), _dt(x), n, k, _p(offsets), _p(pairs),
+                               _p(y_pair), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_combine(y_pair, topk_w, n, k, d, residual, out, stream=None):
+    _check("moe_combine", _lib.moe_combine(_p(y_pair), _p(topk_w), n, k, d, _p(residual),
+                                           _dt(residual), _p(out), _stream(stream)))
+
+
+def moe_layer_forward(bank, wr, bias, x, n, k, logits, topk_idx, topk_w, offsets, pairs, out,
+                      ws, events=None, stream=None):
+    ev = None
+    if events is not None:
+        assert len(events) == MOE_LAYER_EVENTS
+        ev = (ctypes.c_void_p * MOE_LAYER_EVENTS)(*[e.cuda_event for e in events])
+    _check("moe_layer_forward",
+           _lib.moe_layer_forward(ctypes.byref(bank), _p(wr), _p(bias), _p(x), _dt(x), n, k,
+                                  _p(logits), _p(topk_idx), _p(topk_w), _p(offsets), _p(pairs),
+                                  _p(out), _p(ws), _nbytes(ws), ev, _stream(stream)))
+
+
+def rvq_ws_clear(ws, stream=None):
+    _check("rvq_ws_clear", _lib.rvq_ws_clear(_p(ws), _stream(stream)))
+
+
+def rvq_ws_status(ws, stream=None) -> tuple[int, int]:
+    """Returns (status code, raw device bits); clears the bits."""
+    bits = _u32(0)
+    rc = _lib.rvq_ws_status(_p(ws), ctypes.byref(bits), _stream(stream))
+    return int(rc), int(bits.value)

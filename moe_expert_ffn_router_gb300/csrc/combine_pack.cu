@@ -1,0 +1,144 @@
+// Weighted combine + residual, and the packing kernels for the code layout,
+// the codebook layout and the expert-record header.
+#include "internal.cuh"
+
+namespace rvq {
+namespace {
+
+// out[t][c] = res[t][c] + sum_slot w[t][slot] * sum_s ypart[(t*k+slot)*nslot + s][c]
+// (reading: the pages do not describe the combine; this is the standard MoE
+// output with the routing weights).  Four columns per thread, 128-bit loads.
+__global__ void combine_kernel(const float *__restrict__ ypart, int nslot,
+                               const float *__restrict__ w, int n, int k, int d,
+                               const void *res, int rdt, float *out) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int d4 = d >> 2;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)n * d4) return;
+    const int t = (int)(i / d4);
+    const int c = (int)(i % d4) * 4;
+    float4 acc;
+    if (rdt == RVQ_BF16) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(
+            reinterpret_cast<const uint16_t *>(res) + (int64_t)t * d + c);
+        acc.x = __uint_as_float(r.x << 16);
+        acc.y = __uint_as_float(r.x & 0xFFFF0000u);
+        acc.z = __uint_as_float(r.y << 16);
+        acc.w = __uint_as_float(r.y & 0xFFFF0000u);
+    } else {
+        acc = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(res) +
+                                                (int64_t)t * d + c);
+    }
+    for (int s = 0; s < k; ++s) {
+        const float wv = w[(int64_t)t * k + s];
+        const float *yp = ypart + ((int64_t)(t * k + s) * nslot) * d + c;
+        float4 y = __ldg(reinterpret_cast<const float4 *>(yp));
+        for (int q = 1; q < nslot; ++q) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(yp + (int64_t)q * d));
+            y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+        }
+        acc.x = fmaf(wv, y.x, acc.x);
+        acc.y = fmaf(wv, y.y, acc.y);
+        acc.z = fmaf(wv, y.z, acc.z);
+        acc.w = fmaf(wv, y.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
+}
+
+// One thread per 16-byte packed word.  Packed word (tile g,b; stage s; half h;
+// lane l) byte i <-> canonical code (row 32b+l, chunk 32g+((16h+i+l) mod 32), s).
+__global__ void pack_kernel(const uint8_t *__restrict__ src, int rows, int cols,
+                            uint8_t *__restrict__ dst, int unpack) {
+    const int64_t words = (int64_t)rows * cols * 3 / 128;
+    const int64_t wi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (wi >= words) return;
+    const int RB = rows / 32;
+    const int64_t tile = wi / 192;
+    const int within = (int)(wi % 192);
+    const int sh = within / 32, l = within % 32;
+    const int s = sh >> 1, h = sh & 1;
+    const int g = (int)(tile / RB), b = (int)(tile % RB);
+    const int row = 32 * b + l;
+    const int64_t rowbase = (int64_t)row * (cols / 8);
+    if (!unpack) {
+        uint8_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int chunk = 32 * g + ((16 * h + i + l) & 31);
+            v[i] = src[(rowbase + chunk) * 3 + s];
+        }
+        uint4 o;
+        o.x = v[0] | (v[1] << 8) | (v[2] << 16) | ((uint32_t)v[3] << 24);
+        o.y = v[4] | (v[5] << 8) | (v[6] << 16) | ((uint32_t)v[7] << 24);
+        o.z = v[8] | (v[9] << 8) | (v[10] << 16) | ((uint32_t)v[11] << 24);
+        o.w = v[12] | (v[13] << 8) | (v[14] << 16) | ((uint32_t)v[15] << 24);
+        *reinterpret_cast<uint4 *>(dst + wi * 16) = o;
+    } else {
+        const uint8_t *p = src + wi * 16;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int chunk = 32 * g + ((16 * h + i + l) & 31);
+            dst[(rowbase + chunk) * 3 + s] = p[i];
+        }
+    }
+}
+
+// canonical fp32 [count][3][256][8] -> pair-interleaved [count][3][128][8][2]
+__global__ void pack_codebooks_kernel(const float *__restrict__ src, float *__restrict__ dst,
+                                      int count) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= count * 6144) return;
+    const int mat = i / 6144, r = i % 6144;
+    const int s = r / 2048, k = (r / 8) % 256, dim = r % 8;
+    dst[mat * 6144 + ((s * 128 + k / 2) * 8 + dim) * 2 + (k & 1)] = src[i];
+}
+
+__global__ void write_header_kernel(uint8_t *record, rvq_expert_header h) {
+    if (threadIdx.x == 0) *reinterpret_cast<rvq_expert_header *>(record) = h;
+}
+
+}  // namespace
+
+rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
+                          const void *res, int rdt, float *out, cudaStream_t stream, bool pdl) {
+    const int64_t total = (int64_t)n * (d / 4);
+    if (total == 0) return RVQ_OK;
+    const int bs = 256;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((total + bs - 1) / bs));
+    cfg.blockDim = dim3(bs);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, combine_kernel, ypart, nslot, w, n, k, d, res, rdt, out));
+    return RVQ_OK;
+}
+
+rvq_status launch_pack(const uint8_t *src, int rows, int cols, uint8_t *dst, bool unpack,
+                       cudaStream_t stream) {
+    const int64_t words = (int64_t)rows * cols * 3 / 128;
+    const int bs = 256;
+    pack_kernel<<<(unsigned)((words + bs - 1) / bs), bs, 0, stream>>>(src, rows, cols, dst,
+                                                                       unpack ? 1 : 0);
+    RVQ_LAUNCHED("pack");
+    return RVQ_OK;
+}
+
+rvq_status launch_pack_codebooks(const float *src, float *dst, int count, cudaStream_t stream) {
+    const int total = count * 6144;
+    pack_codebooks_kernel<<<(total + 255) / 256, 256, 0, stream>>>(src, dst, count);
+    RVQ_LAUNCHED("pack_codebooks");
+    return RVQ_OK;
+}
+
+rvq_status launch_write_header(uint8_t *record, const rvq_expert_header &h, cudaStream_t stream) {
+    write_header_kernel<<<1, 32, 0, stream>>>(record, h);
+    RVQ_LAUNCHED("write_header");
+    return RVQ_OK;
+}
+
+}  // namespace rvq

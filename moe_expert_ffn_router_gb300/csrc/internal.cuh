@@ -1,0 +1,154 @@
+// Internal declarations shared by the rvqmoe CUDA translation units.
+// Nothing here is part of the public C ABI (include/rvqmoe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/rvqmoe.h"
+
+namespace rvq {
+
+// ------------------------------------------------------------------ errors
+void set_error(const char *fmt, ...);
+rvq_status cuda_status(cudaError_t e, const char *what);
+#define RVQ_TRY(expr)                              \
+    do {                                           \
+        rvq_status _s = (expr);                    \
+        if (_s != RVQ_OK) return _s;               \
+    } while (0)
+#define RVQ_CUDA(expr)                                             \
+    do {                                                           \
+        cudaError_t _e = (expr);                                   \
+        if (_e != cudaSuccess) return ::rvq::cuda_status(_e, #expr); \
+    } while (0)
+#define RVQ_LAUNCHED(what) RVQ_CUDA(cudaGetLastError())
+
+// ------------------------------------------------------------------ layout
+constexpr int kTileRows = 32;          // rows per tile (one per lane)
+constexpr int kTileChunks = 32;        // chunks per tile (rotation period)
+constexpr int kTileBytes = 3 * 2 * 32 * 16;  // 3072
+constexpr int kLutStageBytes = 65536;  // 256 entries x 256 B per stage
+constexpr int kLutBytes = 3 * kLutStageBytes;
+
+inline bool packable(int32_t rows, int32_t cols) {
+    return rows > 0 && cols > 0 && rows % 32 == 0 && cols % 512 == 0;
+}
+
+// Bank record part offsets (bytes from record start).
+struct RecordLayout {
+    uint64_t cb_off, gate_off, up_off, down_off, record_bytes;
+};
+RecordLayout record_layout(int32_t d, int32_t f);
+
+// ------------------------------------------------------------- device utils
+__device__ __forceinline__ void set_dev_error(uint32_t *status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    // Code bytes are read once per step: skip L1.
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ldg_f4(const void *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+
+// Load 8 consecutive inputs (bf16 or fp32) as fp32.
+__device__ __forceinline__ void load8(const void *base, int dtype, int64_t idx, float v[8]) {
+    if (dtype == RVQ_BF16) {
+        uint4 q = __ldg(reinterpret_cast<const uint4 *>(
+            reinterpret_cast<const __nv_bfloat16 *>(base) + idx));
+        uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+        const float *f = reinterpret_cast<const float *>(base) + idx;
+        float4 a = __ldg(reinterpret_cast<const float4 *>(f));
+        float4 b = __ldg(reinterpret_cast<const float4 *>(f) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ float load1(const void *base, int dtype, int64_t idx) {
+    if (dtype == RVQ_BF16)
+        return __uint_as_float(
+            (uint32_t)reinterpret_cast<const uint16_t *>(base)[idx] << 16);
+    return reinterpret_cast<const float *>(base)[idx];
+}
+
+// ------------------------------------------------------- LUT-GEMV job (host)
+// One launch of the fused lookup-table GEMV over grouped (token, expert)
+// pairs.  See lut_gemv.cu for the item decomposition.
+struct LutJob {
+    const uint8_t *base;       // bank base (NULL for a single matrix)
+    uint64_t record_bytes;     // 0 for a single matrix
+    const uint8_t *codes_ptr;  // single matrix: packed codes
+    const float *cb_ptr;       // single matrix: packed codebooks
+    uint64_t codes_off[2];     // per matrix slot (blockIdx.y)
+    uint64_t cb_off[2];
+    float *part[2];            // partial outputs [entry][nslot][rows]
+    int32_t n_mat;             // 1 or 2 (gate+up)
+    int32_t rows, cols;
+    int32_t G;                 // cols / 256
+    int32_t C;                 // chunk groups per item step run (divides G/2)
+    int32_t S;                 // row splits
+    int32_t E;                 // experts (1 for single matrix)
+    int32_t n_pairs;           // n * k (or n)
+    const void *x;             // input rows
+    int32_t x_dtype;
+    int64_t x_stride;          // elements between input rows
+    int32_t x_div;             // input row = entry / x_div
+    const int32_t *offsets;    // [E+1] (NULL: single group of n_pairs)
+    const int32_t *pairs;      // [n_pairs] (NULL: identity)
+    uint32_t *status;
+    // record header check
+    int32_t check_header;
+    int32_t layer, d, f;
+};
+
+inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
+
+rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl);
+rvq_status launch_lut_build(const float *cb, const void *x, int xdt, int n, int cols,
+                            float *lut, cudaStream_t stream);
+// h[entry][r] = silu(sum_slot gate_part) * sum_slot up_part
+rvq_status launch_swiglu_reduce(const float *gpart, const float *upart, int n_pairs, int nslot,
+                                int rows, float *h, cudaStream_t stream, bool pdl);
+// y[entry][r] = sum_slot part[entry][slot][r]
+rvq_status launch_slot_reduce(const float *part, int n_entries, int nslot, int rows, float *y,
+                              cudaStream_t stream, bool pdl);
+rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
+                          const void *res, int rdt, float *out, cudaStream_t stream, bool pdl);
+rvq_status launch_router_logits(const float *wr, const float *bias, const void *x, int xdt,
+                                int n, int E, int d, float *logits, cudaStream_t stream);
+rvq_status launch_route(const float *logits, int n, int E, int k, int32_t *idx, float *w,
+                        int32_t *offsets, int32_t *pairs, uint32_t *status,
+                        cudaStream_t stream, bool pdl);
+int route_max_tokens(int E);
+rvq_status launch_pack(const uint8_t *src, int rows, int cols, uint8_t *dst, bool unpack,
+                       cudaStream_t stream);
+rvq_status launch_pack_codebooks(const float *src, float *dst, int count, cudaStream_t stream);
+rvq_status launch_write_header(uint8_t *record, const rvq_expert_header &h, cudaStream_t stream);
+
+// FFN plan: how moe_expert_ffn splits its work (host side, deterministic).
+struct FfnPlan {
+    int C_gu, S_gu;   // gate/up: chunk groups per item step run, row splits
+    int C_d, S_d;     // down
+    int nslot_gu, nslot_d;
+    size_t off_gpart, off_upart, off_h, off_dpart, total;
+};
+FfnPlan plan_ffn(int d, int f, int n_pairs, int E);
+int num_sms();
+
+}  // namespace rvq

@@ -1,0 +1,110 @@
+"""Owning wrapper around one MoE layer's device buffers (expert bank, router,
+outputs, workspace).  Marshalling only: every step runs in librvqmoe."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (RVQ_WS_STATUS_BYTES, moe_bank_init, moe_bank_record_bytes, moe_bank_validate,
+               moe_bank_write_expert, moe_combine, moe_expert_ffn, moe_layer_forward,
+               moe_route, moe_router_logits, moe_workspace_bytes, rvq_ws_clear, rvq_ws_status)
+
+
+def _dev(a, device, dtype=None):
+    if isinstance(a, torch.Tensor):
+        return a.to(device=device, dtype=dtype or a.dtype).contiguous()
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(device=device, dtype=dtype or t.dtype)
+
+
+class MoeLayer:
+    """Expert bank of `n_experts` RVQ experts (d hidden, f intermediate) plus a
+    linear router; top-k routing."""
+
+    def __init__(self, n_experts: int, d: int, f: int, k: int, layer: int = 0,
+                 device: str | torch.device = "cuda"):
+        self.E, self.d, self.f, self.k, self.layer = n_experts, d, f, k, layer
+        self.device = torch.device(device)
+        rb = moe_bank_record_bytes(d, f)
+        if rb == 0:
+            raise ValueError(f"d={d}, f={f} must be multiples of 512")
+        self.record_bytes = rb
+        self.buf = torch.empty(rb * n_experts, dtype=torch.uint8, device=self.device)
+        assert self.buf.data_ptr() % 256 == 0
+        self.bank = moe_bank_init(self.buf, n_experts, d, f, layer)
+        self.wr = None
+        self.bias = None
+        self._ws = {}
+
+    # ---------------------------------------------------------------- loading
+    def load_expert(self, e: int, gate_codes, up_codes, down_codes, codebooks):
+        """Canonical codes uint8 [f][d/8][3], [f][d/8][3], [d][f/8][3] and
+        codebooks fp32 [3 matrices][3][256][8] (numpy or tensors)."""
+        dev = self.device
+        g = _dev(gate_codes, dev, torch.uint8)
+        u = _dev(up_codes, dev, torch.uint8)
+        dn = _dev(down_codes, dev, torch.uint8)
+        cb = _dev(codebooks, dev, torch.float32)
+        assert g.numel() == self.f * self.d * 3 // 8 and dn.numel() == self.d * self.f * 3 // 8
+        assert cb.numel() == 3 * 3 * 256 * 8
+        moe_bank_write_expert(self.bank, e, g, u, dn, cb)
+
+    def set_router(self, wr, bias=None):
+        self.wr = _dev(wr, self.device, torch.float32)
+        assert self.wr.shape == (self.E, self.d)
+        self.bias = None if bias is None else _dev(bias, self.device, torch.float32)
+
+    def validate(self):
+        moe_bank_validate(self.bank)
+
+    def record(self, e: int) -> torch.Tensor:
+        return self.buf[e * self.record_bytes:(e + 1) * self.record_bytes]
+
+    # ----------------------------------------------------------------- buffers
+    def workspace(self, n: int) -> torch.Tensor:
+        ws = self._ws.get(n)
+        if ws is None:
+            nbytes = moe_workspace_bytes(self.bank, n, self.k)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            rvq_ws_clear(ws)
+            self._ws[n] = ws
+        return ws
+
+    def buffers(self, n: int) -> dict:
+        dev, E, k = self.device, self.E, self.k
+        return dict(
+            logits=torch.empty((n, E), dtype=torch.float32, device=dev),
+            idx=torch.empty((n, k), dtype=torch.int32, device=dev),
+            w=torch.empty((n, k), dtype=torch.float32, device=dev),
+            offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            pairs=torch.empty(n * k, dtype=torch.int32, device=dev),
+            out=torch.empty((n, self.d), dtype=torch.float32, device=dev),
+            ws=self.workspace(n))
+
+    # ----------------------------------------------------------------- compute
+    def forward(self, x: torch.Tensor, bufs: dict | None = None, events=None) -> dict:
+        """Whole layer (fused path): out = x + sum_slot w * expert(x)."""
+        n = x.shape[0]
+        b = bufs or self.buffers(n)
+        moe_layer_forward(self.bank, self.wr, self.bias, x, n, self.k, b["logits"], b["idx"],
+                          b["w"], b["offsets"], b["pairs"], b["out"], b["ws"], events=events)
+        return b
+
+    def forward_steps(self, x: torch.Tensor) -> dict:
+        """Same layer through the separate calls (router, route, FFN, combine)."""
+        n = x.shape[0]
+        b = self.buffers(n)
+        moe_router_logits(self.wr, self.bias, x, n, self.E, self.d, b["logits"])
+        moe_route(b["logits"], n, self.E, self.k, b["idx"], b["w"], b["offsets"], b["pairs"],
+                  b["ws"])
+        y = torch.empty((n * self.k, self.d), dtype=torch.float32, device=self.device)
+        moe_expert_ffn(self.bank, x, n, self.k, b["offsets"], b["pairs"], y, b["ws"])
+        moe_combine(y, b["w"], n, self.k, self.d, x, b["out"])
+        b["y_pair"] = y
+        return b
+
+    def status(self, n: int) -> tuple[int, int]:
+        return rvq_ws_status(self.workspace(n))
+
+
+__all__ = ["MoeLayer", "RVQ_WS_STATUS_BYTES"]

@@ -1,0 +1,156 @@
+"""GPU parity for whole MoE layers (router -> top-k -> RVQ SwiGLU expert FFN
+-> weighted combine + residual) against the oracle, plus device-side fault
+reporting.  Routing is compared bit-exact with the oracle routing the GPU's
+own fp32 logits; floats within 1e-4 x RMS."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import workloads as W
+from tests.support import SynthLayer, assert_rms_close, bf16_bits_to_f64
+
+pytestmark = pytest.mark.gpu
+rvq = pytest.importorskip("moe_expert_ffn_router_gb300")
+DEV = "cuda"
+
+_layers = {}
+
+
+def layer(config, n_experts=None):
+    key = (config, n_experts)
+    if key not in _layers:
+        sl = SynthLayer(config, 0, n_experts=n_experts)
+        _layers[key] = (sl, sl.to_gpu())
+    return _layers[key]
+
+
+def drop_layers():
+    _layers.clear()
+    torch.cuda.empty_cache()
+
+
+def bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def check_layer(sl, L, x_bits, tokens=None, steps=False):
+    n = x_bits.shape[0]
+    x = bf16_dev(x_bits)
+    b = L.forward_steps(x) if steps else L.forward(x)
+    torch.cuda.synchronize()
+    assert L.status(n) == (0, 0)
+    logits = b["logits"].cpu().numpy()
+    idx, w = b["idx"].cpu().numpy(), b["w"].cpu().numpy()
+    off, pairs = b["offsets"].cpu().numpy(), b["pairs"].cpu().numpy()
+    out = b["out"].cpu().numpy()
+    x64 = bf16_bits_to_f64(x_bits)
+    s = sl.shape
+    # logits against the oracle's own
+    ref_lg = oracle.router_logits(sl.wr, x64)
+    assert_rms_close(logits, ref_lg, 1e-5, "logits")
+    # routing and grouping bit-exact given the GPU's logits
+    ridx, rw, _ = oracle.route(logits, s.k)
+    assert np.array_equal(idx, ridx)
+    np.testing.assert_allclose(w, rw, rtol=2e-6, atol=1e-9)
+    roff, rpairs = oracle.group(ridx, L.E)
+    assert np.array_equal(off, roff) and np.array_equal(pairs, rpairs)
+    # expert outputs and combine on a subset of tokens (all by default)
+    tokens = range(n) if tokens is None else tokens
+    for t in tokens:
+        r = oracle.moe_layer(sl.expert, sl.wr, x64[t:t + 1], s.k, s.d, s.f,
+                             route_logits=logits[t:t + 1])
+        assert np.array_equal(r["idx"][0], idx[t])
+        delta_ref = r["out"][0] - x64[t]
+        assert_rms_close(out[t] - x64[t], delta_ref, 1e-4, f"token {t} out-x")
+        assert_rms_close(out[t], r["out"][0], 1e-4, f"token {t} out")
+        if steps:
+            yp = b["y_pair"].cpu().numpy()[t * s.k:(t + 1) * s.k]
+            assert_rms_close(yp, r["y_pair"], 1e-4, f"token {t} y_pair")
+    return b
+
+
+@pytest.mark.parametrize("n", [1, 4, 16])
+def test_decode_layer_d2048(n):
+    sl, L = layer(1)
+    check_layer(sl, L, sl.tokens_bf16(n))
+
+
+def test_decode_layer_separate_calls():
+    sl, L = layer(1)
+    check_layer(sl, L, sl.tokens_bf16(5), steps=True)
+
+
+def test_repeated_tokens_make_large_groups():
+    """Seven copies of one token and two others: experts with 7-9 tokens
+    (two-token items and an odd remainder) next to single-token experts."""
+    sl, L = layer(1)
+    base = sl.tokens_bf16(3)
+    xb = np.concatenate([np.repeat(base[:1], 7, axis=0), base[1:]])
+    b = check_layer(sl, L, xb, tokens=[0, 6, 7, 8])
+    counts = np.diff(b["offsets"].cpu().numpy())
+    assert counts.max() >= 7
+
+
+def test_fp32_residual_input():
+    """Layer input in fp32 (the residual stream of a stack)."""
+    sl, L = layer(1)
+    n = 3
+    x32 = synth.bf16_to_f32(sl.tokens_bf16(n)) * np.float32(1.37)
+    b = L.forward(torch.from_numpy(x32).to(DEV))
+    torch.cuda.synchronize()
+    assert L.status(n) == (0, 0)
+    logits, out = b["logits"].cpu().numpy(), b["out"].cpu().numpy()
+    for t in range(n):
+        r = oracle.moe_layer(sl.expert, sl.wr, x32[t:t + 1].astype(np.float64), 8, 2048, 1024,
+                             route_logits=logits[t:t + 1])
+        assert_rms_close(out[t] - x32[t], r["out"][0] - x32[t], 1e-4, "fp32 out-x")
+
+
+def test_corrupt_record_is_reported_not_used():
+    sl, L = layer(1)
+    n = 2
+    xb = sl.tokens_bf16(n)
+    b = L.forward(bf16_dev(xb))
+    torch.cuda.synchronize()
+    e = int(b["idx"][0, 0])
+    rec = L.record(e)
+    saved = rec[:4].clone()
+    try:
+        rec[:4] = 0                                    # break the magic of a selected expert
+        with pytest.raises(rvq.RvqError) as ei:
+            L.validate()
+        assert ei.value.status == "RVQ_ECORRUPT"
+        L.forward(bf16_dev(xb))
+        rc, bits = L.status(n)
+        assert bits & rvq.DEV_ERR_CORRUPT and rc == 4
+    finally:
+        rec[:4] = saved
+    L.validate()
+    L.forward(bf16_dev(xb))
+    assert L.status(n) == (0, 0)
+
+
+def test_bad_offsets_are_reported():
+    sl, L = layer(1)
+    n, k = 2, 8
+    x = bf16_dev(sl.tokens_bf16(n))
+    b = L.buffers(n)
+    off = torch.zeros(L.E + 1, dtype=torch.int32, device=DEV)
+    off[-1] = n * k + 5                                # inconsistent total
+    pairs = torch.arange(n * k, dtype=torch.int32, device=DEV)
+    y = torch.empty((n * k, L.d), dtype=torch.float32, device=DEV)
+    rvq.moe_expert_ffn(L.bank, x, n, k, off, pairs, y, b["ws"])
+    rc, bits = L.status(n)
+    assert bits & rvq.DEV_ERR_INDEX and rc == 5
+
+
+@pytest.mark.parametrize("n,sample", [(1, [0]), (8, [0, 5]), (64, [3, 60])])
+def test_k3_shaped_layer_full_size(n, sample):
+    """d=7168, f=2048, 256 experts, top-16, 4.2 GB bank: all outputs of the
+    sampled tokens against the oracle; routing of every token bit-exact."""
+    drop_layers()
+    sl, L = layer(2)
+    check_layer(sl, L, sl.tokens_bf16(n), tokens=sample)
+    sl.forget()
