@@ -141,6 +141,28 @@ rvq_status rvq_gemv(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
                     float *y_dev, void *ws_dev, size_t ws_bytes, rvq_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * rvq_gemv for callers that cannot allocate device memory (for example a
+ * plug-in inside a framework that owns all device memory, or a loop where an
+ * allocation and its implicit synchronisation are not allowed).  The source
+ * pages have no counterpart to this call; it is an addition of this library.
+ * Same operation, arguments, layouts and results as rvq_gemv, without the
+ * workspace: the split-K scratch is a fixed RVQ_NOALLOC_SCRATCH_BYTES device
+ * array inside the library, held by every GPU that loads the library until
+ * the process exits.  Calls no cudaMalloc/cudaFree or allocating routine.
+ *  - Returns RVQ_ENOMEM, launching nothing, when rows x cols x n would need
+ *    more scratch than the fixed maximum (rvq_gemv_workspace_bytes > max).
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - Every call shares the one array: calls whose work overlaps on the GPU
+ *    (other streams, other threads) race and give wrong results; serialise
+ *    them.  Each call clears the status block it needs at the start.
+ * ------------------------------------------------------------------------ */
+#define RVQ_NOALLOC_SCRATCH_BYTES 4194304u /* 4 MiB */
+rvq_status rvq_gemv_noalloc(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
+                            int32_t rows, int32_t cols, const void *x_dev, rvq_dtype xdt,
+                            int32_t n, float *y_dev, rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * Expert bank: n_experts records of record_bytes each, contiguous in HBM.
  * Record = [rvq_expert_header, 128 B][packed codebooks gate, up, down]
  *          [packed codes gate f x d][up f x d][down d x f]; every part starts

@@ -59,6 +59,7 @@ _SIGS = {
     "rvq_lut_build": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "rvq_gemv_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "rvq_gemv": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "rvq_gemv_noalloc": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp]),
     "moe_bank_record_bytes": (_u64, [_i32, _i32]),
     "moe_bank_init": (_i32, [_BANKP, _vp, _u64, _i32, _i32, _i32, _i32]),
     "moe_bank_write_expert": (_i32, [_BANKP, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -168,6 +169,19 @@ def rvq_gemv_workspace_bytes(rows, cols, n) -> int:
 def rvq_gemv(packed_codes, packed_cb, rows, cols, x, n, y, ws, stream=None):
     _check("rvq_gemv", _lib.rvq_gemv(_p(packed_codes), _p(packed_cb), rows, cols, _p(x), _dt(x),
                                      n, _p(y), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+RVQ_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def rvq_gemv_noalloc(packed_codes, packed_cb, rows, cols, x, n, y, stream=None):
+    """rvq_gemv without a workspace, for callers that cannot allocate device
+    memory: the scratch is a fixed 4 MiB array inside the library, shared by
+    all calls (calls that overlap on the GPU race).  Make the first call on a
+    device before any stream capture."""
+    _check("rvq_gemv_noalloc",
+           _lib.rvq_gemv_noalloc(_p(packed_codes), _p(packed_cb), rows, cols, _p(x), _dt(x), n,
+                                 _p(y), _stream(stream)))
 
 
 # ------------------------------------------------------------------ bank
