@@ -35,8 +35,9 @@ from synth import workloads as W  # noqa: E402
 METRIC = "RVQ expert-FFN Gweights/s and code-byte HBM GB/s vs ~8 TB/s peak; layer tok/s"
 UNIT = "Gweights/s"
 WORKLOADS = {
-    # name: (config, batch)
+    # name: (config, batch[, experts in the bank])
     "k3_decode_b1": (2, 1),
+    "k3_decode_b1_e64": (2, 1, 64),   # profiling case: same experts, 1.06 GB bank
     "k3_decode_b8": (2, 8),
     "k3_decode_b64": (2, 64),
     "decode_d2048_b1": (1, 1),
@@ -126,9 +127,18 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- GPU arm
-def build_layer(config, device, k=None):
-    from moe_expert_ffn_router_gb300.layer import MoeLayer
+def workload_shape(name):
+    spec = WORKLOADS[name]
+    config, batch = spec[0], spec[1]
     s = W.WORKLOADS[config].shape
+    if len(spec) > 2:
+        s = W.LayerShape(s.d, s.f, spec[2], s.k)
+    return config, batch, s
+
+
+def build_layer(config, device, k=None, shape=None):
+    from moe_expert_ffn_router_gb300.layer import MoeLayer
+    s = shape or W.WORKLOADS[config].shape
     src = W.ExpertSource(config, 0, s)
     L = MoeLayer(s.E, s.d, s.f, k or s.k, layer=0, device=device)
     for e in range(s.E):
@@ -145,9 +155,8 @@ def run_gpu(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    config, batch = WORKLOADS[args.workload]
-    s = W.WORKLOADS[config].shape
-    L, src = build_layer(config, dev)
+    config, batch, s = workload_shape(args.workload)
+    L, src = build_layer(config, dev, shape=s)
     pool = max(64, 4 * batch)
     pool_bits = src.tokens_bf16(pool * batch if batch > 1 else pool)
     xs = torch.from_numpy(pool_bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -271,12 +280,12 @@ def run_gpu(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_sample(config, batch, tokens, src=None):
+def oracle_sample(config, batch, tokens, src=None, shape=None):
     """Time the oracle (as it stands, one thread) on `tokens` tokens of the
     workload.  Returns (Gweights/s, seconds, weights)."""
     import oracle
     import synth
-    s = W.WORKLOADS[config].shape
+    s = shape or W.WORKLOADS[config].shape
     src = src or W.ExpertSource(config, 0, s)
     wr = src.router_weight()
     x64 = synth.bf16_to_f32(src.tokens_bf16(tokens)).astype(np.float64)
@@ -302,8 +311,7 @@ def reference_arm(args, rank):
         return
     import oracle
     import synth
-    config, batch = WORKLOADS[args.workload]
-    s = W.WORKLOADS[config].shape
+    config, batch, s = workload_shape(args.workload)
     src = W.ExpertSource(config, 0, s)
     per_expert_s = 0.15 * (s.d * s.f) / (7168 * 2048)
     m = int(max(1, min(s.k, 60.0 / ((args.steps + args.warmup) * per_expert_s))))
@@ -330,7 +338,8 @@ def reference_arm(args, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(times / args.steps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": W.WORKLOADS[config].name, "batch": batch},
+            "config": {"workload": args.workload + ":" + W.WORKLOADS[config].name,
+                       "batch": batch, "experts": s.E},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
                              "kind": "oracle",
                              "sample": f"{m} of the {s.k} experts one token selects per step "
@@ -348,6 +357,8 @@ def main():
     ap.add_argument("--workload", default="k3_decode_b1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--oracle-tokens", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -366,8 +377,9 @@ def main():
     if rank == 0:
         s = r["shape"]
         cpu = None
-        if world == 1 or rank == 0:
-            v, dt, wts = oracle_sample(r["config"], r["batch"], args.oracle_tokens)
+        if not args.no_cpu_baseline:
+            v, dt, wts = oracle_sample(r["config"], r["batch"], args.oracle_tokens,
+                                       shape=r["shape"])
             cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{args.oracle_tokens} tokens through the whole oracle layer "
                              f"({wts / 1e9:.2f} G weights, {dt:.1f} s)"}
@@ -376,12 +388,12 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": W.WORKLOADS[r["config"]].name, "batch": r["batch"],
+            "config": {"workload": args.workload + ":" + W.WORKLOADS[r["config"]].name,
+                       "batch": r["batch"],
                        "d": s.d, "f": s.f, "experts": s.E, "top_k": s.k,
                        "codes_bytes": 3 * (3 * s.d * s.f // 8) * s.E,
-                       "l2": "inputs larger than L2: 4.23 GB code bank, token pool rotates "
-                             "routing every step" if r["config"] == 2 else
-                             "bank 151 MB; token pool rotates routing every step",
+                       "l2": f"inputs larger than L2: {3 * (3 * s.d * s.f // 8) * s.E / 1e9:.2f} "
+                             "GB code bank (L2 129 MB); token pool rotates routing every step",
                        "parallelism": f"replicas{world}"},
             "code_byte_gbs": round(r["code_gbs"], 1),
             "layer_tok_s": round(r["tok_s"], 1),

@@ -71,6 +71,7 @@ static void choose_split(int rows, int cols, int n_pairs, int n_mat, int E, int 
             if (RB % S) continue;
             const int rs = rows / S;
             if (rs > 2048) continue;
+            if (C > 1 && rs > 1024) continue;
             if (rs < 256 && S > 1) continue;
             const double items = (double)(G / (2 * C)) * n_pairs * S * n_mat;
             const double waves = ceil(items / sms);

@@ -7,17 +7,36 @@ namespace {
 
 // out[t][c] = res[t][c] + sum_slot w[t][slot] * sum_s ypart[(t*k+slot)*nslot + s][c]
 // (reading: the pages do not describe the combine; this is the standard MoE
-// output with the routing weights).  Four columns per thread, 128-bit loads.
+// output with the routing weights).  Block = 16 column quads x k slots: each
+// thread reduces one slot's split-K partials for four columns (128-bit
+// loads), then the slot products are added to the residual in slot order.
+constexpr int CB_Q = 16;  // column quads per block
+
 __global__ void combine_kernel(const float *__restrict__ ypart, int nslot,
                                const float *__restrict__ w, int n, int k, int d,
                                const void *res, int rdt, float *out) {
+    __shared__ float4 prod[32][CB_Q];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int d4 = d >> 2;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)n * d4) return;
-    const int t = (int)(i / d4);
-    const int c = (int)(i % d4) * 4;
+    const int qx = threadIdx.x, slot = threadIdx.y;
+    const int t = blockIdx.y;
+    const int c4 = blockIdx.x * CB_Q + qx;
+    if (c4 < d4) {
+        const float wv = w[(int64_t)t * k + slot];
+        const float4 *yp = reinterpret_cast<const float4 *>(
+            ypart + ((int64_t)(t * k + slot) * nslot) * d) + c4;
+        float4 y = __ldg(yp);
+#pragma unroll 4
+        for (int q = 1; q < nslot; ++q) {
+            const float4 v = __ldg(yp + (int64_t)q * d4);
+            y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+        }
+        prod[slot][qx] = make_float4(wv * y.x, wv * y.y, wv * y.z, wv * y.w);
+    }
+    __syncthreads();
+    if (slot != 0 || c4 >= d4) return;
+    const int c = c4 * 4;
     float4 acc;
     if (rdt == RVQ_BF16) {
         const uint2 r = *reinterpret_cast<const uint2 *>(
@@ -31,17 +50,8 @@ __global__ void combine_kernel(const float *__restrict__ ypart, int nslot,
                                                 (int64_t)t * d + c);
     }
     for (int s = 0; s < k; ++s) {
-        const float wv = w[(int64_t)t * k + s];
-        const float *yp = ypart + ((int64_t)(t * k + s) * nslot) * d + c;
-        float4 y = __ldg(reinterpret_cast<const float4 *>(yp));
-        for (int q = 1; q < nslot; ++q) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(yp + (int64_t)q * d));
-            y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
-        }
-        acc.x = fmaf(wv, y.x, acc.x);
-        acc.y = fmaf(wv, y.y, acc.y);
-        acc.z = fmaf(wv, y.z, acc.z);
-        acc.w = fmaf(wv, y.w, acc.w);
+        const float4 v = prod[s][qx];
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
 }
@@ -102,12 +112,14 @@ __global__ void write_header_kernel(uint8_t *record, rvq_expert_header h) {
 
 rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
                           const void *res, int rdt, float *out, cudaStream_t stream, bool pdl) {
-    const int64_t total = (int64_t)n * (d / 4);
-    if (total == 0) return RVQ_OK;
-    const int bs = 256;
+    if (n == 0) return RVQ_OK;
+    if (k > 32) {
+        set_error("combine: k %d > 32", k);
+        return RVQ_EINVAL;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((total + bs - 1) / bs));
-    cfg.blockDim = dim3(bs);
+    cfg.gridDim = dim3((unsigned)((d / 4 + CB_Q - 1) / CB_Q), (unsigned)n);
+    cfg.blockDim = dim3(CB_Q, (unsigned)k);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

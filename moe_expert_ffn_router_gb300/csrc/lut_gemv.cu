@@ -33,9 +33,11 @@
 namespace rvq {
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 512;
 constexpr int NW = NT / 32;
-constexpr int kMaxSplitRows = 2048;  // shared accumulator: 2048 x float2 = 16 KiB
+constexpr int kMaxSplitRows = 2048;  // rows per item: at most 8 row blocks per warp
+constexpr int kMaxAccRows = 1024;    // rows per item when C > 1 (shared accumulator)
+constexpr int kCbBytes = 3 * 128 * 8 * 2 * 4;  // packed codebook of one matrix, 24 KiB
 
 struct Item {
     int valid;
@@ -76,74 +78,108 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t x, uint64_t y, uint64_t acc) 
     return r;
 }
 
-__device__ int segment_of(const int32_t *offsets, int E, int p) {
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (offsets[mid] <= p) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-// Decode blockIdx into an item (thread 0 only).
+// Decode blockIdx into an item, with the whole of warp 0 (all 32 lanes call
+// it; lane 0 writes `it`).  The expert segment holding pair position p is
+// found with one parallel read of offsets[0..E] (9 per lane) and a ballot;
+// the two pair entries and the record header are then read in parallel: two
+// dependent memory round trips per item.
 __device__ void decode_item(const LutJob &job, int m, Item &it) {
-    it.valid = 0;
+    const int lane = threadIdx.x & 31;
     const int per_pair = job.G / (2 * job.C);
     const int i = blockIdx.x / job.S;
     const int split = blockIdx.x % job.S;
     const int p = i / per_pair;
-    if (p >= job.n_pairs) return;
+    bool ok = p < job.n_pairs;
     int e = 0, o = 0, ne = job.n_pairs;
-    if (job.offsets) {
-        if (job.offsets[0] != 0 || job.offsets[job.E] != job.n_pairs) {
-            set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
-            return;
+    if (ok && job.offsets) {
+        int off[9];
+#pragma unroll
+        for (int q = 0; q < 9; ++q) {
+            const int x = lane * 9 + q;
+            off[q] = x <= job.E ? job.offsets[x] : 0x7fffffff;
         }
-        e = segment_of(job.offsets, job.E, p);
-        o = job.offsets[e];
-        ne = job.offsets[e + 1] - o;
-        if (!(0 <= o && o <= p && p < o + ne && o + ne <= job.n_pairs)) {
-            set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
-            return;
+        const int next_first = __shfl_down_sync(0xffffffffu, off[0], 1);
+        int found = -1, fo = 0, fhi = 0;
+#pragma unroll
+        for (int q = 0; q < 9; ++q) {
+            const int x = lane * 9 + q;
+            const int hi = q < 8 ? off[q + 1] : (lane < 31 ? next_first : 0x7fffffff);
+            if (found < 0 && x < job.E && off[q] <= p && p < hi) {
+                found = x;
+                fo = off[q];
+                fhi = hi;
+            }
         }
+        // offsets[0] sits in lane 0, offsets[E] in lane E / 9
+        const int o0 = __shfl_sync(0xffffffffu, off[0], 0);
+        int oE = 0;
+#pragma unroll
+        for (int q = 0; q < 9; ++q)
+            if (lane * 9 + q == job.E) oE = off[q];
+        oE = __shfl_sync(0xffffffffu, oE, job.E / 9);
+        const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+        if (o0 != 0 || oE != job.n_pairs || hit == 0) {
+            ok = false;
+        } else {
+            const int src = __ffs(hit) - 1;
+            e = __shfl_sync(0xffffffffu, found, src);
+            o = __shfl_sync(0xffffffffu, fo, src);
+            ne = __shfl_sync(0xffffffffu, fhi, src) - o;
+            ok = 0 <= o && o <= p && p < o + ne && o + ne <= job.n_pairs;
+        }
+        if (!ok && lane == 0) set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
     }
-    const uint8_t *rec = job.base ? job.base + (uint64_t)e * job.record_bytes : nullptr;
-    if (job.check_header && rec) {
-        const rvq_expert_header *h = reinterpret_cast<const rvq_expert_header *>(rec);
-        if (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
-            h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes) {
-            set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
-            return;
-        }
+    if (!ok) {
+        if (lane == 0) it.valid = 0;
+        return;
     }
     const int li = i - per_pair * o;
     const int Q = ne >> 1;
     const int runs = job.G / job.C;  // chunk-group runs of the two-token items
-    int tauA, tauB;
+    int type, tauA, tauB, g0, slotA, slotB;
     if (li < Q * runs) {
         const int gr = li / Q, q = li % Q;
-        it.type = 0;
+        type = 0;
         tauA = 2 * q;
         tauB = 2 * q + 1;
-        it.g0 = gr * job.C;
-        it.slotA = it.slotB = gr;
+        g0 = gr * job.C;
+        slotA = slotB = gr;
     } else {
         const int l2 = li - Q * runs;
-        it.type = 1;
+        type = 1;
         tauA = tauB = ne - 1;
-        it.g0 = l2 * 2 * job.C;
-        it.slotA = 2 * l2;
-        it.slotB = 2 * l2 + 1;
+        g0 = l2 * 2 * job.C;
+        slotA = 2 * l2;
+        slotB = 2 * l2 + 1;
     }
-    int eA = o + tauA, eB = o + tauB;
-    if (job.pairs) {
-        eA = job.pairs[eA];
-        eB = job.pairs[eB];
+    const uint8_t *rec = job.base ? job.base + (uint64_t)e * job.record_bytes : nullptr;
+    // parallel reads: lane 0 / 1 the pair entries, lane 2 the header words
+    int v = 0;
+    if (lane == 0) v = job.pairs ? job.pairs[o + tauA] : o + tauA;
+    if (lane == 1) v = job.pairs ? job.pairs[o + tauB] : o + tauB;
+    bool hdr_ok = true;
+    if (lane == 2 && job.check_header && rec) {
+        const rvq_expert_header *h = reinterpret_cast<const rvq_expert_header *>(rec);
+        hdr_ok = h->magic == RVQ_BANK_MAGIC && h->expert == e && h->layer == job.layer &&
+                 h->d == job.d && h->f == job.f && h->record_bytes == job.record_bytes;
+    }
+    const int eA = __shfl_sync(0xffffffffu, v, 0);
+    const int eB = __shfl_sync(0xffffffffu, v, 1);
+    hdr_ok = __shfl_sync(0xffffffffu, hdr_ok ? 1 : 0, 2) != 0;
+    if (lane != 0) return;
+    it.valid = 0;
+    if (!hdr_ok) {
+        set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
+        return;
     }
     if (eA < 0 || eA >= job.n_pairs || eB < 0 || eB >= job.n_pairs) {
         set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
         return;
     }
+    it.type = type;
+    it.g0 = g0;
+    it.slotA = slotA;
+    it.slotB = slotB;
     it.entryA = eA;
     it.entryB = eB;
     if (job.record_bytes) {
@@ -153,10 +189,9 @@ __device__ void decode_item(const LutJob &job, int m, Item &it) {
         it.codes = job.codes_ptr;
         it.cb = job.cb_ptr;
     }
-    it.xA = reinterpret_cast<const uint8_t *>(job.x) +
-            (int64_t)(eA / job.x_div) * job.x_stride * (job.x_dtype == RVQ_BF16 ? 2 : 4);
-    it.xB = reinterpret_cast<const uint8_t *>(job.x) +
-            (int64_t)(eB / job.x_div) * job.x_stride * (job.x_dtype == RVQ_BF16 ? 2 : 4);
+    const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
+    it.xA = reinterpret_cast<const uint8_t *>(job.x) + (int64_t)(eA / job.x_div) * job.x_stride * esz;
+    it.xB = reinterpret_cast<const uint8_t *>(job.x) + (int64_t)(eB / job.x_div) * job.x_stride * esz;
     const int RB = job.rows / 32;
     it.nrb = RB / job.S;
     it.rb0 = split * it.nrb;
@@ -167,7 +202,7 @@ __device__ void decode_item(const LutJob &job, int m, Item &it) {
 // tokens (T[s][k][c][u], 8-byte pairs); type 1 keeps the two chunk groups in
 // separate 128-byte halves (T[s][k][u][c]).  Two entries (k, k+1) per packed
 // FMA, using the pair-interleaved codebook.
-__device__ __forceinline__ void build_table(uint8_t *lut, const float *cb, const float xa[8],
+__device__ __forceinline__ void build_table(uint8_t *lut, const uint8_t *cb_s, const float xa[8],
                                             const float xb[8], int type, int lane, int warp) {
     uint64_t xa2[8], xb2[8];
 #pragma unroll
@@ -175,15 +210,16 @@ __device__ __forceinline__ void build_table(uint8_t *lut, const float *cb, const
         xa2[i] = pk2(xa[i], xa[i]);
         xb2[i] = pk2(xb[i], xb[i]);
     }
-    const ulonglong2 *cb2 = reinterpret_cast<const ulonglong2 *>(cb);
-#pragma unroll 2
+    const ulonglong2 *cb2 = reinterpret_cast<const ulonglong2 *>(cb_s);
+#pragma unroll 4
     for (int kp = warp; kp < 3 * 128; kp += NW) {
         const int s = kp >> 7, k = (kp & 127) * 2;
-        // 16 floats: (k, k+1) interleaved for dims 0..7
-        ulonglong2 c0 = __ldg(cb2 + kp * 4 + 0);
-        ulonglong2 c1 = __ldg(cb2 + kp * 4 + 1);
-        ulonglong2 c2 = __ldg(cb2 + kp * 4 + 2);
-        ulonglong2 c3 = __ldg(cb2 + kp * 4 + 3);
+        // 16 floats: (k, k+1) interleaved for dims 0..7 (same address in every
+        // lane: shared-memory broadcast)
+        const ulonglong2 c0 = cb2[kp * 4 + 0];
+        const ulonglong2 c1 = cb2[kp * 4 + 1];
+        const ulonglong2 c2 = cb2[kp * 4 + 2];
+        const ulonglong2 c3 = cb2[kp * 4 + 3];
         const uint64_t cw[8] = {c0.x, c0.y, c1.x, c1.y, c2.x, c2.y, c3.x, c3.y};
         uint64_t ta = 0, tb = 0;
 #pragma unroll
@@ -206,18 +242,18 @@ __device__ __forceinline__ void build_table(uint8_t *lut, const float *cb, const
     }
 }
 
-__device__ __forceinline__ void load_tile(uint4 (&c)[6], const uint8_t *tile) {
-#pragma unroll
-    for (int q = 0; q < 6; ++q) c[q] = ldg_stream(tile + q * 512);
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-// Two tokens, one chunk group: one permute + one 8-byte LDS per code byte.
-__device__ __forceinline__ uint64_t rows_pair(const uint4 (&c)[6], const uint32_t (&aux)[32],
-                                              const uint8_t *lut) {
+// One 32-row x 32-chunk code tile (6 words of 16 B per lane) against the
+// table.  Two tokens (TYPE 0): one permute + one 8-byte LDS per code byte
+// gives both tokens' entries.  One token (TYPE 1): one permute + one 4-byte LDS
+// per code byte, two lookups per packed add.  aux[t] carries the lane's
+// rotated column offset (and, for TYPE 1, the table half) in bits 0..7.
+template <int TYPE>
+__device__ __forceinline__ uint64_t tile_lookups(const uint4 (&c)[6], const uint32_t (&aux)[32],
+                                                 const uint8_t *lut) {
     uint64_t acc = 0;
 #pragma unroll
     for (int s = 0; s < 3; ++s)
@@ -226,107 +262,133 @@ __device__ __forceinline__ uint64_t rows_pair(const uint4 (&c)[6], const uint32_
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t w = word_of(c[s * 2 + h], q);
+                if constexpr (TYPE == 0) {
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const uint32_t idx = prmt(w, aux[h * 16 + q * 4 + b], 0x7604u | (b << 4));
-                    const uint64_t v =
-                        *reinterpret_cast<const uint64_t *>(lut + s * kLutStageBytes + idx);
-                    acc = fadd2(acc, v);
+                    for (int b = 0; b < 4; ++b) {
+                        const uint32_t idx = prmt(w, aux[h * 16 + q * 4 + b], 0x7604u | (b << 4));
+                        acc = fadd2(acc, *reinterpret_cast<const uint64_t *>(
+                                             lut + s * kLutStageBytes + idx));
+                    }
+                } else {
+#pragma unroll
+                    for (int b = 0; b < 4; b += 2) {
+                        const uint32_t i0 = prmt(w, aux[h * 16 + q * 4 + b], 0x7604u | (b << 4));
+                        const uint32_t i1 =
+                            prmt(w, aux[h * 16 + q * 4 + b + 1], 0x7604u | ((b + 1) << 4));
+                        const float v0 = *reinterpret_cast<const float *>(lut + s * kLutStageBytes + i0);
+                        const float v1 = *reinterpret_cast<const float *>(lut + s * kLutStageBytes + i1);
+                        acc = fadd2(acc, pk2(v0, v1));
+                    }
                 }
             }
     return acc;
 }
 
-// One token, two chunk groups: two permutes + two 4-byte LDS per code pair.
-__device__ __forceinline__ uint64_t rows_single(const uint4 (&ca)[6], const uint4 (&cb)[6],
-                                                const uint32_t (&aux)[32], const uint8_t *lut) {
-    uint64_t acc = 0;
-#pragma unroll
-    for (int s = 0; s < 3; ++s)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t wa = word_of(ca[s * 2 + h], q);
-                const uint32_t wb = word_of(cb[s * 2 + h], q);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const uint32_t a = aux[h * 16 + q * 4 + b];
-                    const uint32_t ia = prmt(wa, a, 0x7604u | (b << 4));
-                    const uint32_t ib = prmt(wb, a, 0x7604u | (b << 4));
-                    const float va =
-                        *reinterpret_cast<const float *>(lut + s * kLutStageBytes + ia);
-                    const float vb =
-                        *reinterpret_cast<const float *>(lut + s * kLutStageBytes + 128 + ib);
-                    acc = fadd2(acc, pk2(va, vb));
-                }
-            }
-    return acc;
-}
-
+// Streams the item's code tiles through a 2-deep register ring.  Work unit =
+// one code tile: TYPE 0 has one tile per row block (both tokens), TYPE 1 two
+// (groups A and B, each against its own table half).  With 16 warps a warp's
+// tiles are q = warp + 16 i; for TYPE 1 the table half is warp & 1.  The first
+// tiles of a step are requested before its table is built, so the build
+// overlaps HBM traffic; tile i + D is requested once tile i is consumed.
 template <int TYPE>
 __device__ __forceinline__ void run_item(const LutJob &job, const Item &it, int m, uint8_t *lut,
-                                         float2 *sacc) {
+                                         uint8_t *cb_s, float *sacc) {
+    constexpr int D = 2;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int RB = job.rows / 32;
     const int C = job.C;
-    const int nrb_w = (it.nrb - warp + NW - 1) / NW;  // may be 0
+    const int ntiles = TYPE == 0 ? it.nrb : 2 * it.nrb;
+    const int nt_w = (ntiles - warp + NW - 1) / NW;  // tiles of this warp (may be 0)
     const int nslot = job.G / C;
+    const int rows_split = it.nrb * 32;
     float *part = job.part[m];
+    const int gstep = TYPE == 0 ? 1 : 2;
+    const int u = TYPE == 0 ? 0 : (warp & 1);  // table half / unit of this warp (TYPE 1)
 
     uint32_t aux[32];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) aux[t] = ((lane + t) & 31) << (TYPE == 0 ? 3 : 2);
+    for (int t = 0; t < 32; ++t)
+        aux[t] = TYPE == 0 ? (((lane + t) & 31) << 3) : ((((lane + t) & 31) << 2) | (u << 7));
 
-    auto tile_ptr = [&](int g, int rb) {
-        return it.codes + ((size_t)g * RB + rb) * kTileBytes + lane * 16;
+    auto tile_rb = [&](int i) {  // row block of this warp's i-th tile
+        const int q = warp + NW * i;
+        return it.rb0 + (TYPE == 0 ? q : (q >> 1));
     };
-    const int gstep = TYPE == 0 ? 1 : 2;
+    uint4 buf[D][6];
+    auto load_tile = [&](uint4 (&b)[6], int gA, int i) {
+        const int g = gA + u;
+        const uint8_t *p = it.codes + ((size_t)g * RB + tile_rb(i)) * kTileBytes + lane * 16;
+#pragma unroll
+        for (int q = 0; q < 6; ++q) b[q] = ldg_stream(p + q * 512);
+    };
 
-    uint4 curA[6], curB[6], nxtA[6], nxtB[6];
-    if (nrb_w > 0) {
-        load_tile(curA, tile_ptr(it.g0, it.rb0 + warp));
-        if (TYPE == 1) load_tile(curB, tile_ptr(it.g0 + 1, it.rb0 + warp));
+    // item prologue: first tiles in flight, then the matrix's codebook into
+    // shared memory (one coalesced 24 KiB copy per item)
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+        if (d < nt_w) load_tile(buf[d], it.g0, d);
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(it.cb);
+        uint4 *dst = reinterpret_cast<uint4 *>(cb_s);
+        uint4 v[kCbBytes / 16 / NT];
+#pragma unroll
+        for (int q = 0; q < kCbBytes / 16 / NT; ++q) v[q] = __ldg(src + threadIdx.x + NT * q);
+#pragma unroll
+        for (int q = 0; q < kCbBytes / 16 / NT; ++q) dst[threadIdx.x + NT * q] = v[q];
     }
     for (int j = 0; j < C; ++j) {
         const int gA = it.g0 + j * gstep, gB = gA + (TYPE == 0 ? 0 : 1);
+        if (j > 0) {
+#pragma unroll
+            for (int d = 0; d < D; ++d)
+                if (d < nt_w) load_tile(buf[d], gA, d);
+        }
         float xa[8], xb[8];
         load8(it.xA, job.x_dtype, (int64_t)(gA * 32 + lane) * 8, xa);
         load8(it.xB, job.x_dtype, (int64_t)(gB * 32 + lane) * 8, xb);
-        if (j > 0) __syncthreads();
-        build_table(lut, it.cb, xa, xb, TYPE, lane, warp);
+        __syncthreads();  // codebook stored (j = 0) / previous step's lookups done (j > 0)
+        build_table(lut, cb_s, xa, xb, TYPE, lane, warp);
         __syncthreads();
-        for (int i = 0; i < nrb_w; ++i) {
-            const int rb = it.rb0 + warp + NW * i;
-            // prefetch the next row block (possibly of the next step)
-            int jn = j, in = i + 1;
-            if (in >= nrb_w) { jn = j + 1; in = 0; }
-            if (jn < C) {
-                const int gnA = it.g0 + jn * gstep;
-                const int rbn = it.rb0 + warp + NW * in;
-                load_tile(nxtA, tile_ptr(gnA, rbn));
-                if (TYPE == 1) load_tile(nxtB, tile_ptr(gnA + 1, rbn));
-            }
-            uint64_t acc = TYPE == 0 ? rows_pair(curA, aux, lut) : rows_single(curA, curB, aux, lut);
-            float2 a = upk2(acc);
-            const int rl = (rb - it.rb0) * 32 + lane;
-            if (C > 1) {
-                if (j > 0) {
-                    const float2 prev = sacc[rl];
-                    a.x += prev.x;
-                    a.y += prev.y;
-                }
-                if (j < C - 1) sacc[rl] = a;
-            }
-            if (j == C - 1) {
-                const int row = rb * 32 + lane;
-                part[((size_t)it.entryA * nslot + it.slotA) * job.rows + row] = a.x;
-                part[((size_t)it.entryB * nslot + it.slotB) * job.rows + row] = a.y;
-            }
+        for (int i0 = 0; i0 < nt_w; i0 += D) {
 #pragma unroll
-            for (int q = 0; q < 6; ++q) {
-                curA[q] = nxtA[q];
-                if (TYPE == 1) curB[q] = nxtB[q];
+            for (int d = 0; d < D; ++d) {
+                const int i = i0 + d;
+                if (i < nt_w) {
+                    const uint64_t acc = tile_lookups<TYPE>(buf[d], aux, lut);
+                    if (i + D < nt_w) load_tile(buf[d], gA, i + D);
+                    const int rb = tile_rb(i);
+                    const int rl = (rb - it.rb0) * 32 + lane;
+                    const int row = rb * 32 + lane;
+                    float2 a = upk2(acc);
+                    if constexpr (TYPE == 1) {
+                        // one token: both halves of the packed sum belong to this unit
+                        float v = a.x + a.y;
+                        if (C > 1) {
+                            if (j > 0) v += sacc[u * rows_split + rl];
+                            if (j < C - 1) sacc[u * rows_split + rl] = v;
+                        }
+                        if (j == C - 1) {
+                            const int e = u ? it.entryB : it.entryA;
+                            const int sl = u ? it.slotB : it.slotA;
+                            part[((size_t)e * nslot + sl) * job.rows + row] = v;
+                        }
+                    } else {
+                        if (C > 1) {
+                            if (j > 0) {
+                                a.x += sacc[rl];
+                                a.y += sacc[rows_split + rl];
+                            }
+                            if (j < C - 1) {
+                                sacc[rl] = a.x;
+                                sacc[rows_split + rl] = a.y;
+                            }
+                        }
+                        if (j == C - 1) {
+                            part[((size_t)it.entryA * nslot + it.slotA) * job.rows + row] = a.x;
+                            part[((size_t)it.entryB * nslot + it.slotB) * job.rows + row] = a.y;
+                        }
+                    }
+                }
             }
         }
     }
@@ -337,35 +399,64 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_kernel(const LutJob job) {
     __shared__ Item it;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int m = blockIdx.y;
-    if (threadIdx.x == 0) decode_item(job, m, it);
+    if (threadIdx.x < 32) decode_item(job, m, it);
     __syncthreads();
     if (!it.valid) return;
     asm volatile("griddepcontrol.launch_dependents;");
-    float2 *sacc = reinterpret_cast<float2 *>(smem + kLutBytes);
+    uint8_t *cb_s = smem + kLutBytes;
+    float *sacc = reinterpret_cast<float *>(cb_s + kCbBytes);
     if (it.type == 0)
-        run_item<0>(job, it, m, smem, sacc);
+        run_item<0>(job, it, m, smem, cb_s, sacc);
     else
-        run_item<1>(job, it, m, smem, sacc);
+        run_item<1>(job, it, m, smem, cb_s, sacc);
 }
 
 // ---------------------------------------------------------------- reductions
 
-__global__ void swiglu_reduce_kernel(const float *__restrict__ gpart,
-                                     const float *__restrict__ upart, int n_pairs, int nslot,
-                                     int rows, float *__restrict__ h) {
+// h[p][r..r+3] = silu(sum_s g) * sum_s u over the split-K slots.  Four
+// adjacent lanes share one float4 of rows and take every fourth slot; two
+// xor-shuffles combine their sums (a fixed order, so results are repeatable).
+__global__ void __launch_bounds__(256) swiglu_reduce_kernel(const float *__restrict__ gpart,
+                                                            const float *__restrict__ upart,
+                                                            int n_pairs, int nslot, int rows,
+                                                            float *__restrict__ h) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)n_pairs * rows) return;
-    const int64_t p = i / rows, r = i % rows;
-    const float *gp = gpart + p * nslot * rows + r;
-    const float *up = upart + p * nslot * rows + r;
-    float g = 0.f, u = 0.f;
-    for (int s = 0; s < nslot; ++s) {
-        g += gp[(int64_t)s * rows];
-        u += up[(int64_t)s * rows];
+    const int r4 = rows >> 2;
+    const int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int j = (int)(gi & 3);
+    const int64_t i = gi >> 2;
+    const bool valid = i < (int64_t)n_pairs * r4;
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    if (valid) {
+        const int64_t p = i / r4, r = (i % r4) * 4;
+        const float4 *gp = reinterpret_cast<const float4 *>(gpart + p * nslot * rows + r);
+        const float4 *up = reinterpret_cast<const float4 *>(upart + p * nslot * rows + r);
+#pragma unroll 4
+        for (int s = j; s < nslot; s += 4) {
+            const float4 a = __ldg(gp + (int64_t)s * r4), b = __ldg(up + (int64_t)s * r4);
+            g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+            u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+        }
     }
-    h[i] = g / (1.0f + expf(-g)) * u;
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        g.x += __shfl_xor_sync(0xffffffffu, g.x, o);
+        g.y += __shfl_xor_sync(0xffffffffu, g.y, o);
+        g.z += __shfl_xor_sync(0xffffffffu, g.z, o);
+        g.w += __shfl_xor_sync(0xffffffffu, g.w, o);
+        u.x += __shfl_xor_sync(0xffffffffu, u.x, o);
+        u.y += __shfl_xor_sync(0xffffffffu, u.y, o);
+        u.z += __shfl_xor_sync(0xffffffffu, u.z, o);
+        u.w += __shfl_xor_sync(0xffffffffu, u.w, o);
+    }
+    if (!valid || j != 0) return;
+    float4 o;
+    o.x = g.x / (1.0f + expf(-g.x)) * u.x;
+    o.y = g.y / (1.0f + expf(-g.y)) * u.y;
+    o.z = g.z / (1.0f + expf(-g.z)) * u.z;
+    o.w = g.w / (1.0f + expf(-g.w)) * u.w;
+    reinterpret_cast<float4 *>(h)[i] = o;
 }
 
 __global__ void slot_reduce_kernel(const float *__restrict__ part, int64_t n_entries, int nslot,
@@ -424,13 +515,14 @@ rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl) {
     static int attr_done[64] = {0};
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
-    const size_t smem = kLutBytes + (size_t)kMaxSplitRows * sizeof(float2);
+    const size_t smem = kLutBytes + kCbBytes + (size_t)kMaxAccRows * 2 * sizeof(float);
     if (dev < 64 && !attr_done[dev]) {
         RVQ_CUDA(cudaFuncSetAttribute(lut_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
         attr_done[dev] = 1;
     }
-    if (job.rows / job.S > kMaxSplitRows || (job.rows / 32) % job.S != 0 ||
+    if (job.rows / job.S > kMaxSplitRows || (job.C > 1 && job.rows / job.S > kMaxAccRows) ||
+        (job.rows / 32) % job.S != 0 ||
         job.G % (2 * job.C) != 0) {
         set_error("lut_gemv: bad split (rows %d, S %d, G %d, C %d)", job.rows, job.S, job.G,
                   job.C);
@@ -445,7 +537,7 @@ rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl) {
 
 rvq_status launch_swiglu_reduce(const float *gpart, const float *upart, int n_pairs, int nslot,
                                 int rows, float *h, cudaStream_t stream, bool pdl) {
-    const int64_t total = (int64_t)n_pairs * rows;
+    const int64_t total = (int64_t)n_pairs * (rows / 4) * 4;
     if (total == 0) return RVQ_OK;
     const int bs = 256;
     RVQ_CUDA(launch_ex(swiglu_reduce_kernel, dim3((unsigned)((total + bs - 1) / bs)), dim3(bs), 0,
