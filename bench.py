@@ -44,8 +44,8 @@ WORKLOADS = {
     "decode_d2048_b4": (1, 4),
     "decode_d2048_b16": (1, 16),
 }
-KERNELS = ["router_logits", "route", "lut_gemv_gate_up", "swiglu_reduce", "lut_gemv_down",
-           "combine"]
+KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
+           "lut_gemv_down", "combine"]
 DOMINANT = "lut_gemv_gate_up"
 
 

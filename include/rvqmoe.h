@@ -267,7 +267,7 @@ rvq_status moe_combine(const float *y_pair_dev, const float *topk_w_dev, int32_t
  * ws >= moe_workspace_bytes(bank, n, k).  If `events` is not NULL it must
  * hold MOE_LAYER_EVENTS cudaEvent_t handles, recorded on `stream` before
  * the first kernel and after each kernel (for per-kernel timing). */
-#define MOE_LAYER_EVENTS 7
+#define MOE_LAYER_EVENTS 8
 rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, const float *bias_dev,
                              const void *x_dev, rvq_dtype xdt, int32_t n, int32_t k,
                              float *logits_dev, int32_t *topk_idx_dev, float *topk_w_dev,

@@ -71,7 +71,7 @@ static void choose_split(int rows, int cols, int n_pairs, int n_mat, int E, int 
             if (RB % S) continue;
             const int rs = rows / S;
             if (rs > 2048) continue;
-            if (C > 1 && rs > 1024) continue;
+            if (C > 1 && rs > 512) continue;  // shared accumulator limit
             if (rs < 256 && S > 1) continue;
             const double items = (double)(G / (2 * C)) * n_pairs * S * n_mat;
             const double waves = ceil(items / sms);
@@ -104,6 +104,10 @@ FfnPlan plan_ffn(int d, int f, int n_pairs, int E) {
     off = align256(off + (size_t)n_pairs * f * 4);
     P.off_dpart = off;
     off = align256(off + (size_t)n_pairs * P.nslot_d * d * 4);
+    P.off_desc_gu = off;
+    off = align256(off + (size_t)((d / 256) / (2 * P.C_gu)) * n_pairs * sizeof(ItemDesc));
+    P.off_desc_d = off;
+    off = align256(off + (size_t)((f / 256) / (2 * P.C_d)) * n_pairs * sizeof(ItemDesc));
     P.total = off;
     return P;
 }
@@ -200,7 +204,9 @@ size_t rvq_gemv_workspace_bytes(int32_t rows, int32_t cols, int32_t n) {
     int C, S;
     choose_split(rows, cols, n, 1, 1 << 30, C, S);
     const int nslot = (cols / 256) / C;
-    return RVQ_WS_STATUS_BYTES + align256((size_t)n * nslot * rows * 4);
+    const size_t items = (size_t)((cols / 256) / (2 * C)) * n;
+    return RVQ_WS_STATUS_BYTES + align256((size_t)n * nslot * rows * 4) +
+           align256(items * sizeof(ItemDesc));
 }
 
 rvq_status rvq_gemv(const uint8_t *packed_codes_dev, const float *packed_cb_dev, int32_t rows,
@@ -238,8 +244,10 @@ rvq_status rvq_gemv(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
     job.status = (uint32_t *)ws_dev;
     float *part = (float *)((uint8_t *)ws_dev + RVQ_WS_STATUS_BYTES);
     job.part[0] = part;
+    job.desc = (ItemDesc *)((uint8_t *)part + align256((size_t)n * (job.G / job.C) * rows * 4));
     cudaStream_t st = (cudaStream_t)stream;
-    RVQ_TRY(launch_lut_gemv(job, st, false));
+    RVQ_TRY(launch_lut_plan(job, nullptr, st, false));
+    RVQ_TRY(launch_lut_gemv(job, st, true));
     return launch_slot_reduce(part, n, job.G / job.C, rows, y_dev, st, true);
 }
 
@@ -401,8 +409,8 @@ static LutJob ffn_job(const rvq_moe_bank *bank, const RecordLayout &L, int n_pai
     return j;
 }
 
-// gate/up LUT-GEMV -> SwiGLU reduction -> down LUT-GEMV; `marks` (3 events or
-// NULL) are recorded after each kernel.
+// item plan -> gate/up LUT-GEMV -> SwiGLU reduction -> down LUT-GEMV; `marks`
+// (4 events or NULL) are recorded after each kernel.
 static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                           int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
                           void *ws_dev, const FfnPlan &P, cudaStream_t st, void **marks,
@@ -438,10 +446,7 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     gu.x_div = k;
     gu.offsets = offsets_dev;
     gu.pairs = pairs_dev;
-    RVQ_TRY(launch_lut_gemv(gu, st, pdl));
-    RVQ_TRY(mark(0));
-    RVQ_TRY(launch_swiglu_reduce(gpart, upart, np, P.nslot_gu, bank->f, h, st, pdl));
-    RVQ_TRY(mark(1));
+    gu.desc = (ItemDesc *)(ws + P.off_desc_gu);
 
     LutJob dn = ffn_job(bank, L, np, ws_dev);
     dn.codes_off[0] = L.down_off;
@@ -459,8 +464,15 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     dn.x_div = 1;
     dn.offsets = offsets_dev;
     dn.pairs = pairs_dev;
+    dn.desc = (ItemDesc *)(ws + P.off_desc_d);
+    RVQ_TRY(launch_lut_plan(gu, &dn, st, pdl));
+    RVQ_TRY(mark(0));
+    RVQ_TRY(launch_lut_gemv(gu, st, pdl));
+    RVQ_TRY(mark(1));
+    RVQ_TRY(launch_swiglu_reduce(gpart, upart, np, P.nslot_gu, bank->f, h, st, pdl));
+    RVQ_TRY(mark(2));
     RVQ_TRY(launch_lut_gemv(dn, st, pdl));
-    return mark(2);
+    return mark(3);
 }
 
 static rvq_status check_ffn_args(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
@@ -542,7 +554,7 @@ rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, cons
     float *dpart = (float *)((uint8_t *)ws_dev + P.off_dpart);
     RVQ_TRY(launch_combine(dpart, P.nslot_d, topk_w_dev, n, k, bank->d, x_dev, (int)xdt, out_dev,
                            st, pdl));
-    return mark(6);
+    return mark(7);
 }
 
 rvq_status rvq_ws_clear(void *ws_dev, rvq_stream_t stream) {

@@ -88,6 +88,17 @@ __device__ __forceinline__ float load1(const void *base, int dtype, int64_t idx)
 }
 
 // ------------------------------------------------------- LUT-GEMV job (host)
+// One work item of a LUT-GEMV launch, written by the plan kernel.
+struct ItemDesc {
+    int32_t expert;   // -1: skip (the plan flagged an error)
+    int32_t entryA;   // pair entries of the two units
+    int32_t entryB;
+    int16_t g0;       // first chunk group
+    int8_t type;      // 0: two tokens, one group per step; 1: one token, two groups per step
+    int8_t pad;
+};
+static_assert(sizeof(ItemDesc) == 16, "ItemDesc is one 16-byte load");
+
 // One launch of the fused lookup-table GEMV over grouped (token, expert)
 // pairs.  See lut_gemv.cu for the item decomposition.
 struct LutJob {
@@ -112,14 +123,17 @@ struct LutJob {
     const int32_t *offsets;    // [E+1] (NULL: single group of n_pairs)
     const int32_t *pairs;      // [n_pairs] (NULL: identity)
     uint32_t *status;
+    ItemDesc *desc;            // [items before the row split], from the plan kernel
     // record header check
     int32_t check_header;
     int32_t layer, d, f;
 };
 
-inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
+__host__ __device__ inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
 
 rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl);
+// Descriptors for one or two LUT-GEMV jobs sharing the same grouping.
+rvq_status launch_lut_plan(const LutJob &ja, const LutJob *jb, cudaStream_t stream, bool pdl);
 rvq_status launch_lut_build(const float *cb, const void *x, int xdt, int n, int cols,
                             float *lut, cudaStream_t stream);
 // h[entry][r] = silu(sum_slot gate_part) * sum_slot up_part
@@ -146,7 +160,7 @@ struct FfnPlan {
     int C_gu, S_gu;   // gate/up: chunk groups per item step run, row splits
     int C_d, S_d;     // down
     int nslot_gu, nslot_d;
-    size_t off_gpart, off_upart, off_h, off_dpart, total;
+    size_t off_gpart, off_upart, off_h, off_dpart, off_desc_gu, off_desc_d, total;
 };
 FfnPlan plan_ffn(int d, int f, int n_pairs, int E);
 int num_sms();

@@ -10,11 +10,17 @@
 // Vector Quantization (RVQ)"].
 //
 // GB300 design (not the pages' CPU loop):
-//  * A block owns one "item": one expert matrix, up to two (token, 32-chunk
-//    group) units, a range of C steps over chunk groups and a range of rows.
-//    Its table for one step (2 units x 3 stages x 256 entries x 32 chunks,
-//    192 KiB) lives in shared memory and is built exactly once per (token,
-//    chunk group, row range); it is never written to HBM.
+//  * Work is split into "items": one expert matrix, two (token, 32-chunk
+//    group) units, a run of C steps over chunk groups and a range of rows.  A
+//    step's table (2 units x 3 stages x 256 entries x 32 chunks, 192 KiB)
+//    lives in shared memory, built once per (token, chunk group, row range)
+//    and never written to HBM.
+//  * A small plan kernel turns the grouping (offsets, pairs) into one 16-byte
+//    descriptor per item and checks each expert record's header.
+//  * The GEMV kernel is persistent: one block per SM walks its items.  While
+//    it streams the codes of one item it already fetches the next item's
+//    codebook and inputs (cp.async into shared memory) and its first code
+//    tiles (register ring), so HBM keeps streaming across item boundaries.
 //  * Lane l of a warp owns row 32b + l.  The packed code layout rotates each
 //    row's chunk order by l, so at every unrolled step t the 32 lanes read 32
 //    different table columns (bank = column): the lookups are conflict-free
@@ -23,9 +29,9 @@
 //  * A code byte becomes a shared-memory address with one byte permute
 //    (code -> bits 8..15, column offset -> bits 0..7), one LDS and half of a
 //    packed fp32x2 add.  Code tiles (3 KiB per 32 rows x 32 chunks) are
-//    streamed with 128-bit non-allocating loads, one row block ahead.
+//    streamed with 128-bit non-allocating loads.
 //  * Items of the same (expert, chunk group) for different token pairs are
-//    adjacent in launch order, so a second token pair re-reads codes from L2.
+//    adjacent in the item order, so a second token pair re-reads codes from L2.
 //  * Split-K partials (one slot per item column range) are reduced by the
 //    next kernel (SwiGLU for gate/up, the combine for down).
 #include "internal.cuh"
@@ -36,27 +42,16 @@ namespace {
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int kMaxSplitRows = 2048;  // rows per item: at most 8 row blocks per warp
-constexpr int kMaxAccRows = 1024;    // rows per item when C > 1 (shared accumulator)
+constexpr int kMaxAccRows = 512;     // rows per item when C > 1 (shared accumulator)
 constexpr int kCbBytes = 3 * 128 * 8 * 2 * 4;  // packed codebook of one matrix, 24 KiB
-
-struct Item {
-    int valid;
-    int type;  // 0: two tokens, one chunk group per step; 1: one token, two groups per step
-    int entryA, entryB;
-    int g0;
-    int slotA, slotB;
-    int rb0, nrb;
-    const uint8_t *codes;
-    const float *cb;
-    const void *xA, *xB;
-};
+constexpr int kXsBytes = 2 * 32 * 8 * 4;        // inputs of one step: 2 units x 32 chunks x 8 fp32
+constexpr int kSmemBytes = kLutBytes + kCbBytes + kXsBytes + kMaxAccRows * 2 * 4;
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
 }
-
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
     uint64_t r;
     asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
@@ -77,167 +72,170 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t x, uint64_t y, uint64_t acc) 
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(acc));
     return r;
 }
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
 
-// Decode blockIdx into an item, with the whole of warp 0 (all 32 lanes call
-// it; lane 0 writes `it`).  The expert segment holding pair position p is
-// found with one parallel read of offsets[0..E] (9 per lane) and a ballot;
-// the two pair entries and the record header are then read in parallel: two
-// dependent memory round trips per item.
-__device__ void decode_item(const LutJob &job, int m, Item &it) {
-    const int lane = threadIdx.x & 31;
+// ----------------------------------------------------------------- plan
+// Item i of a launch (before the row split) -> descriptor.  Item order
+// within expert e (n_e tokens, Q = n_e / 2 token pairs, G/C runs of C chunk
+// groups): two-token items li = run * Q + q, then (n_e odd) the one-token
+// items of the last token, each covering 2C groups.
+__device__ ItemDesc plan_one(const LutJob &job, const int32_t *soff, int i) {
+    ItemDesc d;
+    d.expert = -1;
+    d.entryA = d.entryB = 0;
+    d.g0 = 0;
+    d.type = 0;
+    d.pad = 0;
     const int per_pair = job.G / (2 * job.C);
-    const int i = blockIdx.x / job.S;
-    const int split = blockIdx.x % job.S;
     const int p = i / per_pair;
-    bool ok = p < job.n_pairs;
     int e = 0, o = 0, ne = job.n_pairs;
-    if (ok && job.offsets) {
-        int off[9];
-#pragma unroll
-        for (int q = 0; q < 9; ++q) {
-            const int x = lane * 9 + q;
-            off[q] = x <= job.E ? job.offsets[x] : 0x7fffffff;
+    if (job.offsets) {
+        if (soff[0] != 0 || soff[job.E] != job.n_pairs) {
+            set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+            return d;
         }
-        const int next_first = __shfl_down_sync(0xffffffffu, off[0], 1);
-        int found = -1, fo = 0, fhi = 0;
-#pragma unroll
-        for (int q = 0; q < 9; ++q) {
-            const int x = lane * 9 + q;
-            const int hi = q < 8 ? off[q + 1] : (lane < 31 ? next_first : 0x7fffffff);
-            if (found < 0 && x < job.E && off[q] <= p && p < hi) {
-                found = x;
-                fo = off[q];
-                fhi = hi;
-            }
+        int lo = 0, hi = job.E;  // largest e with offsets[e] <= p
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (soff[mid] <= p) lo = mid; else hi = mid;
         }
-        // offsets[0] sits in lane 0, offsets[E] in lane E / 9
-        const int o0 = __shfl_sync(0xffffffffu, off[0], 0);
-        int oE = 0;
-#pragma unroll
-        for (int q = 0; q < 9; ++q)
-            if (lane * 9 + q == job.E) oE = off[q];
-        oE = __shfl_sync(0xffffffffu, oE, job.E / 9);
-        const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
-        if (o0 != 0 || oE != job.n_pairs || hit == 0) {
-            ok = false;
-        } else {
-            const int src = __ffs(hit) - 1;
-            e = __shfl_sync(0xffffffffu, found, src);
-            o = __shfl_sync(0xffffffffu, fo, src);
-            ne = __shfl_sync(0xffffffffu, fhi, src) - o;
-            ok = 0 <= o && o <= p && p < o + ne && o + ne <= job.n_pairs;
+        e = lo;
+        o = soff[e];
+        ne = soff[e + 1] - o;
+        if (!(0 <= o && o <= p && p < o + ne && o + ne <= job.n_pairs)) {
+            set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+            return d;
         }
-        if (!ok && lane == 0) set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
-    }
-    if (!ok) {
-        if (lane == 0) it.valid = 0;
-        return;
     }
     const int li = i - per_pair * o;
     const int Q = ne >> 1;
-    const int runs = job.G / job.C;  // chunk-group runs of the two-token items
-    int type, tauA, tauB, g0, slotA, slotB;
+    const int runs = job.G / job.C;
+    int tauA, tauB;
     if (li < Q * runs) {
-        const int gr = li / Q, q = li % Q;
-        type = 0;
-        tauA = 2 * q;
-        tauB = 2 * q + 1;
-        g0 = gr * job.C;
-        slotA = slotB = gr;
+        d.type = 0;
+        tauA = 2 * (li % Q);
+        tauB = tauA + 1;
+        d.g0 = (int16_t)((li / Q) * job.C);
     } else {
-        const int l2 = li - Q * runs;
-        type = 1;
+        d.type = 1;
         tauA = tauB = ne - 1;
-        g0 = l2 * 2 * job.C;
-        slotA = 2 * l2;
-        slotB = 2 * l2 + 1;
+        d.g0 = (int16_t)((li - Q * runs) * 2 * job.C);
     }
-    const uint8_t *rec = job.base ? job.base + (uint64_t)e * job.record_bytes : nullptr;
-    // parallel reads: lane 0 / 1 the pair entries, lane 2 the header words
-    int v = 0;
-    if (lane == 0) v = job.pairs ? job.pairs[o + tauA] : o + tauA;
-    if (lane == 1) v = job.pairs ? job.pairs[o + tauB] : o + tauB;
-    bool hdr_ok = true;
-    if (lane == 2 && job.check_header && rec) {
-        const rvq_expert_header *h = reinterpret_cast<const rvq_expert_header *>(rec);
-        hdr_ok = h->magic == RVQ_BANK_MAGIC && h->expert == e && h->layer == job.layer &&
-                 h->d == job.d && h->f == job.f && h->record_bytes == job.record_bytes;
-    }
-    const int eA = __shfl_sync(0xffffffffu, v, 0);
-    const int eB = __shfl_sync(0xffffffffu, v, 1);
-    hdr_ok = __shfl_sync(0xffffffffu, hdr_ok ? 1 : 0, 2) != 0;
-    if (lane != 0) return;
-    it.valid = 0;
-    if (!hdr_ok) {
-        set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
-        return;
-    }
+    const int eA = job.pairs ? job.pairs[o + tauA] : o + tauA;
+    const int eB = job.pairs ? job.pairs[o + tauB] : o + tauB;
     if (eA < 0 || eA >= job.n_pairs || eB < 0 || eB >= job.n_pairs) {
         set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
-        return;
+        return d;
     }
-    it.type = type;
-    it.g0 = g0;
-    it.slotA = slotA;
-    it.slotB = slotB;
-    it.entryA = eA;
-    it.entryB = eB;
-    if (job.record_bytes) {
-        it.codes = rec + job.codes_off[m];
-        it.cb = reinterpret_cast<const float *>(rec + job.cb_off[m]);
-    } else {
-        it.codes = job.codes_ptr;
-        it.cb = job.cb_ptr;
+    if (job.check_header && job.base) {
+        // the pages check magic, expert id and offset range on every read
+        const rvq_expert_header *h =
+            reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)e * job.record_bytes);
+        if (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
+            h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes) {
+            set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
+            return d;
+        }
     }
-    const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
-    it.xA = reinterpret_cast<const uint8_t *>(job.x) + (int64_t)(eA / job.x_div) * job.x_stride * esz;
-    it.xB = reinterpret_cast<const uint8_t *>(job.x) + (int64_t)(eB / job.x_div) * job.x_stride * esz;
-    const int RB = job.rows / 32;
-    it.nrb = RB / job.S;
-    it.rb0 = split * it.nrb;
-    it.valid = 1;
+    d.expert = e;
+    d.entryA = eA;
+    d.entryB = eB;
+    return d;
 }
 
-// Build the step's table.  Column c = lane.  Type 0 interleaves the two
-// tokens (T[s][k][c][u], 8-byte pairs); type 1 keeps the two chunk groups in
-// separate 128-byte halves (T[s][k][u][c]).  Two entries (k, k+1) per packed
-// FMA, using the pair-interleaved codebook.
-__device__ __forceinline__ void build_table(uint8_t *lut, const uint8_t *cb_s, const float xa[8],
-                                            const float xb[8], int type, int lane, int warp) {
-    uint64_t xa2[8], xb2[8];
+__global__ void __launch_bounds__(256) plan_kernel(const LutJob ja, const LutJob jb) {
+    __shared__ int32_t soff[257];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int32_t *offsets = ja.offsets;
+    const int E = ja.E;
+    if (offsets)
+        for (int x = threadIdx.x; x <= E; x += blockDim.x) soff[x] = offsets[x];
+    __syncthreads();
+    const int na = lut_items(ja) / ja.S;
+    const int nb = jb.n_pairs ? lut_items(jb) / jb.S : 0;
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < na)
+        ja.desc[t] = plan_one(ja, soff, t);
+    else if (t < na + nb)
+        jb.desc[t - na] = plan_one(jb, soff, t - na);
+}
+
+// ----------------------------------------------------------------- table build
+// Two entries (k, k+1) per packed FMA from the pair-interleaved codebook in
+// shared memory.  Half-warp h takes entry pair 2w' + h (w' = warp's step), so
+// one 128-bit broadcast load serves two entry pairs; lane r of a half handles
+// columns r and r + 16 (in swapped order in the upper half so the 4-byte
+// stores of the two halves fall in different banks).  Type 0 interleaves the
+// two tokens (T[s][k][c][u], 8-byte pairs); type 1 keeps the two chunk groups
+// in separate 128-byte halves (T[s][k][u][c]).
+__device__ __forceinline__ void build_table(uint8_t *lut, const uint8_t *cb_s, const uint8_t *xs_s,
+                                            int xdt, int type, int lane, int warp) {
+    const int hf = lane >> 4, r = lane & 15;
+    const int c0 = hf ? r + 16 : r, c1 = hf ? r : r + 16;
+    uint64_t x2[4][8];  // (unit A col c0, A c1, B c0, B c1) x dims, duplicated pairs
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        xa2[i] = pk2(xa[i], xa[i]);
-        xb2[i] = pk2(xb[i], xb[i]);
+    for (int v = 0; v < 4; ++v) {
+        const int u = v >> 1, c = (v & 1) ? c1 : c0;
+        float xv[8];
+        if (xdt == RVQ_BF16) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(xs_s + (u * 32 + c) * 16);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                xv[2 * i] = __uint_as_float(w[i] << 16);
+                xv[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+            const float4 a = *reinterpret_cast<const float4 *>(xs_s + (u * 32 + c) * 32);
+            const float4 b = *reinterpret_cast<const float4 *>(xs_s + (u * 32 + c) * 32 + 16);
+            xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+            xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x2[v][i] = pk2(xv[i], xv[i]);
     }
     const ulonglong2 *cb2 = reinterpret_cast<const ulonglong2 *>(cb_s);
-#pragma unroll 4
-    for (int kp = warp; kp < 3 * 128; kp += NW) {
+#pragma unroll 2
+    for (int kq = warp; kq < 3 * 64; kq += NW) {
+        const int kp = 2 * kq + hf;  // entry pair index over all stages
         const int s = kp >> 7, k = (kp & 127) * 2;
-        // 16 floats: (k, k+1) interleaved for dims 0..7 (same address in every
-        // lane: shared-memory broadcast)
-        const ulonglong2 c0 = cb2[kp * 4 + 0];
-        const ulonglong2 c1 = cb2[kp * 4 + 1];
-        const ulonglong2 c2 = cb2[kp * 4 + 2];
-        const ulonglong2 c3 = cb2[kp * 4 + 3];
-        const uint64_t cw[8] = {c0.x, c0.y, c1.x, c1.y, c2.x, c2.y, c3.x, c3.y};
-        uint64_t ta = 0, tb = 0;
+        const ulonglong2 q0 = cb2[kp * 4 + 0];
+        const ulonglong2 q1 = cb2[kp * 4 + 1];
+        const ulonglong2 q2 = cb2[kp * 4 + 2];
+        const ulonglong2 q3 = cb2[kp * 4 + 3];
+        const uint64_t cw[8] = {q0.x, q0.y, q1.x, q1.y, q2.x, q2.y, q3.x, q3.y};
+        uint64_t t[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            ta = ffma2(xa2[i], cw[i], ta);
-            tb = ffma2(xb2[i], cw[i], tb);
-        }
-        const float2 a = upk2(ta), b = upk2(tb);  // (entry k, entry k+1)
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) t[v] = ffma2(x2[v][i], cw[i], t[v]);
+        const float2 a0 = upk2(t[0]), a1 = upk2(t[1]), b0 = upk2(t[2]), b1 = upk2(t[3]);
         uint8_t *row0 = lut + s * kLutStageBytes + k * 256;
         uint8_t *row1 = row0 + 256;
         if (type == 0) {
-            *reinterpret_cast<float2 *>(row0 + lane * 8) = make_float2(a.x, b.x);
-            *reinterpret_cast<float2 *>(row1 + lane * 8) = make_float2(a.y, b.y);
+            *reinterpret_cast<float2 *>(row0 + c0 * 8) = make_float2(a0.x, b0.x);
+            *reinterpret_cast<float2 *>(row1 + c0 * 8) = make_float2(a0.y, b0.y);
+            *reinterpret_cast<float2 *>(row0 + c1 * 8) = make_float2(a1.x, b1.x);
+            *reinterpret_cast<float2 *>(row1 + c1 * 8) = make_float2(a1.y, b1.y);
         } else {
-            *reinterpret_cast<float *>(row0 + lane * 4) = a.x;
-            *reinterpret_cast<float *>(row1 + lane * 4) = a.y;
-            *reinterpret_cast<float *>(row0 + 128 + lane * 4) = b.x;
-            *reinterpret_cast<float *>(row1 + 128 + lane * 4) = b.y;
+            *reinterpret_cast<float *>(row0 + c0 * 4) = a0.x;
+            *reinterpret_cast<float *>(row1 + c0 * 4) = a0.y;
+            *reinterpret_cast<float *>(row0 + c1 * 4) = a1.x;
+            *reinterpret_cast<float *>(row1 + c1 * 4) = a1.y;
+            *reinterpret_cast<float *>(row0 + 128 + c0 * 4) = b0.x;
+            *reinterpret_cast<float *>(row1 + 128 + c0 * 4) = b0.y;
+            *reinterpret_cast<float *>(row0 + 128 + c1 * 4) = b1.x;
+            *reinterpret_cast<float *>(row1 + 128 + c1 * 4) = b1.y;
         }
     }
 }
@@ -247,10 +245,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
 }
 
 // One 32-row x 32-chunk code tile (6 words of 16 B per lane) against the
-// table.  Two tokens (TYPE 0): one permute + one 8-byte LDS per code byte
-// gives both tokens' entries.  One token (TYPE 1): one permute + one 4-byte LDS
-// per code byte, two lookups per packed add.  aux[t] carries the lane's
-// rotated column offset (and, for TYPE 1, the table half) in bits 0..7.
+// table.  Two tokens (type 0): one permute + one 8-byte LDS per code byte
+// gives both tokens' entries.  One token (type 1): one permute + one 4-byte
+// LDS per code byte, two lookups per packed add.  aux[t] carries the lane's
+// rotated column offset (and, for type 1, the table half) in bits 0..7.
 template <int TYPE>
 __device__ __forceinline__ uint64_t tile_lookups(const uint4 (&c)[6], const uint32_t (&aux)[32],
                                                  const uint8_t *lut) {
@@ -284,109 +282,182 @@ __device__ __forceinline__ uint64_t tile_lookups(const uint4 (&c)[6], const uint
     return acc;
 }
 
-// Streams the item's code tiles through a 2-deep register ring.  Work unit =
-// one code tile: TYPE 0 has one tile per row block (both tokens), TYPE 1 two
-// (groups A and B, each against its own table half).  With 16 warps a warp's
-// tiles are q = warp + 16 i; for TYPE 1 the table half is warp & 1.  The first
-// tiles of a step are requested before its table is built, so the build
-// overlaps HBM traffic; tile i + D is requested once tile i is consumed.
-template <int TYPE>
-__device__ __forceinline__ void run_item(const LutJob &job, const Item &it, int m, uint8_t *lut,
-                                         uint8_t *cb_s, float *sacc) {
-    constexpr int D = 2;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int RB = job.rows / 32;
-    const int C = job.C;
-    const int ntiles = TYPE == 0 ? it.nrb : 2 * it.nrb;
-    const int nt_w = (ntiles - warp + NW - 1) / NW;  // tiles of this warp (may be 0)
-    const int nslot = job.G / C;
-    const int rows_split = it.nrb * 32;
-    float *part = job.part[m];
-    const int gstep = TYPE == 0 ? 1 : 2;
-    const int u = TYPE == 0 ? 0 : (warp & 1);  // table half / unit of this warp (TYPE 1)
+// ------------------------------------------------------------ persistent GEMV
+// A phase = (matrix, item, step).  The block's work index w runs over
+// matrix-major (item * S + split), so the items of both matrices of a
+// gate/up launch share one set of persistent blocks.  valid: 1 usable,
+// -1 skipped item (error flagged by the plan), 0 past the end.
+struct Phase {
+    ItemDesc d;
+    int w, step, valid, m, wl;  // wl = item * S + split within matrix m
+};
 
+// What one warp needs to stream a phase, derived once per phase so that a
+// tile costs one pointer increment.
+struct WarpPlan {
+    const uint8_t *tile;  // this warp's first code tile (lane offset included)
+    int tstride;          // bytes between this warp's consecutive tiles
+    int nt;               // tiles of this warp in the phase
+};
+
+__device__ __forceinline__ Phase load_phase(const LutJob &job, int w, int step) {
+    Phase P;
+    P.w = w;
+    P.step = step;
+    P.valid = 0;
+    const int per_m = lut_items(job);
+    P.m = w / per_m;
+    P.wl = w - P.m * per_m;
+    P.d.expert = 0;
+    P.d.entryA = P.d.entryB = 0;
+    P.d.g0 = 0;
+    P.d.type = 0;
+    P.d.pad = 0;
+    if (P.m >= job.n_mat) return P;
+    const int4 raw = __ldg(reinterpret_cast<const int4 *>(job.desc) + P.wl / job.S);
+    *reinterpret_cast<int4 *>(&P.d) = raw;
+    P.valid = P.d.expert < 0 ? -1 : 1;
+    return P;
+}
+
+__device__ __forceinline__ int ph_gA(const Phase &P) {
+    return P.d.g0 + P.step * (P.d.type == 0 ? 1 : 2);
+}
+__device__ __forceinline__ const uint8_t *ph_record(const LutJob &job, const Phase &P) {
+    return job.base + (uint64_t)P.d.expert * job.record_bytes;
+}
+__device__ __forceinline__ const uint8_t *ph_cb(const LutJob &job, const Phase &P) {
+    return job.record_bytes ? ph_record(job, P) + job.cb_off[P.m]
+                            : reinterpret_cast<const uint8_t *>(job.cb_ptr);
+}
+
+__device__ __forceinline__ WarpPlan warp_plan(const LutJob &job, const Phase &P, int lane,
+                                              int warp) {
+    WarpPlan W;
+    const int RB = job.rows / 32;
+    const int nrb = RB / job.S;
+    const int rb0 = (P.wl % job.S) * nrb;
+    const uint8_t *codes =
+        job.record_bytes ? ph_record(job, P) + job.codes_off[P.m] : job.codes_ptr;
+    if (P.d.type == 0) {  // tile q = warp + NW i -> row block q
+        W.tile = codes + ((size_t)ph_gA(P) * RB + rb0 + warp) * kTileBytes + lane * 16;
+        W.tstride = NW * kTileBytes;
+        W.nt = (nrb - warp + NW - 1) / NW;
+    } else {              // tile q -> row block q >> 1, chunk group gA + (q & 1)
+        const int u = warp & 1;
+        W.tile = codes + ((size_t)(ph_gA(P) + u) * RB + rb0 + (warp >> 1)) * kTileBytes + lane * 16;
+        W.tstride = (NW / 2) * kTileBytes;
+        W.nt = (2 * nrb - warp + NW - 1) / NW;
+    }
+    return W;
+}
+
+// cp.async of one step's inputs: 2 units x 32 chunks x 8 values.
+__device__ __forceinline__ void issue_x(const LutJob &job, const Phase &P, uint8_t *xs_s) {
+    const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
+    const int per_unit = 32 * 8 * esz / 16;  // 16-byte pieces per unit
+    const int tid = threadIdx.x;
+    if (tid < 2 * per_unit) {
+        const int u = tid / per_unit, q = tid % per_unit;
+        const int entry = u ? P.d.entryB : P.d.entryA;
+        const int g = ph_gA(P) + (u ? P.d.type : 0);
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(job.x) +
+                             ((int64_t)(entry / job.x_div) * job.x_stride + (int64_t)g * 256) * esz +
+                             q * 16;
+        cp_async16(xs_s + u * 32 * 8 * esz + q * 16, src);
+    }
+}
+
+__device__ __forceinline__ void issue_cb(const uint8_t *cb, uint8_t *cb_s) {
+#pragma unroll
+    for (int q = 0; q < kCbBytes / 16 / NT; ++q) {
+        const int o = (threadIdx.x + NT * q) * 16;
+        cp_async16(cb_s + o, cb + o);
+    }
+}
+
+__device__ __forceinline__ void load_tile(uint4 (&b)[6], const uint8_t *p) {
+#pragma unroll
+    for (int q = 0; q < 6; ++q) b[q] = ldg_stream(p + q * 512);
+}
+
+__device__ __forceinline__ void load_first(const WarpPlan &W, uint4 (&buf)[2][6]) {
+    if (W.nt > 0) load_tile(buf[0], W.tile);
+    if (W.nt > 1) load_tile(buf[1], W.tile + W.tstride);
+}
+
+// Stream one phase's tiles (type TYPE) through the 2-deep ring.  Once the
+// phase's own tiles are all requested, the freed ring slots take the first
+// tiles of the next phase (plan Wn; nt_next = 0 disables that).
+template <int TYPE>
+__device__ __forceinline__ void stream_phase(const LutJob &job, const Phase &P,
+                                             const WarpPlan &W, const WarpPlan &Wn, int nt_next,
+                                             uint4 (&buf)[2][6], const uint8_t *lut, float *sacc,
+                                             int lane, int warp) {
+    const int u = TYPE == 0 ? 0 : (warp & 1);
+    const int C = job.C, j = P.step;
+    const int nslot = job.G / C;
+    const int nrb = job.rows / 32 / job.S;
+    const int rows_split = nrb * 32;
+    const int row0 = (P.wl % job.S) * rows_split;
+    const int slotA = P.d.g0 / C;
+    // partial rows: row = row0 + rbl * 32 + lane, rbl = this tile's row block in the split
+    const int rbl0 = TYPE == 0 ? warp : (warp >> 1);
+    const int rbl_step = TYPE == 0 ? NW : NW / 2;
+    float *part = job.part[P.m];
+    float *pA, *pB;
+    if (TYPE == 0) {
+        pA = part + ((size_t)P.d.entryA * nslot + slotA) * job.rows + row0 + lane;
+        pB = part + ((size_t)P.d.entryB * nslot + slotA) * job.rows + row0 + lane;
+    } else {
+        const int e = u ? P.d.entryB : P.d.entryA;
+        pA = part + ((size_t)e * nslot + slotA + u) * job.rows + row0 + lane;
+        pB = pA;
+    }
     uint32_t aux[32];
 #pragma unroll
     for (int t = 0; t < 32; ++t)
         aux[t] = TYPE == 0 ? (((lane + t) & 31) << 3) : ((((lane + t) & 31) << 2) | (u << 7));
-
-    auto tile_rb = [&](int i) {  // row block of this warp's i-th tile
-        const int q = warp + NW * i;
-        return it.rb0 + (TYPE == 0 ? q : (q >> 1));
-    };
-    uint4 buf[D][6];
-    auto load_tile = [&](uint4 (&b)[6], int gA, int i) {
-        const int g = gA + u;
-        const uint8_t *p = it.codes + ((size_t)g * RB + tile_rb(i)) * kTileBytes + lane * 16;
+    const uint8_t *next = W.tile + 2 * W.tstride;  // tile i + 2 of this phase
+    const uint8_t *next_n = Wn.tile;               // then tiles of the next phase
+    int left_n = nt_next;
+    for (int i0 = 0; i0 < W.nt; i0 += 2) {
 #pragma unroll
-        for (int q = 0; q < 6; ++q) b[q] = ldg_stream(p + q * 512);
-    };
-
-    // item prologue: first tiles in flight, then the matrix's codebook into
-    // shared memory (one coalesced 24 KiB copy per item)
-#pragma unroll
-    for (int d = 0; d < D; ++d)
-        if (d < nt_w) load_tile(buf[d], it.g0, d);
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(it.cb);
-        uint4 *dst = reinterpret_cast<uint4 *>(cb_s);
-        uint4 v[kCbBytes / 16 / NT];
-#pragma unroll
-        for (int q = 0; q < kCbBytes / 16 / NT; ++q) v[q] = __ldg(src + threadIdx.x + NT * q);
-#pragma unroll
-        for (int q = 0; q < kCbBytes / 16 / NT; ++q) dst[threadIdx.x + NT * q] = v[q];
-    }
-    for (int j = 0; j < C; ++j) {
-        const int gA = it.g0 + j * gstep, gB = gA + (TYPE == 0 ? 0 : 1);
-        if (j > 0) {
-#pragma unroll
-            for (int d = 0; d < D; ++d)
-                if (d < nt_w) load_tile(buf[d], gA, d);
-        }
-        float xa[8], xb[8];
-        load8(it.xA, job.x_dtype, (int64_t)(gA * 32 + lane) * 8, xa);
-        load8(it.xB, job.x_dtype, (int64_t)(gB * 32 + lane) * 8, xb);
-        __syncthreads();  // codebook stored (j = 0) / previous step's lookups done (j > 0)
-        build_table(lut, cb_s, xa, xb, TYPE, lane, warp);
-        __syncthreads();
-        for (int i0 = 0; i0 < nt_w; i0 += D) {
-#pragma unroll
-            for (int d = 0; d < D; ++d) {
-                const int i = i0 + d;
-                if (i < nt_w) {
-                    const uint64_t acc = tile_lookups<TYPE>(buf[d], aux, lut);
-                    if (i + D < nt_w) load_tile(buf[d], gA, i + D);
-                    const int rb = tile_rb(i);
-                    const int rl = (rb - it.rb0) * 32 + lane;
-                    const int row = rb * 32 + lane;
-                    float2 a = upk2(acc);
-                    if constexpr (TYPE == 1) {
-                        // one token: both halves of the packed sum belong to this unit
-                        float v = a.x + a.y;
-                        if (C > 1) {
-                            if (j > 0) v += sacc[u * rows_split + rl];
-                            if (j < C - 1) sacc[u * rows_split + rl] = v;
+        for (int dd = 0; dd < 2; ++dd) {
+            const int i = i0 + dd;
+            if (i < W.nt) {
+                const uint64_t acc = tile_lookups<TYPE>(buf[dd], aux, lut);
+                if (i + 2 < W.nt) {
+                    load_tile(buf[dd], next);
+                    next += W.tstride;
+                } else if (left_n > 0) {
+                    load_tile(buf[dd], next_n);
+                    next_n += Wn.tstride;
+                    --left_n;
+                }
+                const int rl = (rbl0 + i * rbl_step) * 32 + lane;  // row within the split
+                float2 a = upk2(acc);
+                if constexpr (TYPE == 1) {
+                    float v = a.x + a.y;
+                    if (C > 1) {
+                        if (j > 0) v += sacc[u * rows_split + rl];
+                        if (j < C - 1) sacc[u * rows_split + rl] = v;
+                    }
+                    if (j == C - 1) pA[rl - lane] = v;
+                } else {
+                    if (C > 1) {
+                        if (j > 0) {
+                            a.x += sacc[rl];
+                            a.y += sacc[rows_split + rl];
                         }
-                        if (j == C - 1) {
-                            const int e = u ? it.entryB : it.entryA;
-                            const int sl = u ? it.slotB : it.slotA;
-                            part[((size_t)e * nslot + sl) * job.rows + row] = v;
+                        if (j < C - 1) {
+                            sacc[rl] = a.x;
+                            sacc[rows_split + rl] = a.y;
                         }
-                    } else {
-                        if (C > 1) {
-                            if (j > 0) {
-                                a.x += sacc[rl];
-                                a.y += sacc[rows_split + rl];
-                            }
-                            if (j < C - 1) {
-                                sacc[rl] = a.x;
-                                sacc[rows_split + rl] = a.y;
-                            }
-                        }
-                        if (j == C - 1) {
-                            part[((size_t)it.entryA * nslot + it.slotA) * job.rows + row] = a.x;
-                            part[((size_t)it.entryB * nslot + it.slotB) * job.rows + row] = a.y;
-                        }
+                    }
+                    if (j == C - 1) {
+                        pA[rl - lane] = a.x;
+                        pB[rl - lane] = a.y;
                     }
                 }
             }
@@ -396,19 +467,67 @@ __device__ __forceinline__ void run_item(const LutJob &job, const Item &it, int 
 
 __global__ void __launch_bounds__(NT, 1) lut_gemv_kernel(const LutJob job) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ Item it;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int m = blockIdx.y;
-    if (threadIdx.x < 32) decode_item(job, m, it);
-    __syncthreads();
-    if (!it.valid) return;
-    asm volatile("griddepcontrol.launch_dependents;");
+    uint8_t *lut = smem;
     uint8_t *cb_s = smem + kLutBytes;
-    float *sacc = reinterpret_cast<float *>(cb_s + kCbBytes);
-    if (it.type == 0)
-        run_item<0>(job, it, m, smem, cb_s, sacc);
-    else
-        run_item<1>(job, it, m, smem, cb_s, sacc);
+    uint8_t *xs_s = cb_s + kCbBytes;
+    float *sacc = reinterpret_cast<float *>(xs_s + kXsBytes);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    Phase P = load_phase(job, blockIdx.x, 0);
+    uint4 buf[2][6];
+    const uint8_t *cb_loaded = nullptr;
+    if (P.valid > 0) {
+        // codebook and inputs first (the build waits for them), then tiles
+        cb_loaded = ph_cb(job, P);
+        issue_cb(cb_loaded, cb_s);
+        issue_x(job, P, xs_s);
+        cp_async_commit();
+        load_first(warp_plan(job, P, lane, warp), buf);
+    } else {
+        cp_async_commit();
+    }
+
+    while (P.valid != 0) {
+        // the phase after this one: the next step of this item, or this
+        // block's next item (descriptor read now, used after the build)
+        const Phase N = P.step + 1 < job.C ? load_phase(job, P.w, P.step + 1)
+                                           : load_phase(job, P.w + gridDim.x, 0);
+        cp_async_wait_all();
+        __syncthreads();  // codebook + inputs landed; previous lookups done
+        if (P.valid > 0) build_table(lut, cb_s, xs_s, job.x_dtype, P.d.type, lane, warp);
+        __syncthreads();
+        if (N.valid > 0) {
+            issue_x(job, N, xs_s);
+            const uint8_t *ncb = ph_cb(job, N);
+            if (ncb != cb_loaded) {
+                issue_cb(ncb, cb_s);
+                cb_loaded = ncb;
+            }
+        }
+        cp_async_commit();
+        WarpPlan Wn;
+        Wn.tile = nullptr;
+        Wn.tstride = 0;
+        Wn.nt = 0;
+        if (N.valid > 0) Wn = warp_plan(job, N, lane, warp);
+        if (P.valid > 0) {
+            const WarpPlan W = warp_plan(job, P, lane, warp);
+            // tile i of the next phase must land in ring slot i % 2: the
+            // hand-over works when this warp's tile count is even
+            const int nt_next = (W.nt > 0 && (W.nt % 2) == 0) ? min(Wn.nt, 2) : 0;
+            if (P.d.type == 0)
+                stream_phase<0>(job, P, W, Wn, nt_next, buf, lut, sacc, lane, warp);
+            else
+                stream_phase<1>(job, P, W, Wn, nt_next, buf, lut, sacc, lane, warp);
+            if (nt_next == 0) load_first(Wn, buf);
+        } else {
+            load_first(Wn, buf);
+        }
+        P = N;
+    }
+    cp_async_wait_all();
 }
 
 // ---------------------------------------------------------------- reductions
@@ -511,27 +630,36 @@ cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
 
 }  // namespace
 
+rvq_status launch_lut_plan(const LutJob &ja, const LutJob *jb, cudaStream_t stream, bool pdl) {
+    const int na = lut_items(ja) / ja.S;
+    const int nb = jb ? lut_items(*jb) / jb->S : 0;
+    if (na + nb == 0) return RVQ_OK;
+    LutJob b = jb ? *jb : LutJob{};
+    if (!jb) b.n_pairs = 0;
+    RVQ_CUDA(launch_ex(plan_kernel, dim3((na + nb + 255) / 256), dim3(256), 0, stream, pdl, ja, b));
+    return RVQ_OK;
+}
+
 rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl) {
     static int attr_done[64] = {0};
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
-    const size_t smem = kLutBytes + kCbBytes + (size_t)kMaxAccRows * 2 * sizeof(float);
     if (dev < 64 && !attr_done[dev]) {
         RVQ_CUDA(cudaFuncSetAttribute(lut_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem));
+                                      kSmemBytes));
         attr_done[dev] = 1;
     }
     if (job.rows / job.S > kMaxSplitRows || (job.C > 1 && job.rows / job.S > kMaxAccRows) ||
-        (job.rows / 32) % job.S != 0 ||
-        job.G % (2 * job.C) != 0) {
+        (job.rows / 32) % job.S != 0 || job.G % (2 * job.C) != 0 || !job.desc) {
         set_error("lut_gemv: bad split (rows %d, S %d, G %d, C %d)", job.rows, job.S, job.G,
                   job.C);
         return RVQ_EINVAL;
     }
-    const int items = lut_items(job);
-    if (items == 0) return RVQ_OK;
-    dim3 grid(items, job.n_mat);
-    RVQ_CUDA(launch_ex(lut_gemv_kernel, grid, dim3(NT), smem, stream, pdl, job));
+    const int work = lut_items(job) * job.n_mat;
+    if (work == 0) return RVQ_OK;
+    const int grid = work < num_sms() ? work : num_sms();
+    RVQ_CUDA(launch_ex(lut_gemv_kernel, dim3(grid), dim3(NT), (size_t)kSmemBytes, stream, pdl,
+                       job));
     return RVQ_OK;
 }
 
