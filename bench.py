@@ -49,6 +49,22 @@ KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_red
 DOMINANT = "lut_gemv_gate_up"
 
 
+def load_traffic(name):
+    """DRAM bytes per launch of `name` from the committed ncu summary, or None
+    when the kernel source changed since that capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "lut_gemv_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(name)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -238,7 +254,8 @@ def run_gpu(args, rank, world, local_rank):
     achieved = gu_bytes / (avg[DOMINANT] / 1e3) / 1e9
     roofline = {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "peak_source": peak_kind, "traffic": None,
+                "peak_source": peak_kind,
+                "traffic": load_traffic(DOMINANT) if s.E == 256 and batch == 1 else None,
                 "algorithmic_bytes_per_launch": int(gu_bytes),
                 "avg_launch_us": round(avg[DOMINANT] * 1e3, 2)}
 

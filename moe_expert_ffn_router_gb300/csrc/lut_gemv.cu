@@ -247,10 +247,12 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
 // One 32-row x 32-chunk code tile (6 words of 16 B per lane) against the
 // table.  Two tokens (type 0): one permute + one 8-byte LDS per code byte
 // gives both tokens' entries.  One token (type 1): one permute + one 4-byte
-// LDS per code byte, two lookups per packed add.  aux[t] carries the lane's
-// rotated column offset (and, for type 1, the table half) in bits 0..7.
+// LDS per code byte, two lookups per packed add.  The lane's rotated column
+// offset for step t (and, for type 1, the table half) is byte (t & 1) of
+// aux2[t >> 1]; bytes 2..3 of aux2 are zero, so a single byte permute
+// assembles the shared-memory address (code << 8) | offset.
 template <int TYPE>
-__device__ __forceinline__ uint64_t tile_lookups(const uint4 (&c)[6], const uint32_t (&aux)[32],
+__device__ __forceinline__ uint64_t tile_lookups(const uint4 (&c)[6], const uint32_t (&aux2)[16],
                                                  const uint8_t *lut) {
     uint64_t acc = 0;
 #pragma unroll
@@ -263,16 +265,18 @@ __device__ __forceinline__ uint64_t tile_lookups(const uint4 (&c)[6], const uint
                 if constexpr (TYPE == 0) {
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
-                        const uint32_t idx = prmt(w, aux[h * 16 + q * 4 + b], 0x7604u | (b << 4));
+                        const int t = h * 16 + q * 4 + b;
+                        const uint32_t idx =
+                            prmt(w, aux2[t >> 1], 0x7600u | (b << 4) | (4 + (t & 1)));
                         acc = fadd2(acc, *reinterpret_cast<const uint64_t *>(
                                              lut + s * kLutStageBytes + idx));
                     }
                 } else {
 #pragma unroll
                     for (int b = 0; b < 4; b += 2) {
-                        const uint32_t i0 = prmt(w, aux[h * 16 + q * 4 + b], 0x7604u | (b << 4));
-                        const uint32_t i1 =
-                            prmt(w, aux[h * 16 + q * 4 + b + 1], 0x7604u | ((b + 1) << 4));
+                        const int t = h * 16 + q * 4 + b;  // even: t and t + 1 share aux2
+                        const uint32_t i0 = prmt(w, aux2[t >> 1], 0x7604u | (b << 4));
+                        const uint32_t i1 = prmt(w, aux2[t >> 1], 0x7605u | ((b + 1) << 4));
                         const float v0 = *reinterpret_cast<const float *>(lut + s * kLutStageBytes + i0);
                         const float v1 = *reinterpret_cast<const float *>(lut + s * kLutStageBytes + i1);
                         acc = fadd2(acc, pk2(v0, v1));
@@ -414,10 +418,15 @@ __device__ __forceinline__ void stream_phase(const LutJob &job, const Phase &P,
         pA = part + ((size_t)e * nslot + slotA + u) * job.rows + row0 + lane;
         pB = pA;
     }
-    uint32_t aux[32];
+    uint32_t aux2[16];
 #pragma unroll
-    for (int t = 0; t < 32; ++t)
-        aux[t] = TYPE == 0 ? (((lane + t) & 31) << 3) : ((((lane + t) & 31) << 2) | (u << 7));
+    for (int p = 0; p < 16; ++p) {
+        const uint32_t c0 = TYPE == 0 ? (((lane + 2 * p) & 31) << 3)
+                                      : ((((lane + 2 * p) & 31) << 2) | (u << 7));
+        const uint32_t c1 = TYPE == 0 ? (((lane + 2 * p + 1) & 31) << 3)
+                                      : ((((lane + 2 * p + 1) & 31) << 2) | (u << 7));
+        aux2[p] = c0 | (c1 << 8);
+    }
     const uint8_t *next = W.tile + 2 * W.tstride;  // tile i + 2 of this phase
     const uint8_t *next_n = Wn.tile;               // then tiles of the next phase
     int left_n = nt_next;
@@ -426,7 +435,7 @@ __device__ __forceinline__ void stream_phase(const LutJob &job, const Phase &P,
         for (int dd = 0; dd < 2; ++dd) {
             const int i = i0 + dd;
             if (i < W.nt) {
-                const uint64_t acc = tile_lookups<TYPE>(buf[dd], aux, lut);
+                const uint64_t acc = tile_lookups<TYPE>(buf[dd], aux2, lut);
                 if (i + 2 < W.nt) {
                     load_tile(buf[dd], next);
                     next += W.tstride;
