@@ -252,6 +252,21 @@ rvq_status moe_expert_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
                           const int32_t *pairs_dev, float *y_pair_dev, void *ws_dev,
                           size_t ws_bytes, rvq_stream_t stream);
 
+/* As moe_expert_ffn, with per-expert dispatch to the tensor-core path.
+ * Experts whose group holds at least tc_min_tokens tokens are computed by
+ * the prefill path: their codes are decoded tile by tile to bf16 in shared
+ * memory (W = C1[c1] + C2[c2] + C3[c3], rounded to bf16) and multiplied with
+ * bf16 activations on the tensor cores (tcgen05, fp32 accumulators in TMEM):
+ * gate and up GEMMs, h = silu(g) * u rounded to bf16, down GEMM.  Results of
+ * those experts carry bf16 rounding (the tests hold them to 2e-2 x RMS).
+ * tc_min_tokens <= 0: every expert takes the lookup-table path (identical to
+ * moe_expert_ffn); 1: every expert takes the tensor-core path.  A bounded
+ * device wait that expires sets RVQ_DEV_ERR_TIMEOUT. */
+rvq_status moe_expert_ffn_ex(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
+                             int32_t n, int32_t k, const int32_t *offsets_dev,
+                             const int32_t *pairs_dev, float *y_pair_dev, void *ws_dev,
+                             size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream);
+
 /* Weighted combine plus residual: out[t][c] = residual[t][c] +
  * sum_slot topk_w[t][slot] * y_pair[t*k + slot][c], fp32.  residual [n][d]
  * of rdt (dev), out fp32 [n][d] (dev); out may alias residual only if rdt is

@@ -69,6 +69,8 @@ _SIGS = {
     "moe_route": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_workspace_bytes": (_sz, [_BANKP, _i32, _i32]),
     "moe_expert_ffn": (_i32, [_BANKP, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_expert_ffn_ex": (_i32, [_BANKP, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _i32,
+                                 _vp]),
     "moe_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),
     "moe_layer_forward": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
                                  _vp, _vp, _vp, _sz, _vp, _vp]),
@@ -233,6 +235,13 @@ def moe_expert_ffn(bank, x, n, k, offsets, pairs, y_pair, ws, stream=None):
     _check("moe_expert_ffn",
            _lib.moe_expert_ffn(ctypes.byref(bank), _p(x), _dt(x), n, k, _p(offsets), _p(pairs),
                                _p(y_pair), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_expert_ffn_ex(bank, x, n, k, offsets, pairs, y_pair, ws, tc_min_tokens, stream=None):
+    _check("moe_expert_ffn_ex",
+           _lib.moe_expert_ffn_ex(ctypes.byref(bank), _p(x), _dt(x), n, k, _p(offsets), _p(pairs),
+                                  _p(y_pair), _p(ws), _nbytes(ws), int(tc_min_tokens),
+                                  _stream(stream)))
 
 
 def moe_combine(y_pair, topk_w, n, k, d, residual, out, stream=None):

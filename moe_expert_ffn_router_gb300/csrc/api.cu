@@ -108,6 +108,10 @@ FfnPlan plan_ffn(int d, int f, int n_pairs, int E) {
     off = align256(off + (size_t)((d / 256) / (2 * P.C_gu)) * n_pairs * sizeof(ItemDesc));
     P.off_desc_d = off;
     off = align256(off + (size_t)((f / 256) / (2 * P.C_d)) * n_pairs * sizeof(ItemDesc));
+    P.off_h16 = off;
+    off = align256(off + (size_t)n_pairs * f * 2);
+    P.off_ypair = off;
+    off = align256(off + (size_t)n_pairs * d * 4);
     P.total = off;
     return P;
 }
@@ -414,7 +418,7 @@ static LutJob ffn_job(const rvq_moe_bank *bank, const RecordLayout &L, int n_pai
 static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                           int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
                           void *ws_dev, const FfnPlan &P, cudaStream_t st, void **marks,
-                          bool pdl) {
+                          bool pdl, int32_t tc_min_tokens = 0) {
     auto mark = [&](int i) -> rvq_status {
         if (marks) RVQ_CUDA(cudaEventRecord((cudaEvent_t)marks[i], st));
         return RVQ_OK;
@@ -465,6 +469,7 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     dn.offsets = offsets_dev;
     dn.pairs = pairs_dev;
     dn.desc = (ItemDesc *)(ws + P.off_desc_d);
+    gu.tc_min_tokens = dn.tc_min_tokens = tc_min_tokens;
     RVQ_TRY(launch_lut_plan(gu, &dn, st, pdl));
     RVQ_TRY(mark(0));
     RVQ_TRY(launch_lut_gemv(gu, st, pdl));
@@ -473,6 +478,54 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     RVQ_TRY(mark(2));
     RVQ_TRY(launch_lut_gemv(dn, st, pdl));
     return mark(3);
+}
+
+// Tensor-core (prefill) path for experts with at least tc_min_tokens tokens:
+// gate/up GEMMs with the SwiGLU epilogue into h (bf16), then the down GEMM
+// writing y fp32 [pair][d] for those experts' pairs.
+static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
+                             int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
+                             void *ws_dev, const FfnPlan &P, float *y_pair, int32_t tc_min_tokens,
+                             cudaStream_t st, bool pdl) {
+    const RecordLayout L = record_layout(bank->d, bank->f);
+    uint8_t *ws = (uint8_t *)ws_dev;
+    PfJob g = {};
+    g.base = bank->base;
+    g.record_bytes = bank->record_bytes;
+    g.codes_off[0] = L.gate_off;
+    g.codes_off[1] = L.up_off;
+    g.cb_off[0] = L.cb_off;
+    g.cb_off[1] = L.cb_off + RVQ_CODEBOOK_BYTES;
+    g.n_mat = 2;
+    g.rows = bank->f;
+    g.cols = bank->d;
+    g.E = bank->n_experts;
+    g.n_pairs = n * k;
+    g.min_tokens = tc_min_tokens;
+    g.offsets = offsets_dev;
+    g.pairs = pairs_dev;
+    g.x = x_dev;
+    g.x_dtype = (int)xdt;
+    g.x_stride = bank->d;
+    g.x_div = k;
+    g.out = ws + P.off_h16;
+    g.status = (uint32_t *)ws_dev;
+    g.layer = bank->layer;
+    g.d = bank->d;
+    g.f = bank->f;
+    RVQ_TRY(launch_prefill_gemm(g, st, pdl));
+    PfJob dn = g;
+    dn.codes_off[0] = L.down_off;
+    dn.cb_off[0] = L.cb_off + 2 * RVQ_CODEBOOK_BYTES;
+    dn.n_mat = 1;
+    dn.rows = bank->d;
+    dn.cols = bank->f;
+    dn.x = ws + P.off_h16;
+    dn.x_dtype = RVQ_BF16;
+    dn.x_stride = bank->f;
+    dn.x_div = 1;
+    dn.out = y_pair;
+    return launch_prefill_gemm(dn, st, pdl);
 }
 
 static rvq_status check_ffn_args(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
@@ -495,16 +548,32 @@ static rvq_status check_ffn_args(const rvq_moe_bank *bank, const void *x_dev, rv
     return RVQ_OK;
 }
 
+rvq_status moe_expert_ffn_ex(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
+                             int32_t n, int32_t k, const int32_t *offsets_dev,
+                             const int32_t *pairs_dev, float *y_pair_dev, void *ws_dev,
+                             size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream) {
+    RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_expert_ffn"));
+    CHECK_ARG(offsets_dev && pairs_dev && y_pair_dev, "moe_expert_ffn: null pointer");
+    CHECK_ALIGN(y_pair_dev, "moe_expert_ffn: y_pair");
+    const FfnPlan P = plan_ffn(bank->d, bank->f, n * k, bank->n_experts);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (tc_min_tokens != 1) {  // some experts take the lookup-table path
+        RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st, nullptr,
+                        true, tc_min_tokens > 0 ? tc_min_tokens : 0));
+        RVQ_TRY(launch_slot_reduce((float *)((uint8_t *)ws_dev + P.off_dpart), n * k, P.nslot_d,
+                                   bank->d, y_pair_dev, st, true));
+    }
+    if (tc_min_tokens > 0)  // and the rest the tensor-core path (overwrites their y_pair rows)
+        RVQ_TRY(run_ffn_tc(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, y_pair_dev,
+                           tc_min_tokens, st, true));
+    return RVQ_OK;
+}
+
 rvq_status moe_expert_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                           int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
                           float *y_pair_dev, void *ws_dev, size_t ws_bytes, rvq_stream_t stream) {
-    RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_expert_ffn"));
-    CHECK_ARG(offsets_dev && pairs_dev && y_pair_dev, "moe_expert_ffn: null pointer");
-    const FfnPlan P = plan_ffn(bank->d, bank->f, n * k, bank->n_experts);
-    cudaStream_t st = (cudaStream_t)stream;
-    RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st, nullptr, true));
-    return launch_slot_reduce((float *)((uint8_t *)ws_dev + P.off_dpart), n * k, P.nslot_d,
-                              bank->d, y_pair_dev, st, true);
+    return moe_expert_ffn_ex(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, y_pair_dev, ws_dev,
+                             ws_bytes, 0, stream);
 }
 
 rvq_status moe_combine(const float *y_pair_dev, const float *topk_w_dev, int32_t n, int32_t k,

@@ -124,6 +124,8 @@ struct LutJob {
     const int32_t *pairs;      // [n_pairs] (NULL: identity)
     uint32_t *status;
     ItemDesc *desc;            // [items before the row split], from the plan kernel
+    int32_t tc_min_tokens;     // > 0: experts with at least this many tokens are left to the
+                               // tensor-core path (their items are skipped here)
     // record header check
     int32_t check_header;
     int32_t layer, d, f;
@@ -155,12 +157,34 @@ rvq_status launch_pack(const uint8_t *src, int rows, int cols, uint8_t *dst, boo
 rvq_status launch_pack_codebooks(const float *src, float *dst, int count, cudaStream_t stream);
 rvq_status launch_write_header(uint8_t *record, const rvq_expert_header &h, cudaStream_t stream);
 
+// ------------------------------------------------- tensor-core (prefill) job
+struct PfJob {
+    const uint8_t *base;       // bank
+    uint64_t record_bytes;
+    uint64_t codes_off[2];     // gate, up (n_mat 2) or down (n_mat 1)
+    uint64_t cb_off[2];
+    int32_t n_mat;
+    int32_t rows, cols;        // of each matrix
+    int32_t E, n_pairs;
+    int32_t min_tokens;        // experts with fewer tokens are not this launch's work
+    const int32_t *offsets, *pairs;
+    const void *x;             // B rows: x[entry / x_div] (gate/up) or h[entry] (down, bf16)
+    int32_t x_dtype;
+    int64_t x_stride;
+    int32_t x_div;
+    void *out;                 // gate/up: h bf16 [n_pairs][rows]; down: y fp32 [n_pairs][rows]
+    uint32_t *status;
+    int32_t layer, d, f;       // record header check
+};
+rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
+
 // FFN plan: how moe_expert_ffn splits its work (host side, deterministic).
 struct FfnPlan {
     int C_gu, S_gu;   // gate/up: chunk groups per item step run, row splits
     int C_d, S_d;     // down
     int nslot_gu, nslot_d;
-    size_t off_gpart, off_upart, off_h, off_dpart, off_desc_gu, off_desc_d, total;
+    size_t off_gpart, off_upart, off_h, off_dpart, off_desc_gu, off_desc_d;
+    size_t off_h16, off_ypair, total;  // tensor-core path: h bf16, y fp32 [pair][d]
 };
 FfnPlan plan_ffn(int d, int f, int n_pairs, int E);
 int num_sms();

@@ -115,6 +115,10 @@ __device__ ItemDesc plan_one(const LutJob &job, const int32_t *soff, int i) {
             set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
             return d;
         }
+        if (job.tc_min_tokens > 0 && ne >= job.tc_min_tokens) {
+            d.expert = -2;  // the tensor-core path takes this expert
+            return d;
+        }
     }
     const int li = i - per_pair * o;
     const int Q = ne >> 1;
