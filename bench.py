@@ -10,6 +10,12 @@ experts, top-16, 4.23 GB of RVQ codes resident in HBM) at batch 1; each step
 takes the next token of a seeded pool, so the routed experts change every
 step and the codes stream from HBM (inputs larger than L2).
 
+Workload k3_prefill2048: the same layer shape over a 2048-token chunk with the
+Zipf-skewed router bias; every expert group runs on the tensor-core path (RVQ
+tiles decoded to bf16 in shared memory, tcgen05 GEMMs).  Its roofline is the
+tensor pipe: useful FLOPs (2 per multiply-add of gate, up and down over every
+routed token) per launch of the gate/up GEMM.
+
 Prints one JSON line (rank 0).  Multi-GPU (torchrun): independent replicas,
 no collective on the data path; value = all ranks' weights / max time.
 """
@@ -43,10 +49,16 @@ WORKLOADS = {
     "decode_d2048_b1": (1, 1),
     "decode_d2048_b4": (1, 4),
     "decode_d2048_b16": (1, 16),
+    "k3_prefill2048": (4, 2048),
 }
 KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
            "lut_gemv_down", "combine"]
 DOMINANT = "lut_gemv_gate_up"
+# event intervals of the layer call when every expert takes the tensor-core path
+KERNELS_TC = ["router_logits", "route", "lut_experts", "prefill_gate_up", "prefill_down",
+              "unused", "combine"]
+DOMINANT_TC = "prefill_gate_up"
+TC_LAUNCHES_PER_STEP = 5   # router logits, route, gate/up GEMM, down GEMM, combine
 
 
 def load_traffic(name):
@@ -65,12 +77,16 @@ def load_traffic(name):
     return int(rec["dram_bytes_per_launch"])
 
 
-def load_peaks():
+def load_peaks(kind="hbm"):
+    """(peak, source): HBM GB/s, or sustained dense bf16 TFLOP/s (the kernels
+    are timed inside a seconds-long loop of steps)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
+        if kind == "tensor":
+            return float(d["bf16_tflops_sustained"]), "measured (sustained bf16)"
         return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+    return (1700.0, "fallback (sustained bf16)") if kind == "tensor" else (6800.0, "fallback")
 
 
 # ------------------------------------------------------------------ clocks
@@ -152,6 +168,13 @@ def workload_shape(name):
     return config, batch, s
 
 
+def router_bias(config, src):
+    wl = W.WORKLOADS[config]
+    if wl.kind != "prefill":
+        return None
+    return W.zipf_bias(src.lseed, src.shape.E, wl.zipf_beta)
+
+
 def build_layer(config, device, k=None, shape=None):
     from moe_expert_ffn_router_gb300.layer import MoeLayer
     s = shape or W.WORKLOADS[config].shape
@@ -160,7 +183,7 @@ def build_layer(config, device, k=None, shape=None):
     for e in range(s.E):
         mats = [(src.codes(e, m), src.codebooks(e, m)) for m in range(3)]
         L.load_expert(e, mats[0][0], mats[1][0], mats[2][0], np.stack([c for _, c in mats]))
-    L.set_router(src.router_weight())
+    L.set_router(src.router_weight(), router_bias(config, src))
     L.validate()
     return L, src
 
@@ -172,9 +195,15 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     config, batch, s = workload_shape(args.workload)
+    prefill = W.WORKLOADS[config].kind == "prefill"
+    tc_min = 1 if prefill else 0
+    kernels = KERNELS_TC if prefill else KERNELS
     L, src = build_layer(config, dev, shape=s)
-    pool = max(64, 4 * batch)
-    pool_bits = src.tokens_bf16(pool * batch if batch > 1 else pool)
+    if prefill:
+        pool_bits = src.tokens_bf16(2 * batch)          # two chunks, alternating
+    else:
+        pool = max(64, 4 * batch)
+        pool_bits = src.tokens_bf16(pool * batch if batch > 1 else pool)
     xs = torch.from_numpy(pool_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     xs = xs.reshape(-1, batch, s.d)
     nsteps = xs.shape[0]
@@ -184,7 +213,7 @@ def run_gpu(args, rank, world, local_rank):
     cb_bytes_per_expert = 3 * rvq.RVQ_CODEBOOK_BYTES
 
     def step(i, events=None):
-        return L.forward(xs[i % nsteps], bufs, events=events)
+        return L.forward(xs[i % nsteps], bufs, events=events, tc_min_tokens=tc_min)
 
     # unique experts per step (from the routing the GPU computed); the pool
     # is replayed identically in the timed loop, so count once per pool entry
@@ -239,25 +268,43 @@ def run_gpu(args, rank, world, local_rank):
     for e in evs:
         e.record()
     torch.cuda.synchronize()
-    per = {k: [] for k in KERNELS}
+    per = {k: [] for k in kernels}
     for i in range(args.steps):
         step(args.warmup + i, events=evs)
         torch.cuda.synchronize()
-        for j, name in enumerate(KERNELS):
+        for j, name in enumerate(kernels):
             per[name].append(evs[j].elapsed_time(evs[j + 1]))
-    avg = {k: float(np.mean(v)) for k, v in per.items()}
-    # algorithmic bytes of the gate/up launch: gate + up codes and codebooks of
-    # every unique selected expert
-    gu_bytes = np.mean([uniq[j] for j in steps_idx]) * 2 * (
-        3 * s.d * s.f // 8 + rvq.RVQ_CODEBOOK_BYTES)
-    peak, peak_kind = load_peaks()
-    achieved = gu_bytes / (avg[DOMINANT] / 1e3) / 1e9
-    roofline = {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "peak_source": peak_kind,
-                "traffic": load_traffic(DOMINANT) if s.E == 256 and batch == 1 else None,
-                "algorithmic_bytes_per_launch": int(gu_bytes),
-                "avg_launch_us": round(avg[DOMINANT] * 1e3, 2)}
+    avg = {k: float(np.mean(v)) for k, v in per.items() if k != "unused"}
+    if prefill:
+        # useful FLOPs: 2 per multiply-add, gate + up (2 d f) then down (d f)
+        # for each of the n k routed (token, expert) pairs
+        pairs = batch * s.k
+        gu_flops = 2.0 * 2 * s.d * s.f * pairs
+        dn_flops = 2.0 * s.d * s.f * pairs
+        peak, peak_kind = load_peaks("tensor")
+        achieved = gu_flops / (avg[DOMINANT_TC] / 1e3) / 1e12
+        ffn_tflops = (gu_flops + dn_flops) / (
+            (avg["prefill_gate_up"] + avg["prefill_down"]) / 1e3) / 1e12
+        roofline = {"kernel": DOMINANT_TC, "bound": "tensor", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "peak_source": peak_kind, "traffic": None,
+                    "algorithmic_flops_per_launch": int(gu_flops),
+                    "avg_launch_us": round(avg[DOMINANT_TC] * 1e3, 2),
+                    "ffn_tflops": round(ffn_tflops, 1),
+                    "ffn_frac": round(ffn_tflops / peak, 4)}
+    else:
+        # algorithmic bytes of the gate/up launch: gate + up codes and
+        # codebooks of every unique selected expert
+        gu_bytes = np.mean([uniq[j] for j in steps_idx]) * 2 * (
+            3 * s.d * s.f // 8 + rvq.RVQ_CODEBOOK_BYTES)
+        peak, peak_kind = load_peaks()
+        achieved = gu_bytes / (avg[DOMINANT] / 1e3) / 1e9
+        roofline = {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "peak_source": peak_kind,
+                    "traffic": load_traffic(DOMINANT) if s.E == 256 and batch == 1 else None,
+                    "algorithmic_bytes_per_launch": int(gu_bytes),
+                    "avg_launch_us": round(avg[DOMINANT] * 1e3, 2)}
 
     # ---- end to end through host buffers ----
     pinned_in = torch.from_numpy(pool_bits.view(np.int16).copy()).reshape(-1, batch, s.d)
@@ -266,14 +313,14 @@ def run_gpu(args, rank, world, local_rank):
     xbuf = torch.empty((batch, s.d), dtype=torch.bfloat16, device=dev)
     for i in range(args.warmup):
         xbuf.view(torch.int16).copy_(pinned_in[i % nsteps], non_blocking=True)
-        L.forward(xbuf, bufs)
+        L.forward(xbuf, bufs, tc_min_tokens=tc_min)
         pinned_out.copy_(bufs["out"], non_blocking=True)
     barrier()
     e0.record()
     for i in range(args.steps):
         j = (args.warmup + i) % nsteps
         xbuf.view(torch.int16).copy_(pinned_in[j], non_blocking=True)
-        L.forward(xbuf, bufs)
+        L.forward(xbuf, bufs, tc_min_tokens=tc_min)
         pinned_out.copy_(bufs["out"], non_blocking=True)
     e1.record()
     barrier()
@@ -291,53 +338,67 @@ def run_gpu(args, rank, world, local_rank):
     res = dict(value=value, ms=ms, code_gbs=code_gbs, tok_s=tok_s, roofline=roofline, e2e=e2e,
                clocks=clocks, kernels_us={k: round(v * 1e3, 2) for k, v in avg.items()},
                uniq_mean=float(np.mean([uniq[j] for j in steps_idx])),
-               launches=len(KERNELS) * args.steps, config=config, batch=batch, shape=s)
+               launches=(TC_LAUNCHES_PER_STEP if prefill else len(KERNELS)) * args.steps,
+               config=config, batch=batch, shape=s, prefill=prefill)
     del L
     return res
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_sample(config, batch, tokens, src=None, shape=None):
-    """Time the oracle (as it stands, one thread) on `tokens` tokens of the
-    workload.  Returns (Gweights/s, seconds, weights)."""
+def oracle_sample(config, tokens, src=None, shape=None):
+    """Time the oracle (as it stands, one thread) on `tokens` tokens through the
+    whole oracle layer.  Returns seconds per token."""
     import oracle
     import synth
     s = shape or W.WORKLOADS[config].shape
     src = src or W.ExpertSource(config, 0, s)
     wr = src.router_weight()
+    bias = router_bias(config, src)
     x64 = synth.bf16_to_f32(src.tokens_bf16(tokens)).astype(np.float64)
-    lg = oracle.router_logits(wr, x64).astype(np.float32)
+    lg = oracle.router_logits(wr, x64, bias).astype(np.float32)
     idx, _, _ = oracle.route(lg, s.k)
     cache = {}
     for e in sorted(set(idx.reshape(-1).tolist())):
         cache[e] = tuple((src.codes(e, m), src.codebooks(e, m)) for m in range(3))
     t0 = time.perf_counter()
-    weights = 0
     for t in range(tokens):
-        r = oracle.moe_layer(lambda e: cache[e], wr, x64[t:t + 1], s.k, s.d, s.f)
-        weights += len(set(r["idx"].reshape(-1).tolist())) * 3 * s.d * s.f
-    dt = time.perf_counter() - t0
-    return weights / dt / 1e9, dt, weights
+        oracle.moe_layer(lambda e: cache[e], wr, x64[t:t + 1], s.k, s.d, s.f, bias=bias)
+    return (time.perf_counter() - t0) / tokens
+
+
+def oracle_unique_experts(config, batch, src, s):
+    """Distinct experts the oracle router selects for the workload's first batch."""
+    import oracle
+    import synth
+    x64 = synth.bf16_to_f32(src.tokens_bf16(batch)).astype(np.float64)
+    lg = oracle.router_logits(src.router_weight(), x64, router_bias(config, src))
+    idx, _, _ = oracle.route(lg.astype(np.float32), s.k)
+    return len(set(idx.reshape(-1).tolist()))
 
 
 def reference_arm(args, rank):
-    """The oracle as the reference implementation: each step evaluates m of
-    the experts one token selects (all k when the step budget allows), so the
-    whole --steps/--warmup run stays near a minute of CPU time."""
+    """The oracle as the reference implementation.  Each step evaluates m of
+    the (token, expert) pairs of one batch (all of them when the step budget
+    allows), so the whole --steps/--warmup run stays near a minute of CPU
+    time; a step's time is the measured time per pair times the batch's n k
+    pairs, and the value counts the distinct experts' weights of the batch,
+    as the GPU arm does."""
     if rank != 0:
         return
     import oracle
     import synth
     config, batch, s = workload_shape(args.workload)
     src = W.ExpertSource(config, 0, s)
-    per_expert_s = 0.15 * (s.d * s.f) / (7168 * 2048)
-    m = int(max(1, min(s.k, 60.0 / ((args.steps + args.warmup) * per_expert_s))))
+    per_pair_s = 0.15 * (s.d * s.f) / (7168 * 2048)
+    m = int(max(1, min(s.k * batch, 60.0 / ((args.steps + args.warmup) * per_pair_s))))
     wr = src.router_weight()
+    bias = router_bias(config, src)
     ntok = max(1, (args.steps + args.warmup) * m // s.k + 1)
     x64 = synth.bf16_to_f32(src.tokens_bf16(ntok)).astype(np.float64)
-    idx, _, _ = oracle.route(oracle.router_logits(wr, x64).astype(np.float32), s.k)
+    idx, _, _ = oracle.route(oracle.router_logits(wr, x64, bias).astype(np.float32), s.k)
     work = [(t, int(e)) for t in range(ntok) for e in idx[t]]
-    times, weights, pos = 0.0, 0, 0
+    uniq = s.k if batch == 1 else oracle_unique_experts(config, batch, src, s)
+    times, npairs, pos = 0.0, 0, 0
     for i in range(args.warmup + args.steps):
         chunk = work[pos:pos + m]
         pos += m
@@ -349,19 +410,22 @@ def reference_arm(args, rank):
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times += dt
-            weights += len(chunk) * 3 * s.d * s.f
-    value = weights / times / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            npairs += len(chunk)
+    step_s = times / npairs * batch * s.k
+    value = uniq * 3 * s.d * s.f / step_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(times / args.steps * 1e3, 2), "higher_is_better": True,
+            "ms_per_step": round(step_s * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload + ":" + W.WORKLOADS[config].name,
                        "batch": batch, "experts": s.E},
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1,
                              "kind": "oracle",
-                             "sample": f"{m} of the {s.k} experts one token selects per step "
-                                       "(oracle expert FFN: explicit dequant + fp64 matmuls)"},
-            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                             "sample": f"{m} (token, expert) pairs of the {batch * s.k} per "
+                                       "step timed (oracle expert FFN: explicit dequant + "
+                                       "fp64 matmuls), scaled to the whole batch; "
+                                       f"{uniq} distinct experts per batch"},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -395,15 +459,17 @@ def main():
         s = r["shape"]
         cpu = None
         if not args.no_cpu_baseline:
-            v, dt, wts = oracle_sample(r["config"], r["batch"], args.oracle_tokens,
-                                       shape=r["shape"])
-            cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            tok_s = oracle_sample(r["config"], args.oracle_tokens, shape=r["shape"])
+            v = r["uniq_mean"] * 3 * s.d * s.f / (tok_s * r["batch"]) / 1e9
+            cpu = {"value": round(v, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{args.oracle_tokens} tokens through the whole oracle layer "
-                             f"({wts / 1e9:.2f} G weights, {dt:.1f} s)"}
+                             f"({tok_s:.2f} s per token), scaled to the {r['batch']}-token "
+                             "batch and its distinct experts"}
         line = {
             "metric": METRIC, "value": round(r["value"], 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if r["prefill"] else "f32",
             "data": "synthetic",
             "config": {"workload": args.workload + ":" + W.WORKLOADS[r["config"]].name,
                        "batch": r["batch"],
@@ -411,7 +477,10 @@ def main():
                        "codes_bytes": 3 * (3 * s.d * s.f // 8) * s.E,
                        "l2": f"inputs larger than L2: {3 * (3 * s.d * s.f // 8) * s.E / 1e9:.2f} "
                              "GB code bank (L2 129 MB); token pool rotates routing every step",
-                       "parallelism": f"replicas{world}"},
+                       "parallelism": f"replicas{world}",
+                       "path": ("tensor cores for every expert group (bf16 operands, "
+                                "fp32 accumulate)") if r["prefill"] else
+                               "fp32 lookup tables"},
             "code_byte_gbs": round(r["code_gbs"], 1),
             "layer_tok_s": round(r["tok_s"], 1),
             "unique_experts_per_step": round(r["uniq_mean"], 2),

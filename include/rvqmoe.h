@@ -290,6 +290,18 @@ rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, cons
                              void *ws_dev, size_t ws_bytes, void **events,
                              rvq_stream_t stream);
 
+/* As moe_layer_forward, with the per-expert tensor-core dispatch of
+ * moe_expert_ffn_ex (tc_min_tokens <= 0: lookup tables only).  With dispatch
+ * the event marks are: 0 start, 1 router logits, 2 routing, 3 lookup-table
+ * experts done, 4 tensor-core gate/up GEMM, 5 tensor-core down GEMM, 6 = 5,
+ * 7 combine. */
+rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
+                                const float *bias_dev, const void *x_dev, rvq_dtype xdt, int32_t n,
+                                int32_t k, float *logits_dev, int32_t *topk_idx_dev,
+                                float *topk_w_dev, int32_t *offsets_dev, int32_t *pairs_dev,
+                                float *out_dev, void *ws_dev, size_t ws_bytes,
+                                int32_t tc_min_tokens, void **events, rvq_stream_t stream);
+
 /* --------------------------------------------------------------------------
  * Workspace status block.
  * rvq_ws_clear: zero the status block (async).  Call once per workspace.

@@ -74,6 +74,8 @@ _SIGS = {
     "moe_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),
     "moe_layer_forward": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
                                  _vp, _vp, _vp, _sz, _vp, _vp]),
+    "moe_layer_forward_ex": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _vp, _sz, _i32, _vp, _vp]),
     "rvq_ws_clear": (_i32, [_vp, _vp]),
     "rvq_ws_status": (_i32, [_vp, ctypes.POINTER(_u32), _vp]),
 }
@@ -250,15 +252,16 @@ def moe_combine(y_pair, topk_w, n, k, d, residual, out, stream=None):
 
 
 def moe_layer_forward(bank, wr, bias, x, n, k, logits, topk_idx, topk_w, offsets, pairs, out,
-                      ws, events=None, stream=None):
+                      ws, events=None, stream=None, tc_min_tokens=0):
     ev = None
     if events is not None:
         assert len(events) == MOE_LAYER_EVENTS
         ev = (ctypes.c_void_p * MOE_LAYER_EVENTS)(*[e.cuda_event for e in events])
     _check("moe_layer_forward",
-           _lib.moe_layer_forward(ctypes.byref(bank), _p(wr), _p(bias), _p(x), _dt(x), n, k,
-                                  _p(logits), _p(topk_idx), _p(topk_w), _p(offsets), _p(pairs),
-                                  _p(out), _p(ws), _nbytes(ws), ev, _stream(stream)))
+           _lib.moe_layer_forward_ex(ctypes.byref(bank), _p(wr), _p(bias), _p(x), _dt(x), n, k,
+                                     _p(logits), _p(topk_idx), _p(topk_w), _p(offsets),
+                                     _p(pairs), _p(out), _p(ws), _nbytes(ws), int(tc_min_tokens),
+                                     ev, _stream(stream)))
 
 
 def rvq_ws_clear(ws, stream=None):

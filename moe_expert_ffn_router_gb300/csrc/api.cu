@@ -486,7 +486,7 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
 static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                              int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
                              void *ws_dev, const FfnPlan &P, float *y_pair, int32_t tc_min_tokens,
-                             cudaStream_t st, bool pdl) {
+                             cudaStream_t st, bool pdl, void *mid_event = nullptr) {
     const RecordLayout L = record_layout(bank->d, bank->f);
     uint8_t *ws = (uint8_t *)ws_dev;
     PfJob g = {};
@@ -514,6 +514,7 @@ static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dt
     g.d = bank->d;
     g.f = bank->f;
     RVQ_TRY(launch_prefill_gemm(g, st, pdl));
+    if (mid_event) RVQ_CUDA(cudaEventRecord((cudaEvent_t)mid_event, st));
     PfJob dn = g;
     dn.codes_off[0] = L.down_off;
     dn.cb_off[0] = L.cb_off + 2 * RVQ_CODEBOOK_BYTES;
@@ -591,11 +592,12 @@ rvq_status moe_combine(const float *y_pair_dev, const float *topk_w_dev, int32_t
                           (cudaStream_t)stream, false);
 }
 
-rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, const float *bias_dev,
-                             const void *x_dev, rvq_dtype xdt, int32_t n, int32_t k,
-                             float *logits_dev, int32_t *topk_idx_dev, float *topk_w_dev,
-                             int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
-                             void *ws_dev, size_t ws_bytes, void **events, rvq_stream_t stream) {
+rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
+                                const float *bias_dev, const void *x_dev, rvq_dtype xdt, int32_t n,
+                                int32_t k, float *logits_dev, int32_t *topk_idx_dev,
+                                float *topk_w_dev, int32_t *offsets_dev, int32_t *pairs_dev,
+                                float *out_dev, void *ws_dev, size_t ws_bytes,
+                                int32_t tc_min_tokens, void **events, rvq_stream_t stream) {
     RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_layer_forward"));
     CHECK_ARG(wr_dev && logits_dev && topk_idx_dev && topk_w_dev && offsets_dev && pairs_dev &&
                   out_dev,
@@ -618,12 +620,41 @@ rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, cons
     RVQ_TRY(launch_route(logits_dev, n, bank->n_experts, k, topk_idx_dev, topk_w_dev, offsets_dev,
                          pairs_dev, (uint32_t *)ws_dev, st, pdl));
     RVQ_TRY(mark(2));
-    RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st,
-                    events ? events + 3 : nullptr, pdl));
-    float *dpart = (float *)((uint8_t *)ws_dev + P.off_dpart);
-    RVQ_TRY(launch_combine(dpart, P.nslot_d, topk_w_dev, n, k, bank->d, x_dev, (int)xdt, out_dev,
-                           st, pdl));
+    if (tc_min_tokens <= 0) {
+        // lookup-table path only; the down partials are reduced inside the combine
+        RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st,
+                        events ? events + 3 : nullptr, pdl));
+        float *dpart = (float *)((uint8_t *)ws_dev + P.off_dpart);
+        RVQ_TRY(launch_combine(dpart, P.nslot_d, topk_w_dev, n, k, bank->d, x_dev, (int)xdt,
+                               out_dev, st, pdl));
+        return mark(7);
+    }
+    // with tensor-core dispatch: marks 3 = lookup-table experts done, 4 = after the
+    // tensor-core gate/up GEMM, 5 = after the tensor-core down GEMM, 7 = after the combine
+    float *ypair = (float *)((uint8_t *)ws_dev + P.off_ypair);
+    if (tc_min_tokens != 1) {
+        RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st, nullptr,
+                        pdl, tc_min_tokens));
+        RVQ_TRY(launch_slot_reduce((float *)((uint8_t *)ws_dev + P.off_dpart), n * k, P.nslot_d,
+                                   bank->d, ypair, st, pdl));
+    }
+    RVQ_TRY(mark(3));
+    RVQ_TRY(run_ffn_tc(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, ypair,
+                       tc_min_tokens, st, pdl, events ? events[4] : nullptr));
+    RVQ_TRY(mark(5));
+    RVQ_TRY(mark(6));
+    RVQ_TRY(launch_combine(ypair, 1, topk_w_dev, n, k, bank->d, x_dev, (int)xdt, out_dev, st, pdl));
     return mark(7);
+}
+
+rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, const float *bias_dev,
+                             const void *x_dev, rvq_dtype xdt, int32_t n, int32_t k,
+                             float *logits_dev, int32_t *topk_idx_dev, float *topk_w_dev,
+                             int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
+                             void *ws_dev, size_t ws_bytes, void **events, rvq_stream_t stream) {
+    return moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
+                                topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes, 0,
+                                events, stream);
 }
 
 rvq_status rvq_ws_clear(void *ws_dev, rvq_stream_t stream) {

@@ -82,12 +82,15 @@ class MoeLayer:
             ws=self.workspace(n))
 
     # ----------------------------------------------------------------- compute
-    def forward(self, x: torch.Tensor, bufs: dict | None = None, events=None) -> dict:
-        """Whole layer (fused path): out = x + sum_slot w * expert(x)."""
+    def forward(self, x: torch.Tensor, bufs: dict | None = None, events=None,
+                tc_min_tokens: int = 0) -> dict:
+        """Whole layer: out = x + sum_slot w * expert(x).  Experts with at
+        least tc_min_tokens tokens use the tensor-core path (0: none)."""
         n = x.shape[0]
         b = bufs or self.buffers(n)
         moe_layer_forward(self.bank, self.wr, self.bias, x, n, self.k, b["logits"], b["idx"],
-                          b["w"], b["offsets"], b["pairs"], b["out"], b["ws"], events=events)
+                          b["w"], b["offsets"], b["pairs"], b["out"], b["ws"], events=events,
+                          tc_min_tokens=tc_min_tokens)
         return b
 
     def forward_steps(self, x: torch.Tensor) -> dict:
