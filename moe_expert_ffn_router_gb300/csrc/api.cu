@@ -496,7 +496,9 @@ static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dt
     g.codes_off[1] = L.up_off;
     g.cb_off[0] = L.cb_off;
     g.cb_off[1] = L.cb_off + RVQ_CODEBOOK_BYTES;
-    g.n_mat = 2;
+    g.row_off[0] = g.row_off[1] = 0;
+    g.tile_rows = 128;
+    g.mode = PF_MODE_SWIGLU;
     g.rows = bank->f;
     g.cols = bank->d;
     g.E = bank->n_experts;
@@ -516,9 +518,12 @@ static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dt
     RVQ_TRY(launch_prefill_gemm(g, st, pdl));
     if (mid_event) RVQ_CUDA(cudaEventRecord((cudaEvent_t)mid_event, st));
     PfJob dn = g;
-    dn.codes_off[0] = L.down_off;
-    dn.cb_off[0] = L.cb_off + 2 * RVQ_CODEBOOK_BYTES;
-    dn.n_mat = 1;
+    dn.codes_off[0] = dn.codes_off[1] = L.down_off;
+    dn.cb_off[0] = dn.cb_off[1] = L.cb_off + 2 * RVQ_CODEBOOK_BYTES;
+    dn.row_off[0] = 0;
+    dn.row_off[1] = 128;
+    dn.tile_rows = 256;
+    dn.mode = PF_MODE_PLAIN;
     dn.rows = bank->d;
     dn.cols = bank->f;
     dn.x = ws + P.off_h16;

@@ -158,12 +158,16 @@ rvq_status launch_pack_codebooks(const float *src, float *dst, int count, cudaSt
 rvq_status launch_write_header(uint8_t *record, const rvq_expert_header &h, cudaStream_t stream);
 
 // ------------------------------------------------- tensor-core (prefill) job
+constexpr int PF_MODE_SWIGLU = 0;  // gate/up: tiles = gate, up rows; out = h bf16
+constexpr int PF_MODE_PLAIN = 1;   // down: tiles = two row blocks; out = y fp32
 struct PfJob {
     const uint8_t *base;       // bank
     uint64_t record_bytes;
-    uint64_t codes_off[2];     // gate, up (n_mat 2) or down (n_mat 1)
+    uint64_t codes_off[2];     // per A tile: gate, up (SWIGLU) or down, down (PLAIN)
     uint64_t cb_off[2];
-    int32_t n_mat;
+    int32_t row_off[2];        // row of each A tile within the M tile (0, 0 or 0, 128)
+    int32_t tile_rows;         // rows per M tile: 128 (SWIGLU) or 256 (PLAIN)
+    int32_t mode;
     int32_t rows, cols;        // of each matrix
     int32_t E, n_pairs;
     int32_t min_tokens;        // experts with fewer tokens are not this launch's work

@@ -8,37 +8,80 @@
 // Quantization (RVQ)") -- rounded to bf16 and multiplied on the tensor cores.
 //
 // GEMM orientation (swap-AB): A = 128 rows of W x 64 K-columns (K-major), B =
-// up to 256 tokens of the expert's group x 64 K-columns (K-major), D = W x^T
+// up to 256 tokens of one expert's group x 64 K-columns (K-major), D = W x^T
 // (128 rows x N tokens, fp32, in TMEM).  One RVQ chunk (8 weights) is exactly
 // one 16-byte unit of the 128-byte swizzle row, so a decoded chunk is stored
 // with one 128-bit shared-memory store at its swizzled position.
-//  * gate/up launch: two accumulators (gate at TMEM column 0, up at 256); the
-//    epilogue computes h = silu(g) * u and writes it as bf16 [pair][f].
-//  * down launch: one accumulator; the epilogue writes y fp32 [pair][d].
-// Every mbarrier wait is bounded; on expiry the block records
-// RVQ_DEV_ERR_TIMEOUT, frees its TMEM and returns.
+//
+// A work item is (expert, pass of <= 256 tokens, M tile) and carries two A
+// tiles that share the B tile:
+//  * gate/up launch: tile 0 = 128 rows of gate, tile 1 = the same rows of up;
+//    the epilogue computes h = silu(g) * u and writes bf16 h [pair][f].
+//  * down launch: tiles 0 and 1 = rows [256 m, 256 m + 128) and the next 128
+//    rows of down; the epilogue writes fp32 y [pair][d].
+// Items are split into contiguous ranges over a persistent grid (one CTA per
+// SM), so consecutive items of a CTA mostly share the expert and its codebooks.
+//
+// Warp roles (512 threads):
+//  warp 0      TMEM owner; lane 0 issues the MMAs (8 per K step) and commits
+//  warps 1-3   B producers: cp.async gathers of token rows into the B stage
+//  warps 4-7   epilogue: TMEM -> registers -> global (lane quarter = warp % 4)
+//  warps 8-15  A producers: decode code bytes into the two bf16 A tiles
+// The stages (A0, A1, B) form a two-deep ring guarded by full/empty mbarriers;
+// the accumulators (512 TMEM columns: tile 0 at 0, tile 1 at 256) by acc_full
+// and acc_empty.
+//
+// Decoding is bound by shared-memory gathers of codewords, so the codebooks
+// sit in shared memory as fp16 (summed in fp16, then rounded once to bf16) in
+// a bank-private layout: line (stage s, codeword k) is 128 bytes, and 16-byte
+// group q of every line serves lane q of each quarter-warp.  Groups 0-3 hold
+// tile 0's codebook, groups 4-7 tile 1's.  A quarter-warp thus reads eight
+// codewords from eight distinct bank groups whatever the codes are, and the
+// eight rows it decodes have distinct (row mod 8), so its swizzled stores are
+// conflict-free as well.
+//
+// Every wait is bounded (1 s); on expiry the CTA records RVQ_DEV_ERR_TIMEOUT,
+// every role leaves its loop, the MMAs in flight are drained and TMEM is freed.
 #include "internal.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace rvq {
 namespace {
 
-constexpr int PF_NT = 128;                      // 4 warps <-> TMEM lanes 0..127 (rows of the tile)
-constexpr int PF_M = 128;                       // rows of W per tile
-constexpr int PF_NMAX = 256;                    // tokens per pass (MMA N)
-constexpr int PF_KC = 64;                       // K columns per step: one 128-byte swizzle row
-constexpr int kTileA = PF_M * PF_KC * 2;        // 16 KiB
-constexpr int kTileB = PF_NMAX * PF_KC * 2;     // 32 KiB
-constexpr int kCbF32 = 3 * 256 * 8 * 4;         // 24 KiB: one matrix's codebooks, fp32 [s][k][8]
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: a bounded wait, never a hang
+constexpr int PF_THREADS = 512;
+constexpr int PF_NMAX = 256;                     // tokens per pass (MMA N)
+constexpr int PF_KC = 64;                        // K columns per stage (one 128-byte swizzle row)
+constexpr int PF_NST = 2;                        // ring depth
+constexpr int kTileA = 128 * PF_KC * 2;          // 16 KiB
+constexpr int kTileB = PF_NMAX * PF_KC * 2;      // 32 KiB
+constexpr int kStage = 2 * kTileA + kTileB;      // 64 KiB
+constexpr int kCbLine = 128;                     // one (stage, codeword) line
+constexpr int kCbBytes = 3 * 256 * kCbLine;      // 96 KiB
+constexpr int OFF_CB = 0;
+constexpr int OFF_ST = kCbBytes;
+constexpr int OFF_BAR = OFF_ST + PF_NST * kStage;
+// mbarriers, 8 bytes each from OFF_BAR
+constexpr int BAR_FULL = 0;                      // [PF_NST]
+constexpr int BAR_EMPTY = PF_NST;                // [PF_NST]
+constexpr int BAR_ACC_FULL = 2 * PF_NST;
+constexpr int BAR_ACC_EMPTY = 2 * PF_NST + 1;
+constexpr int BAR_DONE = 2 * PF_NST + 2;
+constexpr int BAR_CB = 2 * PF_NST + 3;           // A producers: codebook swap rendezvous
+constexpr int kNumBars = 2 * PF_NST + 4;
+constexpr int OFF_TMEM = OFF_BAR + 8 * kNumBars;
+constexpr int OFF_FLAG = OFF_TMEM + 4;
+constexpr int OFF_Q = OFF_BAR + 128;             // pass prefix [E + 1]
+constexpr int kMaxE = 256;
+constexpr int kPfSmem = OFF_Q + 4 * (kMaxE + 1) + 1024;  // + slack to align the base to 1 KiB
+static_assert(OFF_FLAG + 4 <= OFF_Q, "control block overlaps the pass prefix");
+static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
-// shared memory layout (dynamic, 1024-byte aligned)
-constexpr int OFF_A = 0;                        // 2 A tiles
-constexpr int OFF_B = 2 * kTileA;               // B tile
-constexpr int OFF_CB = OFF_B + kTileB;          // 2 fp32 codebooks
-constexpr int OFF_ENT = OFF_CB + 2 * kCbF32;    // pair entries of the pass [256] int32
-constexpr int OFF_Q = OFF_ENT + PF_NMAX * 4;    // per-expert pass prefix [257] int32
-constexpr int OFF_MISC = OFF_Q + 260 * 4;       // mbarrier, tmem slot, flags
-constexpr int kPfSmem = OFF_MISC + 64 + 1024;  // + slack to align the tile base to 1024 B
+constexpr int kLoaders = 96;                     // B producer threads (warps 1-3)
+constexpr int kDecoders = 256;                   // A producer threads (warps 8-15)
+constexpr uint32_t kFullCount = kLoaders + kDecoders / 32;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: a bounded wait, never a hang
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -82,19 +125,41 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Bounded wait on an mbarrier phase; returns false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.b32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false once another role has
+// aborted, or after kWaitLimitNs (then this thread raises the abort flag and
+// records the timeout).
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag,
+                                          uint32_t *status) {
+    if (mbar_try(mbar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            "selp.b32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(mbar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (mbar_try(mbar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            set_dev_error(status, RVQ_DEV_ERR_TIMEOUT);
+            return false;
+        }
     }
 }
 
@@ -118,224 +183,421 @@ __device__ __forceinline__ uint32_t bf16_bits(float f) {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Code byte of (row r, chunk j, stage s) in the packed tile layout.
-__device__ __forceinline__ uint8_t code_at(const uint8_t *codes, int RB, int r, int j, int s) {
-    const int l = r & 31, g = j >> 5;
-    const int t = ((j & 31) - l) & 31;
-    return codes[((size_t)g * RB + (r >> 5)) * kTileBytes + ((s * 2 + (t >> 4)) * 32 + l) * 16 +
-                 (t & 15)];
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// Three fp16x2 codeword words summed in fp16, rounded once to bf16x2.
+__device__ __forceinline__ uint32_t sum3_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+    const __half2 s = __hadd2(__hadd2(*reinterpret_cast<const __half2 *>(&a),
+                                      *reinterpret_cast<const __half2 *>(&b)),
+                              *reinterpret_cast<const __half2 *>(&c));
+    const float2 f = __half22float2(s);
+    return pack_bf16x2(f.x, f.y);
+}
+
+// Rotate a 32-byte vector left by l bytes (l in 0..31).  The packed code
+// layout stores chunk j of a row with lane l = row mod 32 at byte
+// (j - l) mod 32 of its stage plane; the rotation puts chunk j at byte j.
+__device__ __forceinline__ void derotate(uint32_t (&w)[8], int l) {
+    const int wl = l >> 2;
+    const uint32_t bl = (uint32_t)(l & 3) * 8u;
+    uint32_t a[8], b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (wl & 1) ? w[(i + 7) & 7] : w[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = (wl & 2) ? a[(i + 6) & 7] : a[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (wl & 4) ? b[(i + 4) & 7] : b[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __funnelshift_l(a[(i + 7) & 7], a[i], bl);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 struct PfItem {
-    int valid, e, o, n, npad, mt, j0;
+    int e, o, j0, n, npad, mt;
+    bool valid;
 };
 
-__global__ void __launch_bounds__(PF_NT, 1) prefill_gemm_kernel(const PfJob job) {
+// Work item `it` -> (expert, pass, M tile).  Q[e] = passes before expert e.
+__device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, int MT, int it) {
+    PfItem I;
+    const int pi = it / MT;
+    I.mt = it - pi * MT;
+    int lo = 0, hi = job.E;  // largest e < E with Q[e] <= pi (it has a pass there)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (Q[mid] <= pi) lo = mid; else hi = mid;
+    }
+    I.e = lo;
+    I.o = job.offsets[lo];
+    const int ne = job.offsets[lo + 1] - I.o;
+    I.j0 = (pi - Q[lo]) * PF_NMAX;
+    I.n = min(PF_NMAX, ne - I.j0);
+    I.npad = (I.n + 15) & ~15;
+    const rvq_expert_header *h =
+        reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)lo * job.record_bytes);
+    I.valid = I.n > 0 && h->magic == RVQ_BANK_MAGIC && h->expert == lo && h->layer == job.layer &&
+              h->d == job.d && h->f == job.f && h->record_bytes == job.record_bytes;
+    return I;
+}
+
+__global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob job) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle is a function of shared-address bits 4..9: tiles
     // must start on 1024-byte boundaries of the shared window
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    int32_t *ent = reinterpret_cast<int32_t *>(smem + OFF_ENT);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + OFF_BAR;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
     int32_t *Q = reinterpret_cast<int32_t *>(smem + OFF_Q);
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 8);
-    int *flag = reinterpret_cast<int *>(smem + OFF_MISC + 12);
-    PfItem *itp = reinterpret_cast<PfItem *>(smem + OFF_MISC + 16);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int MT = job.rows / PF_M;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int MT = job.rows / job.tile_rows;
+    const int KS = job.cols / PF_KC;
+
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- item: (expert e, pass of <= 256 tokens, M tile) ----------------
-    if (tid == 0) {
-        PfItem it = {0, 0, 0, 0, 0, 0, 0};
-        int acc = 0;
-        bool ok = job.offsets[0] == 0 && job.offsets[job.E] == job.n_pairs;
-        for (int e = 0; e < job.E && ok; ++e) {
+    // ---- setup: pass prefix (warp 1), barriers + TMEM (warp 0) ----------
+    if (warp == 1) {
+        const int E = job.E;
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int cnt = 0;
+        bool ok = true;
+        for (int e = e0; e < e1; ++e) {
             const int ne = job.offsets[e + 1] - job.offsets[e];
-            if (ne < 0) ok = false;
-            Q[e] = acc;
-            acc += job.min_tokens <= ne ? (ne + PF_NMAX - 1) / PF_NMAX : 0;
+            ok = ok && ne >= 0;
+            cnt += (ne >= job.min_tokens) ? (ne + PF_NMAX - 1) / PF_NMAX : 0;
         }
-        Q[job.E] = acc;
-        const int pi = blockIdx.x / MT;
-        if (!ok) {
-            set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
-        } else if (pi < acc) {
-            int lo = 0, hi = job.E;  // largest e with Q[e] <= pi (and a pass there)
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (Q[mid] <= pi) lo = mid; else hi = mid;
-            }
-            const int e = lo;
+        int incl = cnt;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, s);
+            if (lane >= s) incl += v;
+        }
+        int pre = incl - cnt;
+        for (int e = e0; e < e1; ++e) {
+            Q[e] = pre;
             const int ne = job.offsets[e + 1] - job.offsets[e];
-            const int np = pi - Q[e];
-            it.e = e;
-            it.o = job.offsets[e];
-            it.j0 = np * PF_NMAX;
-            it.n = min(PF_NMAX, ne - it.j0);
-            it.npad = (it.n + 15) & ~15;
-            it.mt = blockIdx.x % MT;
-            it.valid = it.n > 0;
-            const rvq_expert_header *h =
-                reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)e * job.record_bytes);
-            if (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
-                h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes) {
-                set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
-                it.valid = 0;
-            }
+            pre += (ne >= job.min_tokens) ? (ne + PF_NMAX - 1) / PF_NMAX : 0;
         }
-        *itp = it;
-        *flag = 0;
-    }
-    __syncthreads();
-    const PfItem it = *itp;
-    if (!it.valid) return;
-    asm volatile("griddepcontrol.launch_dependents;");
-
-    const uint8_t *rec = job.base + (uint64_t)it.e * job.record_bytes;
-    // pair entries of this pass; codebooks -> fp32 [s][k][8] (each weight is
-    // rounded to bf16 once, after the three codewords are summed)
-    for (int j = tid; j < it.n; j += PF_NT) {
-        const int p = job.pairs[it.o + it.j0 + j];
-        ent[j] = (p >= 0 && p < job.n_pairs) ? p : -1;
-        if (p < 0 || p >= job.n_pairs) set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
-    }
-    for (int m = 0; m < job.n_mat; ++m) {
-        const float *cbp = reinterpret_cast<const float *>(rec + job.cb_off[m]);
-        float *cbs = reinterpret_cast<float *>(smem + OFF_CB + m * kCbF32);
-        for (int x = tid; x < 3 * 256 * 8; x += PF_NT) {
-            const int s = x / 2048, k = (x / 8) % 256, i = x % 8;
-            cbs[x] = cbp[((s * 128 + k / 2) * 8 + i) * 2 + (k & 1)];
-        }
-    }
-    if (warp == 0) {
+        ok = __all_sync(0xffffffffu, ok) && job.offsets[0] == 0 && job.offsets[E] == job.n_pairs;
+        if (lane == 31) Q[E] = ok ? incl : 0;
+        if (!ok && lane == 0) set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+    } else if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(job.n_mat == 2 ? 512 : 256));
+                         sbase + OFF_TMEM),
+                     "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar)), "r"(1));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (lane == 0) {
+            for (int s = 0; s < PF_NST; ++s) {
+                mbar_init(bar(BAR_FULL + s), kFullCount);
+                mbar_init(bar(BAR_EMPTY + s), 1);
+            }
+            mbar_init(bar(BAR_ACC_FULL), 1);
+            mbar_init(bar(BAR_ACC_EMPTY), 4);
+            mbar_init(bar(BAR_DONE), 1);
+            mbar_init(bar(BAR_CB), kDecoders / 32);
+            *abort_flag = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = *tmem_slot;
+    asm volatile("griddepcontrol.launch_dependents;");
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM);
 
-    const int RB = job.rows / 32;
-    const int row = tid;                           // this thread's row within the tile
-    const int R = it.mt * PF_M + row;              // row of W
-    const uint32_t idesc = idesc_bf16(PF_M, it.npad);
-    const int ksteps = job.cols / PF_KC;
-    const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
-    bool ok = true;
+    const int total = Q[job.E] * MT;
+    const int it0 = (int)((int64_t)blockIdx.x * total / gridDim.x);
+    const int it1 = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
 
-    for (int ks = 0; ks < ksteps && ok; ++ks) {
-        // (a) decode this thread's row: 8 chunks per matrix, one 16-byte
-        //     swizzle unit each
-        for (int m = 0; m < job.n_mat; ++m) {
-            const uint8_t *codes = rec + job.codes_off[m];
-            const float4 *cbs = reinterpret_cast<const float4 *>(smem + OFF_CB + m * kCbF32);
-            uint8_t *tile = smem + OFF_A + m * kTileA;
-#pragma unroll 2
-            for (int cc = 0; cc < 8; ++cc) {
-                const int j = ks * 8 + cc;
-                const int k0 = code_at(codes, RB, R, j, 0);
-                const int k1 = code_at(codes, RB, R, j, 1);
-                const int k2 = code_at(codes, RB, R, j, 2);
-                const float4 a0 = cbs[(0 * 256 + k0) * 2], b0 = cbs[(0 * 256 + k0) * 2 + 1];
-                const float4 a1 = cbs[(1 * 256 + k1) * 2], b1 = cbs[(1 * 256 + k1) * 2 + 1];
-                const float4 a2 = cbs[(2 * 256 + k2) * 2], b2 = cbs[(2 * 256 + k2) * 2 + 1];
-                uint32_t o[4];
-                o[0] = bf16_bits(a0.x + a1.x + a2.x) | (bf16_bits(a0.y + a1.y + a2.y) << 16);
-                o[1] = bf16_bits(a0.z + a1.z + a2.z) | (bf16_bits(a0.w + a1.w + a2.w) << 16);
-                o[2] = bf16_bits(b0.x + b1.x + b2.x) | (bf16_bits(b0.y + b1.y + b2.y) << 16);
-                o[3] = bf16_bits(b0.z + b1.z + b2.z) | (bf16_bits(b0.w + b1.w + b2.w) << 16);
-                *reinterpret_cast<uint4 *>(tile + row * 128 + ((cc ^ (row & 7)) * 16)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
+    if (warp == 0) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            uint32_t st = 0, ph = 0, nacc = 0;
+            for (int it = it0; it < it1; ++it) {
+                const PfItem I = pf_item(job, Q, MT, it);
+                if (!I.valid) continue;
+                if (!mbar_wait(bar(BAR_ACC_EMPTY), (nacc & 1u) ^ 1u, abort_flag, job.status)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t idesc = idesc_bf16(128, I.npad);
+                bool ok = true;
+                for (int ks = 0; ks < KS; ++ks) {
+                    if (!mbar_wait(bar(BAR_FULL + st), ph, abort_flag, job.status)) {
+                        ok = false;
+                        break;
+                    }
+                    // the B stage was written through the generic proxy (cp.async)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t sa = sbase + OFF_ST + st * kStage;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            mma_bf16(tmem + t * 256, smem_desc(sa + t * kTileA + kk * 32),
+                                     smem_desc(sa + 2 * kTileA + kk * 32), idesc,
+                                     (ks > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(bar(BAR_EMPTY + st));
+                    if (++st == PF_NST) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar(BAR_ACC_FULL));
+                ++nacc;
             }
+            // drain: every MMA issued has completed before TMEM is released
+            mma_commit(bar(BAR_DONE));
+            int no_abort = 0;
+            mbar_wait(bar(BAR_DONE), 0, &no_abort, job.status);
         }
-        // (b) B tile: the pass's tokens (rows beyond n are zero)
-        for (int x = tid; x < it.npad * 8; x += PF_NT) {
-            const int j = x >> 3, cc = x & 7;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (j < it.n && ent[j] >= 0) {
-                const int64_t rowi = (int64_t)(ent[j] / job.x_div) * job.x_stride + ks * PF_KC + cc * 8;
+        __syncwarp();
+    } else if (warp < 4) {
+        // ================= B producers =================
+        const int lt = tid - 32;
+        const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
+        uint32_t st = 0, ph = 0;
+        for (int it = it0; it < it1 && !*abort_flag; ++it) {
+            const PfItem I = pf_item(job, Q, MT, it);
+            if (!I.valid) continue;
+            const uint8_t *src[3];
+#pragma unroll
+            for (int r = 0; r < 3; ++r) {
+                const int j = lt + kLoaders * r;
+                src[r] = nullptr;
+                if (j < I.n) {
+                    const int p = job.pairs[I.o + I.j0 + j];
+                    if (p >= 0 && p < job.n_pairs)
+                        src[r] = reinterpret_cast<const uint8_t *>(job.x) +
+                                 ((int64_t)(p / job.x_div) * job.x_stride) * esz;
+                    else
+                        set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+                }
+            }
+            bool ok = true;
+            for (int ks = 0; ks < KS; ++ks) {
+                if (!mbar_wait(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, job.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = sbase + OFF_ST + st * kStage + 2 * kTileA;
+                const uint32_t full = bar(BAR_FULL + st);
                 if (esz == 2) {
-                    v = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(job.x) +
-                                                         rowi * 2);
+#pragma unroll
+                    for (int r = 0; r < 3; ++r) {
+                        const int j = lt + kLoaders * r;
+                        if (src[r] != nullptr) {
+                            const uint8_t *s = src[r] + ks * PF_KC * 2;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                cp_async16(sb + j * 128 + ((c ^ (j & 7)) << 4), s + c * 16);
+                        }
+                    }
+                    // arrives once this thread's copies have landed
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full)
+                                 : "memory");
                 } else {
-                    const float4 *f = reinterpret_cast<const float4 *>(
-                        reinterpret_cast<const float *>(job.x) + rowi);
-                    const float4 f0 = f[0], f1 = f[1];
-                    v.x = bf16_bits(f0.x) | (bf16_bits(f0.y) << 16);
-                    v.y = bf16_bits(f0.z) | (bf16_bits(f0.w) << 16);
-                    v.z = bf16_bits(f1.x) | (bf16_bits(f1.y) << 16);
-                    v.w = bf16_bits(f1.z) | (bf16_bits(f1.w) << 16);
+                    uint8_t *bt = smem + OFF_ST + st * kStage + 2 * kTileA;
+#pragma unroll
+                    for (int r = 0; r < 3; ++r) {
+                        const int j = lt + kLoaders * r;
+                        if (src[r] != nullptr) {
+                            const float4 *s =
+                                reinterpret_cast<const float4 *>(src[r] + ks * PF_KC * 4);
+                            for (int c = 0; c < 8; ++c) {
+                                const float4 f0 = s[2 * c], f1 = s[2 * c + 1];
+                                *reinterpret_cast<uint4 *>(bt + j * 128 + ((c ^ (j & 7)) << 4)) =
+                                    make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f0.z, f0.w),
+                                               pack_bf16x2(f1.x, f1.y), pack_bf16x2(f1.z, f1.w));
+                            }
+                        }
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive(full);
+                }
+                if (++st == PF_NST) {
+                    st = 0;
+                    ph ^= 1u;
                 }
             }
-            *reinterpret_cast<uint4 *>(smem + OFF_B + j * 128 + ((cc ^ (j & 7)) * 16)) = v;
+            if (!ok) break;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        // (c) one thread issues the MMAs: 4 x K=16 per matrix
-        if (tid == 0) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp < 8) {
+        // ================= epilogue =================
+        const int ew = warp - 4;                 // TMEM lanes 32 ew .. 32 ew + 31
+        const int rit = ew * 32 + lane;          // row within the tile
+        const uint32_t tl = tmem + ((uint32_t)(ew * 32) << 16);
+        uint32_t nacc = 0;
+        for (int it = it0; it < it1; ++it) {
+            const PfItem I = pf_item(job, Q, MT, it);
+            if (!I.valid) continue;
+            if (!mbar_wait(bar(BAR_ACC_FULL), nacc & 1u, abort_flag, job.status)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            for (int m = 0; m < job.n_mat; ++m) {
+            const int R0 = I.mt * job.tile_rows;
+            for (int c0 = 0; c0 < I.n; c0 += 32) {
+                const int jl = c0 + lane;
+                const int pl = jl < I.n ? job.pairs[I.o + I.j0 + jl] : -1;
+                float a0[32], a1[32];
+                tmem_ld32(tl + c0, a0);
+                tmem_ld32(tl + 256 + c0, a1);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = smem_desc(smem_u32(smem + OFF_A + m * kTileA) + kk * 32);
-                    const uint64_t bd = smem_desc(smem_u32(smem + OFF_B) + kk * 32);
-                    mma_bf16(tmem + m * 256, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-                }
-            }
-            mma_commit(smem_u32(mbar));
-        }
-        // (d) the tiles may be overwritten once the MMAs have read them
-        if (!mbar_wait(smem_u32(mbar), (uint32_t)(ks & 1))) *flag = 1;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        __syncthreads();
-        ok = *flag == 0;
-    }
-
-    if (ok) {
-        // epilogue: lane <-> row; 32 token columns per TMEM load
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        for (int c0 = 0; c0 < it.npad; c0 += 32) {
-            float g[32], u[32];
-            tmem_ld32(tmem + lane_base + c0, g);
-            if (job.n_mat == 2) tmem_ld32(tmem + lane_base + 256 + c0, u);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int j = c0 + q;
-                if (j < it.n && ent[j] >= 0) {
-                    if (job.n_mat == 2) {
-                        const float hv = g[q] / (1.0f + expf(-g[q])) * u[q];
-                        reinterpret_cast<uint16_t *>(job.out)[(size_t)ent[j] * job.rows + R] =
-                            (uint16_t)bf16_bits(hv);
-                    } else {
-                        reinterpret_cast<float *>(job.out)[(size_t)ent[j] * job.rows + R] = g[q];
+                for (int q = 0; q < 32; ++q) {
+                    const int p = __shfl_sync(0xffffffffu, pl, q);
+                    if (c0 + q < I.n && p >= 0 && p < job.n_pairs) {
+                        if (job.mode == PF_MODE_SWIGLU) {
+                            const float g = a0[q];
+                            const float hv = g / (1.0f + expf(-g)) * a1[q];
+                            reinterpret_cast<uint16_t *>(job.out)[(size_t)p * job.rows + R0 + rit] =
+                                (uint16_t)bf16_bits(hv);
+                        } else {
+                            float *y = reinterpret_cast<float *>(job.out) + (size_t)p * job.rows + R0;
+                            y[job.row_off[0] + rit] = a0[q];
+                            y[job.row_off[1] + rit] = a1[q];
+                        }
                     }
                 }
             }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY));
+            ++nacc;
         }
-    } else if (tid == 0) {
-        set_dev_error(job.status, RVQ_DEV_ERR_TIMEOUT);
+    } else {
+        // ================= A producers (decode) =================
+        const int dt = tid - 256;
+        const int dw = dt >> 5, qw = lane >> 3, q = lane & 7;
+        const int b8 = dw * 4 + qw;              // quarter-warp 0..31
+        const int r0 = (b8 >> 1) * 8;
+        const int tile = q >> 2;
+        // quarter-warps of type 0 decode tile-0 rows r0..r0+3 and tile-1 rows
+        // r0+4..r0+7, type 1 the other halves: (row mod 8) differs per lane
+        const int rit = (b8 & 1) == 0 ? r0 + q : (tile == 0 ? r0 + 4 + q : r0 + q - 4);
+        const int sw = rit & 7;
+        const uint8_t *cbl = smem + OFF_CB + q * 16;  // this lane's bank group
+        const int RB = job.rows / 32;
+        const int G = KS / 4;                    // 32-chunk groups along K
+        int cur_e = -1;
+        uint32_t st = 0, ph = 0, ncb = 0;
+        for (int it = it0; it < it1 && !*abort_flag; ++it) {
+            const PfItem I = pf_item(job, Q, MT, it);
+            if (!I.valid) continue;
+            const uint8_t *rec = job.base + (uint64_t)I.e * job.record_bytes;
+            if (I.e != cur_e) {
+                // every A producer is done with the previous codebooks
+                if (cur_e >= 0) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_CB));
+                    if (!mbar_wait(bar(BAR_CB), ncb & 1u, abort_flag, job.status)) break;
+                    ++ncb;
+                }
+                // record fp32 [s][k/2][i][k&1] -> fp16 lines, one 16-byte group per unit
+                for (int u = dt; u < 3 * 256 * 8; u += kDecoders) {
+                    const int L = u >> 3, g = u & 7;
+                    const int s = L >> 8, k = L & 255;
+                    const float *cb = reinterpret_cast<const float *>(rec + job.cb_off[g >> 2]) +
+                                      ((s * 128 + (k >> 1)) * 8) * 2 + (k & 1);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __half2 h2 = __floats2half2_rn(cb[(2 * i) * 2], cb[(2 * i + 1) * 2]);
+                        w[i] = *reinterpret_cast<const uint32_t *>(&h2);
+                    }
+                    *reinterpret_cast<uint4 *>(smem + OFF_CB + L * kCbLine + g * 16) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_CB));
+                if (!mbar_wait(bar(BAR_CB), ncb & 1u, abort_flag, job.status)) break;
+                ++ncb;
+                cur_e = I.e;
+            }
+            const int R = I.mt * job.tile_rows + job.row_off[tile] + rit;
+            const int l = R & 31;
+            // this row's code planes of 32-chunk group g: 6 x 16 bytes (stage s, half h)
+            const uint8_t *cp = rec + job.codes_off[tile] + (size_t)(R >> 5) * kTileBytes + l * 16;
+            uint4 nxt[6];
+#pragma unroll
+            for (int v = 0; v < 6; ++v) nxt[v] = *reinterpret_cast<const uint4 *>(cp + v * 512);
+            bool ok = true;
+            for (int g = 0; g < G && ok; ++g) {
+                uint32_t U[3][8];
+#pragma unroll
+                for (int s = 0; s < 3; ++s) {
+                    U[s][0] = nxt[2 * s].x;
+                    U[s][1] = nxt[2 * s].y;
+                    U[s][2] = nxt[2 * s].z;
+                    U[s][3] = nxt[2 * s].w;
+                    U[s][4] = nxt[2 * s + 1].x;
+                    U[s][5] = nxt[2 * s + 1].y;
+                    U[s][6] = nxt[2 * s + 1].z;
+                    U[s][7] = nxt[2 * s + 1].w;
+                }
+                if (g + 1 < G) {
+                    const uint8_t *cpn = cp + (size_t)(g + 1) * RB * kTileBytes;
+#pragma unroll
+                    for (int v = 0; v < 6; ++v)
+                        nxt[v] = *reinterpret_cast<const uint4 *>(cpn + v * 512);
+                }
+#pragma unroll
+                for (int s = 0; s < 3; ++s) derotate(U[s], l);
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    if (!mbar_wait(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, job.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *A = smem + OFF_ST + st * kStage + tile * kTileA + rit * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int cg = k4 * 8 + c;
+                        const uint32_t k0 = (U[0][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
+                        const uint32_t k1 = (U[1][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
+                        const uint32_t k2 = (U[2][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(cbl + k0 * kCbLine);
+                        const uint4 w1 =
+                            *reinterpret_cast<const uint4 *>(cbl + (256 + k1) * kCbLine);
+                        const uint4 w2 =
+                            *reinterpret_cast<const uint4 *>(cbl + (512 + k2) * kCbLine);
+                        uint4 o;
+                        o.x = sum3_bf16x2(w0.x, w1.x, w2.x);
+                        o.y = sum3_bf16x2(w0.y, w1.y, w2.y);
+                        o.z = sum3_bf16x2(w0.z, w1.z, w2.z);
+                        o.w = sum3_bf16x2(w0.w, w1.w, w2.w);
+                        *reinterpret_cast<uint4 *>(A + ((c ^ sw) << 4)) = o;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_FULL + st));
+                    if (++st == PF_NST) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) break;
+        }
     }
+
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(job.n_mat == 2 ? 512 : 256));
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    }
 }
 
 }  // namespace
-
-int prefill_max_items(const PfJob &job) {
-    // sum over experts of ceil(n_e / 256) <= E + n_pairs / 256, times the M tiles
-    return (job.E + job.n_pairs / PF_NMAX + 1) * (job.rows / PF_M);
-}
 
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) {
     static int attr_done[64] = {0};
@@ -346,13 +608,16 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem));
         attr_done[dev] = 1;
     }
-    if (job.rows % PF_M || job.cols % PF_KC || job.n_mat < 1 || job.n_mat > 2) {
-        set_error("prefill: rows %d / cols %d not tileable", job.rows, job.cols);
+    if ((job.tile_rows != 128 && job.tile_rows != 256) || job.rows % job.tile_rows ||
+        job.cols % (4 * PF_KC) || job.E < 1 || job.E > kMaxE || job.min_tokens < 1 ||
+        (job.mode != PF_MODE_SWIGLU && job.mode != PF_MODE_PLAIN)) {
+        set_error("prefill: rows %d / cols %d / tile %d / E %d not supported", job.rows, job.cols,
+                  job.tile_rows, job.E);
         return RVQ_EINVAL;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)prefill_max_items(job));
-    cfg.blockDim = dim3(PF_NT);
+    cfg.gridDim = dim3((unsigned)num_sms());
+    cfg.blockDim = dim3(PF_THREADS);
     cfg.dynamicSmemBytes = kPfSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
