@@ -50,6 +50,7 @@ WORKLOADS = {
     "decode_d2048_b4": (1, 4),
     "decode_d2048_b16": (1, 16),
     "k3_prefill2048": (4, 2048),
+    "k3_prefill512_e64": (4, 512, 64),  # profiling case: ~128 tokens per expert, 1.06 GB bank
 }
 KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
            "lut_gemv_down", "combine"]

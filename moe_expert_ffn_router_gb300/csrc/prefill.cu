@@ -134,13 +134,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
                  : "memory");
 }
 
+// try_wait with a suspend hint: a waiting warp sleeps (up to 20 us) instead
+// of spinning, leaving issue slots to the decoding warps; it wakes when the
+// phase completes.
 __device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         "selp.b32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(mbar), "r"(parity)
+        : "r"(mbar), "r"(parity), "r"(20000u)
         : "memory");
     return done != 0;
 }
@@ -212,6 +215,15 @@ __device__ __forceinline__ void derotate(uint32_t (&w)[8], int l) {
     for (int i = 0; i < 8; ++i) a[i] = (wl & 4) ? b[(i + 4) & 7] : b[i];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = __funnelshift_l(a[(i + 7) & 7], a[i], bl);
+}
+
+// 128-bit shared store issued as volatile asm without a memory clobber: the
+// compiler keeps it in order with the fences and barrier arrivals (also
+// volatile asm) but may schedule the codebook loads of later chunks ahead of
+// it -- the A tiles and the codebooks never overlap.
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w));
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
@@ -557,7 +569,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                         ok = false;
                         break;
                     }
-                    uint8_t *A = smem + OFF_ST + st * kStage + tile * kTileA + rit * 128;
+                    const uint32_t A = sbase + OFF_ST + st * kStage + tile * kTileA + rit * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const int cg = k4 * 8 + c;
@@ -574,7 +586,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                         o.y = sum3_bf16x2(w0.y, w1.y, w2.y);
                         o.z = sum3_bf16x2(w0.z, w1.z, w2.z);
                         o.w = sum3_bf16x2(w0.w, w1.w, w2.w);
-                        *reinterpret_cast<uint4 *>(A + ((c ^ sw) << 4)) = o;
+                        sts128(A + ((c ^ sw) << 4), o);
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
