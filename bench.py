@@ -59,7 +59,8 @@ DOMINANT = "lut_gemv_gate_up"
 KERNELS_TC = ["router_logits", "route", "lut_experts", "prefill_gate_up", "prefill_down",
               "unused", "combine"]
 DOMINANT_TC = "prefill_gate_up"
-TC_LAUNCHES_PER_STEP = 5   # router logits, route, gate/up GEMM, down GEMM, combine
+# router logits, top-k selection, grouping, gate/up GEMM, down GEMM, combine
+TC_LAUNCHES_PER_STEP = 6
 
 
 def load_traffic(name):

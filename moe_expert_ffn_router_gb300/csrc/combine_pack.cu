@@ -56,6 +56,52 @@ __global__ void combine_kernel(const float *__restrict__ ypart, int nslot,
     *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
 }
 
+// nslot == 1 (outputs already reduced, e.g. by the tensor-core path): one
+// thread per (token, column quad) with all k slot loads in flight at once.
+__global__ void __launch_bounds__(256) combine1_kernel(const float *__restrict__ y,
+                                                       const float *__restrict__ w, int n, int k,
+                                                       int d, const void *res, int rdt,
+                                                       float *out) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int d4 = d >> 2;
+    const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
+    const int t = blockIdx.y;
+    if (c4 >= d4) return;
+    const int c = c4 * 4;
+    float4 acc;
+    if (rdt == RVQ_BF16) {
+        const uint2 r = __ldg(reinterpret_cast<const uint2 *>(
+            reinterpret_cast<const uint16_t *>(res) + (int64_t)t * d + c));
+        acc.x = __uint_as_float(r.x << 16);
+        acc.y = __uint_as_float(r.x & 0xFFFF0000u);
+        acc.z = __uint_as_float(r.y << 16);
+        acc.w = __uint_as_float(r.y & 0xFFFF0000u);
+    } else {
+        acc = __ldg(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(res) +
+                                                     (int64_t)t * d + c));
+    }
+    const float4 *yp = reinterpret_cast<const float4 *>(y + (int64_t)t * k * d) + c4;
+    for (int s0 = 0; s0 < k; s0 += 8) {
+        float4 v[8];
+        float ws[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const bool on = s0 + i < k;
+            v[i] = on ? __ldg(yp + (int64_t)(s0 + i) * d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ws[i] = on ? __ldg(w + (int64_t)t * k + s0 + i) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc.x += ws[i] * v[i].x;
+            acc.y += ws[i] * v[i].y;
+            acc.z += ws[i] * v[i].z;
+            acc.w += ws[i] * v[i].w;
+        }
+    }
+    *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
+}
+
 // One thread per 16-byte packed word.  Packed word (tile g,b; stage s; half h;
 // lane l) byte i <-> canonical code (row 32b+l, chunk 32g+((16h+i+l) mod 32), s).
 __global__ void pack_kernel(const uint8_t *__restrict__ src, int rows, int cols,
@@ -118,14 +164,20 @@ rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, 
         return RVQ_EINVAL;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((d / 4 + CB_Q - 1) / CB_Q), (unsigned)n);
-    cfg.blockDim = dim3(CB_Q, (unsigned)k);
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    cfg.stream = stream;
+    if (nslot == 1 && n > 64) {
+        cfg.gridDim = dim3((unsigned)((d / 4 + 255) / 256), (unsigned)n);
+        cfg.blockDim = dim3(256);
+        RVQ_CUDA(cudaLaunchKernelEx(&cfg, combine1_kernel, ypart, w, n, k, d, res, rdt, out));
+        return RVQ_OK;
+    }
+    cfg.gridDim = dim3((unsigned)((d / 4 + CB_Q - 1) / CB_Q), (unsigned)n);
+    cfg.blockDim = dim3(CB_Q, (unsigned)k);
     RVQ_CUDA(cudaLaunchKernelEx(&cfg, combine_kernel, ypart, nslot, w, n, k, d, res, rdt, out));
     return RVQ_OK;
 }

@@ -72,6 +72,106 @@ __global__ void __launch_bounds__(LG_NT) router_logits_kernel(
     }
 }
 
+// Prefill-sized batches: a tiled fp32 GEMM, logits[n][E] = x Wr^T.  Each
+// block computes 64 tokens x 64 experts; 256 threads hold 4 x 4 outputs each;
+// K runs in slices of 32 staged (k-major, fp32) in shared memory with the next
+// slice prefetched into registers.  Sums run in a fixed order, so the result
+// does not depend on the launch.
+constexpr int LT_T = 64, LT_E = 64, LT_K = 32, LT_PAD = 4;
+
+__global__ void __launch_bounds__(256) router_logits_tiled_kernel(
+    const float *__restrict__ wr, const float *__restrict__ bias, const void *__restrict__ x,
+    int xdt, int n, int E, int d, float *__restrict__ logits) {
+    __shared__ __align__(16) float xs[LT_K][LT_T + LT_PAD];
+    __shared__ __align__(16) float ws[LT_K][LT_E + LT_PAD];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int e0 = blockIdx.x * LT_E, t0 = blockIdx.y * LT_T;
+    // loader: row = tid / 4 (token or expert), 8 consecutive k at (tid % 4) * 8
+    const int lr = tid >> 2, lk = (tid & 3) * 8;
+    const bool xin = t0 + lr < n, win = e0 + lr < E;
+    const int64_t xrow = (int64_t)(t0 + lr) * d, wrow = (int64_t)(e0 + lr) * d;
+    float xv[8], wv[8];
+    auto load = [&](int k0) {
+        if (xin) {
+            if (xdt == RVQ_BF16) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4 *>(
+                    reinterpret_cast<const uint16_t *>(x) + xrow + k0 + lk));
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xv[2 * i] = __uint_as_float(w[i] << 16);
+                    xv[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+            } else {
+                const float4 *p = reinterpret_cast<const float4 *>(
+                    reinterpret_cast<const float *>(x) + xrow + k0 + lk);
+                const float4 a = __ldg(p), b = __ldg(p + 1);
+                xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+                xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xv[i] = 0.f;
+        }
+        if (win) {
+            const float4 *p = reinterpret_cast<const float4 *>(wr + wrow + k0 + lk);
+            const float4 a = __ldg(p), b = __ldg(p + 1);
+            wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+            wv[4] = b.x; wv[5] = b.y; wv[6] = b.z; wv[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) wv[i] = 0.f;
+        }
+    };
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    load(0);
+    for (int k0 = 0; k0 < d; k0 += LT_K) {
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            xs[lk + i][lr] = xv[i];
+            ws[lk + i][lr] = wv[i];
+        }
+        __syncthreads();
+        if (k0 + LT_K < d) load(k0 + LT_K);
+        // two-level sums (a slice of 32 products, then across slices) keep the
+        // rounding error of the 7168-term dot products near the tree-sum level
+        float part[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < LT_K; ++kk) {
+            const float4 a = *reinterpret_cast<const float4 *>(&xs[kk][ty * 4]);
+            const float4 b = *reinterpret_cast<const float4 *>(&ws[kk][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] += part[i][j];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= n) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx * 4 + j;
+            if (e < E) logits[(int64_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+        }
+    }
+}
+
 // ------------------------------------------------------------------- route
 constexpr size_t RT_SMEM_MAX = 200 * 1024;
 constexpr int RT_KEEP = 4;  // tokens per warp whose selection stays in registers
@@ -85,12 +185,88 @@ __device__ __forceinline__ float key_float(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// One block.  Phase 1: one warp per token selects the k largest keys with
-// warp-wide max/min reductions (one redux.sync each per pick) and writes the
-// renormalised softmax weights.  Phase 2: per-expert token bitmaps give
+// One warp selects the k largest keys of one token's logits with warp-wide
+// max/min reductions (one redux.sync each per pick); lane s < k returns the
+// s-th pick and its renormalised softmax weight.
+__device__ __forceinline__ void warp_topk(const float *__restrict__ row, int E, int k, int lane,
+                                          uint32_t *status, int &my_idx, float &my_w) {
+    const int EP = (E + 31) >> 5;  // <= 8
+    uint32_t key[8];
+    bool bad = false;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int e = lane + 32 * q;
+        if (q < EP && e < E) {
+            const float v = row[e];
+            bad |= !isfinite(v);
+            key[q] = float_key(v);
+        } else {
+            key[q] = 0u;  // below every real key
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_dev_error(status, RVQ_DEV_ERR_NONFINITE);
+    // lane-local best (ties: lower q = lower expert index)
+    uint32_t taken = 0u, lk = 0u;
+    int lq = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (key[q] > lk) { lk = key[q]; lq = q; }
+    uint32_t kmax0 = 0u, my_key = 0u;
+    my_idx = 0;
+    for (int s = 0; s < k; ++s) {
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, lk);
+        const uint32_t cand = (lk == kmax) ? (uint32_t)(lane + 32 * lq) : 0xffffffffu;
+        uint32_t emin = __reduce_min_sync(0xffffffffu, cand);
+        if (emin >= (uint32_t)E) emin = 0;  // only with invalid inputs
+        if (s == 0) kmax0 = kmax;
+        if (lane == s) {
+            my_idx = (int)emin;
+            my_key = kmax;
+        }
+        if ((int)(emin & 31) == lane) {
+            taken |= 1u << (emin >> 5);
+            lk = 0u;
+            lq = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (!((taken >> q) & 1u) && key[q] > lk) { lk = key[q]; lq = q; }
+        }
+    }
+    // w = exp(l - l_max) / sum over the selection (l_max = first pick)
+    const float lmax = key_float(kmax0);
+    const float ex = (lane < k) ? expf(key_float(my_key) - lmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    sum = __shfl_sync(0xffffffffu, sum, 0);  // one denominator for every slot
+    my_w = ex / sum;
+}
+
+// Selection only, one warp per token over the whole grid (prefill batches);
+// the grouping follows in route_kernel<NT, false>.
+__global__ void __launch_bounds__(256) route_select_kernel(const float *__restrict__ logits, int n,
+                                                           int E, int k, int32_t *__restrict__ idx,
+                                                           float *__restrict__ wout,
+                                                           uint32_t *status) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= n) return;
+    int my_idx;
+    float my_w;
+    warp_topk(logits + (int64_t)t * E, E, k, lane, status, my_idx, my_w);
+    if (lane < k) {
+        idx[(int64_t)t * k + lane] = my_idx;
+        wout[(int64_t)t * k + lane] = my_w;
+    }
+}
+
+// One block.  Phase 1: one warp per token selects its k experts (SELECT), or
+// the selection is read back from idx.  Phase 2: per-expert token bitmaps give
 // counts and running ranks; phase 3 scatters each (token, slot) to
 // offsets[e] + rank, i.e. pairs sorted by (expert, token).
-template <int NT>
+template <int NT, bool SELECT>
 __global__ void __launch_bounds__(NT, 1) route_kernel(const float *__restrict__ logits, int n,
                                                       int E, int k, int32_t *idx,
                                                       float *__restrict__ wout,
@@ -110,68 +286,30 @@ __global__ void __launch_bounds__(NT, 1) route_kernel(const float *__restrict__ 
     for (int i = threadIdx.x; i < E * W; i += NT) mask[i] = 0u;
     __syncthreads();
 
-    const int EP = (E + 31) >> 5;  // <= 8
     int keep[RT_KEEP];
 #pragma unroll
     for (int r = 0; r < RT_KEEP; ++r) keep[r] = 0;
     int r = 0;
-    for (int t = warp; t < n; t += NWARP, ++r) {
-        uint32_t key[8];
-        bool bad = false;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int e = lane + 32 * q;
-            if (q < EP && e < E) {
-                const float v = logits[(int64_t)t * E + e];
-                bad |= !isfinite(v);
-                key[q] = float_key(v);
-            } else {
-                key[q] = 0u;  // below every real key
+    if (SELECT) {
+        for (int t = warp; t < n; t += NWARP, ++r) {
+            int my_idx;
+            float my_w;
+            warp_topk(logits + (int64_t)t * E, E, k, lane, status, my_idx, my_w);
+            if (lane < k) {
+                idx[(int64_t)t * k + lane] = my_idx;
+                wout[(int64_t)t * k + lane] = my_w;
+                atomicOr(&mask[(size_t)my_idx * W + (t >> 5)], 1u << (t & 31));
             }
+#pragma unroll
+            for (int q = 0; q < RT_KEEP; ++q)
+                if (q == r) keep[q] = my_idx;
         }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) set_dev_error(status, RVQ_DEV_ERR_NONFINITE);
-        // lane-local best (ties: lower q = lower expert index)
-        uint32_t taken = 0u, lk = 0u;
-        int lq = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (key[q] > lk) { lk = key[q]; lq = q; }
-        uint32_t kmax0 = 0u, my_key = 0u;
-        int my_idx = 0;
-        for (int s = 0; s < k; ++s) {
-            const uint32_t kmax = __reduce_max_sync(0xffffffffu, lk);
-            const uint32_t cand = (lk == kmax) ? (uint32_t)(lane + 32 * lq) : 0xffffffffu;
-            uint32_t emin = __reduce_min_sync(0xffffffffu, cand);
-            if (emin >= (uint32_t)E) emin = 0;  // only with invalid inputs
-            if (s == 0) kmax0 = kmax;
-            if (lane == s) {
-                my_idx = (int)emin;
-                my_key = kmax;
-            }
-            if ((int)(emin & 31) == lane) {
-                taken |= 1u << (emin >> 5);
-                lk = 0u;
-                lq = 0;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (!((taken >> q) & 1u) && key[q] > lk) { lk = key[q]; lq = q; }
-            }
+    } else {
+        for (int i = threadIdx.x; i < n * k; i += NT) {
+            const int t = i / k;
+            const int e = idx[i];
+            atomicOr(&mask[(size_t)e * W + (t >> 5)], 1u << (t & 31));
         }
-        // w = exp(l - l_max) / sum over the selection (l_max = first pick)
-        const float lmax = key_float(kmax0);
-        const float ex = (lane < k) ? expf(key_float(my_key) - lmax) : 0.f;
-        float sum = ex;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        sum = __shfl_sync(0xffffffffu, sum, 0);  // one denominator for every slot
-        if (lane < k) {
-            idx[(int64_t)t * k + lane] = my_idx;
-            wout[(int64_t)t * k + lane] = ex / sum;
-            atomicOr(&mask[(size_t)my_idx * W + (t >> 5)], 1u << (t & 31));
-        }
-#pragma unroll
-        for (int q = 0; q < RT_KEEP; ++q)
-            if (q == r) keep[q] = my_idx;
     }
     __syncthreads();
 
@@ -220,7 +358,7 @@ __global__ void __launch_bounds__(NT, 1) route_kernel(const float *__restrict__ 
     for (int t = warp; t < n; t += NWARP, ++r) {
         if (lane < k) {
             int e = 0;
-            if (r < RT_KEEP) {
+            if (SELECT && r < RT_KEEP) {
 #pragma unroll
                 for (int q = 0; q < RT_KEEP; ++q)
                     if (q == r) e = keep[q];
@@ -254,6 +392,9 @@ rvq_status launch_router_logits(const float *wr, const float *bias, const void *
                                 int E, int d, float *logits, cudaStream_t stream) {
     if (n == 1) {
         router_logits_kernel<1><<<dim3(E, 1), LG_NT, 0, stream>>>(wr, bias, x, xdt, n, E, d, logits);
+    } else if (n > 64 && d % LT_K == 0) {
+        router_logits_tiled_kernel<<<dim3((E + LT_E - 1) / LT_E, (n + LT_T - 1) / LT_T), 256, 0,
+                                     stream>>>(wr, bias, x, xdt, n, E, d, logits);
     } else {
         router_logits_kernel<8><<<dim3(E, (n + 7) / 8), LG_NT, 0, stream>>>(wr, bias, x, xdt, n, E, d,
                                                                             logits);
@@ -262,7 +403,7 @@ rvq_status launch_router_logits(const float *wr, const float *bias, const void *
     return RVQ_OK;
 }
 
-template <int NT>
+template <int NT, bool SELECT>
 rvq_status launch_route_nt(const float *logits, int n, int E, int k, int32_t *idx, float *w,
                            int32_t *offsets, int32_t *pairs, uint32_t *status,
                            cudaStream_t stream, bool pdl) {
@@ -270,7 +411,8 @@ rvq_status launch_route_nt(const float *logits, int n, int E, int k, int32_t *id
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {
-        RVQ_CUDA(cudaFuncSetAttribute(route_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        RVQ_CUDA(cudaFuncSetAttribute(route_kernel<NT, SELECT>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)RT_SMEM_MAX));
         attr_done[dev] = 1;
     }
@@ -284,8 +426,8 @@ rvq_status launch_route_nt(const float *logits, int n, int E, int k, int32_t *id
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    RVQ_CUDA(cudaLaunchKernelEx(&cfg, route_kernel<NT>, logits, n, E, k, idx, w, offsets, pairs,
-                                status));
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, route_kernel<NT, SELECT>, logits, n, E, k, idx, w, offsets,
+                                pairs, status));
     return RVQ_OK;
 }
 
@@ -293,8 +435,21 @@ rvq_status launch_route(const float *logits, int n, int E, int k, int32_t *idx, 
                         int32_t *offsets, int32_t *pairs, uint32_t *status, cudaStream_t stream,
                         bool pdl) {
     if (n <= 64)
-        return launch_route_nt<256>(logits, n, E, k, idx, w, offsets, pairs, status, stream, pdl);
-    return launch_route_nt<1024>(logits, n, E, k, idx, w, offsets, pairs, status, stream, pdl);
+        return launch_route_nt<256, true>(logits, n, E, k, idx, w, offsets, pairs, status, stream,
+                                          pdl);
+    // larger batches: the selection spreads over the grid, the grouping stays in one block
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((n + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, route_select_kernel, logits, n, E, k, idx, w, status));
+    return launch_route_nt<1024, false>(logits, n, E, k, idx, w, offsets, pairs, status, stream,
+                                        pdl);
 }
 
 }  // namespace rvq

@@ -131,3 +131,52 @@ def test_prefill_chunk_full_size_zipf():
         assert_rms_close(y[p], ref, TC_TOL, f"pair {p} (expert {e}, group {counts[e]})")
     assert np.isfinite(y).all()
     sl.forget()
+
+
+def test_layer_forward_with_dispatch_d2048():
+    """Whole layer through moe_layer_forward_ex for 100 tokens (tiled router
+    logits, grid-wide selection, tensor-core experts, all-slot combine):
+    routing bit-exact given the GPU's logits, sampled outputs within 2e-2."""
+    sl, L, _ = layer(1)
+    n = 100
+    bits = sl.tokens_bf16(n)
+    x = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    b = L.forward(x, tc_min_tokens=1)
+    torch.cuda.synchronize()
+    assert L.status(n) == (0, 0)
+    x64 = bf16_bits_to_f64(bits)
+    s = sl.shape
+    logits = b["logits"].cpu().numpy()
+    assert_rms_close(logits, oracle.router_logits(sl.wr, x64), 1e-5, "logits")
+    idx, w = b["idx"].cpu().numpy(), b["w"].cpu().numpy()
+    ridx, rw, _ = oracle.route(logits, s.k)
+    assert np.array_equal(idx, ridx)
+    np.testing.assert_allclose(w, rw, rtol=2e-6, atol=1e-9)
+    roff, rpairs = oracle.group(ridx, L.E)
+    assert np.array_equal(b["offsets"].cpu().numpy(), roff)
+    assert np.array_equal(b["pairs"].cpu().numpy(), rpairs)
+    out = b["out"].cpu().numpy()
+    for t in (0, 37, n - 1):
+        r = oracle.moe_layer(sl.expert, sl.wr, x64[t:t + 1], s.k, s.d, s.f,
+                             route_logits=logits[t:t + 1])
+        assert_rms_close(out[t] - x64[t], r["out"][0] - x64[t], TC_TOL, f"token {t} out - x")
+
+
+def test_combine_reduced_outputs_many_tokens():
+    """moe_combine with one slot partial per pair and > 64 tokens (the
+    all-slots-in-flight kernel), bf16 and fp32 residuals."""
+    rng = np.random.default_rng(11)
+    n, k, d = 100, 16, 1024
+    y = rng.normal(size=(n * k, d)).astype(np.float32)
+    w = rng.random(size=(n, k)).astype(np.float32)
+    res = rng.normal(size=(n, d)).astype(np.float32)
+    res_bits = synth.f32_to_bf16(res)
+    cases = [(torch.from_numpy(res).to(DEV), res.astype(np.float64)),
+             (torch.from_numpy(res_bits.view(np.int16)).to(DEV).view(torch.bfloat16),
+              bf16_bits_to_f64(res_bits))]
+    for r, r64 in cases:
+        ref = oracle.combine(y.reshape(n, k, d), w, r64)
+        out = torch.empty((n, d), dtype=torch.float32, device=DEV)
+        rvq.moe_combine(torch.from_numpy(y).to(DEV), torch.from_numpy(w).to(DEV), n, k, d, r, out)
+        torch.cuda.synchronize()
+        assert_rms_close(out.cpu().numpy(), ref, 1e-5, "combine")

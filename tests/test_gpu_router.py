@@ -56,6 +56,7 @@ def test_route_ties_and_degenerate():
     lg[6] = np.float32(1e30)
     check_route(lg, k)
     check_route(lg[:, :64], 1)                                         # k = 1 (argmax)
+    check_route(np.tile(lg, (3, 1)), k)                    # > 64 tokens: grid-wide selection
 
 
 def test_route_skewed_prefill_counts():
@@ -73,9 +74,14 @@ def test_route_flags_non_finite():
     assert bits & rvq.DEV_ERR_NONFINITE and rc != 0
     assert ((idx >= 0) & (idx < 64)).all()          # outputs stay in range
     assert off[-1] == 4 * 8
+    big = rng.normal(size=(100, 64)).astype(np.float32)
+    big[77, 3] = np.inf
+    idx, w, off, pairs, rc, bits = run_route(big, 8)
+    assert bits & rvq.DEV_ERR_NONFINITE and rc != 0
+    assert ((idx >= 0) & (idx < 64)).all() and off[-1] == 100 * 8
 
 
-@pytest.mark.parametrize("config,n", [(1, 1), (1, 16), (2, 1), (2, 64)])
+@pytest.mark.parametrize("config,n", [(1, 1), (1, 16), (2, 1), (2, 64), (1, 65), (2, 300)])
 def test_router_logits_match_oracle(config, n):
     s = W.WORKLOADS[config].shape
     lseed = W.layer_seed(config)
@@ -86,6 +92,25 @@ def test_router_logits_match_oracle(config, n):
     rvq.moe_router_logits(torch.from_numpy(wr).to(DEV), None, x, n, s.E, s.d, out)
     ref = oracle.router_logits(wr, synth.bf16_to_f32(bits).astype(np.float64))
     assert_rms_close(out.cpu().numpy(), ref, 1e-5, "logits")
+
+
+def test_router_logits_prefill_chunk():
+    """2048 tokens with the Zipf router bias (the tiled path), bf16 and fp32 x."""
+    wl = W.WORKLOADS[4]
+    s = wl.shape
+    lseed = W.layer_seed(4)
+    wr = W.router_weight(lseed, s.E, s.d)
+    bias = W.zipf_bias(lseed, s.E, wl.zipf_beta)
+    n = 2048
+    bits = W.tokens_bf16(lseed, n, s.d)
+    x64 = synth.bf16_to_f32(bits).astype(np.float64)
+    ref = oracle.router_logits(wr, x64, bias)
+    for x in (torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16),
+              torch.from_numpy(x64.astype(np.float32)).to(DEV)):
+        out = torch.empty((n, s.E), dtype=torch.float32, device=DEV)
+        rvq.moe_router_logits(torch.from_numpy(wr).to(DEV), torch.from_numpy(bias).to(DEV), x, n,
+                              s.E, s.d, out)
+        assert_rms_close(out.cpu().numpy(), ref, 1e-5, "prefill logits")
 
 
 def test_router_bias():
