@@ -470,6 +470,19 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     dn.pairs = pairs_dev;
     dn.desc = (ItemDesc *)(ws + P.off_desc_d);
     gu.tc_min_tokens = dn.tc_min_tokens = tc_min_tokens;
+    if (P.C_gu == 1 && P.C_d == 1 && n <= 8) {
+        // decode batches: build/stream overlapped units; the pair plan reuses
+        // the gate/up descriptor space (>= n_pairs x 16 bytes)
+        int4 *pd = (int4 *)(ws + P.off_desc_gu);
+        RVQ_TRY(launch_lut_plan_pairs(gu, pd, st, pdl));
+        RVQ_TRY(mark(0));
+        RVQ_TRY(launch_lut_gemv_il(gu, pd, st, pdl));
+        RVQ_TRY(mark(1));
+        RVQ_TRY(launch_swiglu_reduce(gpart, upart, np, P.nslot_gu, bank->f, h, st, pdl));
+        RVQ_TRY(mark(2));
+        RVQ_TRY(launch_lut_gemv_il(dn, pd, st, pdl));
+        return mark(3);
+    }
     RVQ_TRY(launch_lut_plan(gu, &dn, st, pdl));
     RVQ_TRY(mark(0));
     RVQ_TRY(launch_lut_gemv(gu, st, pdl));

@@ -134,6 +134,10 @@ struct LutJob {
 __host__ __device__ inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
 
 rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl);
+// One token per unit, table build interleaved with streaming (C == 1 layout:
+// one partial slot per chunk group).  pd: per sorted pair {expert | -1, entry}.
+rvq_status launch_lut_plan_pairs(const LutJob &job, int4 *pd, cudaStream_t stream, bool pdl);
+rvq_status launch_lut_gemv_il(const LutJob &job, const int4 *pd, cudaStream_t stream, bool pdl);
 // Descriptors for one or two LUT-GEMV jobs sharing the same grouping.
 rvq_status launch_lut_plan(const LutJob &ja, const LutJob *jb, cudaStream_t stream, bool pdl);
 rvq_status launch_lut_build(const float *cb, const void *x, int xdt, int n, int cols,

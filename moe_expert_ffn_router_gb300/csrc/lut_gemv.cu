@@ -36,6 +36,8 @@
 //    next kernel (SwiGLU for gate/up, the combine for down).
 #include "internal.cuh"
 
+#include <type_traits>
+
 namespace rvq {
 namespace {
 
@@ -288,6 +290,38 @@ __device__ __forceinline__ uint64_t tile_lookups(const uint4 (&c)[6], const uint
                 }
             }
     return acc;
+}
+
+// One-token lookups of one tile with more independent work in flight: the 16
+// lookups of a 16-byte code plane are issued before any is added, and four
+// accumulators split the add chain (for warps that cannot rely on other
+// warps to hide the shared-memory latency).
+__device__ __forceinline__ float tile_lookups1_ilp(const uint4 (&c)[6], const uint32_t (&aux2)[16],
+                                                   const uint8_t *lut) {
+    uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int s = 0; s < 3; ++s)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t w = word_of(c[s * 2 + h], q);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int t = h * 16 + q * 4 + b;
+                    const uint32_t idx = prmt(w, aux2[t >> 1], 0x7600u | (b << 4) | (4 + (t & 1)));
+                    v[q * 4 + b] = *reinterpret_cast<const float *>(lut + s * kLutStageBytes + idx);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[q] = fadd2(acc[q], pk2(v[q * 4], v[q * 4 + 1]));
+                acc[q] = fadd2(acc[q], pk2(v[q * 4 + 2], v[q * 4 + 3]));
+            }
+        }
+    const float2 a0 = upk2(fadd2(acc[0], acc[1])), a1 = upk2(fadd2(acc[2], acc[3]));
+    return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
 // ------------------------------------------------------------ persistent GEMV
@@ -543,6 +577,386 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_kernel(const LutJob job) {
     cp_async_wait_all();
 }
 
+// ------------------------------------------- interleaved build-and-stream GEMV
+// For one token per expert (decode) the table build of the next unit is
+// interleaved with the streaming of the current one inside each block: the
+// shared table holds two halves (column block h of the one-token layout
+// T[s][k][h][c], the type-1 layout), every warp streams code tiles against
+// the current half and, after its last tile of a phase, builds its share of
+// the next table into the other half.  A block barrier per table swaps them.
+// A unit is (matrix, token-expert pair, 32-chunk group, 512-row slice): one
+// 32-row tile per warp.  A table serves all units of one (matrix, pair,
+// group) in the block's contiguous unit range.  The next table's inputs (its
+// 256 input values and, when the expert or matrix changes, its codebook) are
+// fetched by one bulk copy onto an mbarrier while the warps stream.
+constexpr int IL_ROWS = 512;                   // rows per unit = 16 warps x 32
+constexpr int IL_XS = 32 * 8 * 4;              // one table's inputs, fp32 or bf16
+constexpr int kIlSmemBytes = kLutBytes + kCbBytes + IL_XS + 64;
+constexpr unsigned long long kIlWaitNs = 1000000000ull;  // bounded waits: 1 s
+
+__device__ __forceinline__ unsigned long long il_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Per sorted pair position p: {expert or -1 (skip), entry, 0, 0}.
+__global__ void __launch_bounds__(256) plan_pairs_kernel(const LutJob job, int4 *pd) {
+    __shared__ int32_t soff[257];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int E = job.E;
+    for (int x = threadIdx.x; x <= E; x += blockDim.x) soff[x] = job.offsets[x];
+    __syncthreads();
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= job.n_pairs) return;
+    int4 d = make_int4(-1, 0, 0, 0);
+    if (soff[0] != 0 || soff[E] != job.n_pairs) {
+        set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+        pd[p] = d;
+        return;
+    }
+    int lo = 0, hi = E;  // largest e with offsets[e] <= p
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (soff[mid] <= p) lo = mid; else hi = mid;
+    }
+    const int e = lo, ne = soff[e + 1] - soff[e];
+    const int entry = job.pairs[p];
+    if (!(soff[e] <= p && p < soff[e + 1]) || entry < 0 || entry >= job.n_pairs) {
+        set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+    } else if (job.tc_min_tokens > 0 && ne >= job.tc_min_tokens) {
+        // the tensor-core path takes this expert
+    } else {
+        const rvq_expert_header *h =
+            reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)e * job.record_bytes);
+        if (job.check_header &&
+            (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
+             h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes))
+            set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
+        else
+            d = make_int4(e, entry, 0, 0);
+    }
+    pd[p] = d;
+}
+
+__device__ __forceinline__ bool il_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.b32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded phase wait; false after the limit (the thread then records the
+// timeout).
+__device__ __forceinline__ bool il_wait(uint32_t bar, uint32_t parity, uint32_t *status) {
+    if (il_try(bar, parity)) return true;
+    const unsigned long long t0 = il_now();
+    for (;;) {
+        if (il_try(bar, parity)) return true;
+        if (il_now() - t0 > kIlWaitNs) {
+            set_dev_error(status, RVQ_DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// One table: (matrix, pair position, chunk group), first row slice and the
+// number of consecutive row-slice units of the block's range it serves.
+struct IlTab {
+    int m, p, g, r0, nr;
+    int2 d;  // {expert, entry}
+};
+
+// Walk over the block's unit range [w, w1): units (m, p, g, r) in that order
+// with S row slices; positions whose pair descriptor says skip are passed
+// over whole.  Fills the next table and advances past it.
+struct IlWalk {
+    int w, m, p, g, r;
+    int pc;   // pair position whose descriptor is cached in dc
+    int2 dc;
+};
+__device__ __forceinline__ IlWalk il_start(const LutJob &job, int S, int w) {
+    const int per_m = job.n_pairs * job.G * S, gs = job.G * S;
+    IlWalk k;
+    k.w = w;
+    k.pc = -1;
+    k.dc = make_int2(-1, 0);
+    k.m = w / per_m;
+    int rem = w - k.m * per_m;
+    k.p = rem / gs;
+    rem -= k.p * gs;
+    k.g = rem / S;
+    k.r = rem - k.g * S;
+    return k;
+}
+__device__ __forceinline__ bool il_next(const LutJob &job, int S, int w1, const int4 *pd,
+                                        IlWalk &k, IlTab &t) {
+    for (;;) {
+        if (k.w >= w1) return false;
+        if (k.p != k.pc) {
+            const int4 v = __ldg(pd + k.p);
+            k.dc = make_int2(v.x, v.y);
+            k.pc = k.p;
+        }
+        const int2 d = k.dc;
+        if (d.x >= 0) {
+            t.m = k.m;
+            t.p = k.p;
+            t.g = k.g;
+            t.r0 = k.r;
+            t.nr = min(S - k.r, w1 - k.w);
+            t.d = d;
+            k.w += t.nr;
+            k.r = 0;
+            if (++k.g == job.G) {
+                k.g = 0;
+                if (++k.p == job.n_pairs) {
+                    k.p = 0;
+                    ++k.m;
+                }
+            }
+            return true;
+        }
+        k.w += (job.G - k.g) * S - k.r;  // rest of this pair position
+        k.g = 0;
+        k.r = 0;
+        if (++k.p == job.n_pairs) {
+            k.p = 0;
+            ++k.m;
+        }
+    }
+}
+
+// This warp's share of one table (16 warps x 6 iterations of four entry
+// pairs).  Quarter q of the warp takes entry pair 4 it + q (a 64-byte
+// codeword pair, broadcast to its 8 lanes); lane r of the quarter computes
+// columns r, r + 8, r + 16, r + 24 for both entries.  Stores rotate the
+// column order by the quarter, so every 4-byte store instruction writes 32
+// distinct banks.
+__device__ __forceinline__ void il_build(uint8_t *lut, int h, const uint8_t *cb_s,
+                                         const uint8_t *xs_s, int xdt, int warp, int lane) {
+    const int q = lane >> 3, r = lane & 7;
+    float x[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int c = r + 8 * j;
+        if (xdt == RVQ_BF16) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(xs_s + c * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[j][2 * i] = __uint_as_float(w[i] << 16);
+                x[j][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+            const float4 a = *reinterpret_cast<const float4 *>(xs_s + c * 32);
+            const float4 b = *reinterpret_cast<const float4 *>(xs_s + c * 32 + 16);
+            x[j][0] = a.x; x[j][1] = a.y; x[j][2] = a.z; x[j][3] = a.w;
+            x[j][4] = b.x; x[j][5] = b.y; x[j][6] = b.z; x[j][7] = b.w;
+        }
+    }
+    const float4 *cb4 = reinterpret_cast<const float4 *>(cb_s);
+#pragma unroll 1
+    for (int it = warp; it < 96; it += NW) {
+        const int kp = 4 * it + q;  // entry pair over the three stages
+        const int s = kp >> 7, k = (kp & 127) * 2;
+        // pair layout: (C_k[i], C_k+1[i]) for i = 0..7
+        const float4 c0 = cb4[kp * 4 + 0], c1 = cb4[kp * 4 + 1];
+        const float4 c2 = cb4[kp * 4 + 2], c3 = cb4[kp * 4 + 3];
+        const float ca[8] = {c0.x, c0.z, c1.x, c1.z, c2.x, c2.z, c3.x, c3.z};
+        const float cbv[8] = {c0.y, c0.w, c1.y, c1.w, c2.y, c2.w, c3.y, c3.w};
+        float ta[4], tb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            ta[j] = 0.f;
+            tb[j] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ta[j] = fmaf(x[j][i], ca[i], ta[j]);
+                tb[j] = fmaf(x[j][i], cbv[i], tb[j]);
+            }
+        }
+        uint8_t *row0 = lut + s * kLutStageBytes + k * 256 + h * 128;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = (jj + q) & 3;
+            float va = ta[0], vb = tb[0];
+#pragma unroll
+            for (int z = 1; z < 4; ++z)
+                if (j == z) {
+                    va = ta[z];
+                    vb = tb[z];
+                }
+            const int c = r + 8 * j;
+            *reinterpret_cast<float *>(row0 + c * 4) = va;
+            *reinterpret_cast<float *>(row0 + 256 + c * 4) = vb;
+        }
+    }
+}
+
+// One thread fetches a table's inputs onto the mbarrier: the pair's 256
+// input values of chunk group g and, unless `same_cb`, the codebook.
+__device__ __forceinline__ void il_fetch(const LutJob &job, const IlTab &t, bool same_cb,
+                                         uint8_t *cb_s, uint8_t *xs_s, uint32_t bar) {
+    const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
+    const uint32_t xbytes = 256u * esz;
+    const uint32_t bytes = xbytes + (same_cb ? 0u : (uint32_t)kCbBytes);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+    const uint8_t *xsrc = reinterpret_cast<const uint8_t *>(job.x) +
+                          ((int64_t)(t.d.y / job.x_div) * job.x_stride + (int64_t)t.g * 256) * esz;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            (uint32_t)__cvta_generic_to_shared(xs_s)),
+        "l"(xsrc), "r"(xbytes), "r"(bar)
+        : "memory");
+    if (!same_cb) {
+        const uint8_t *cb = job.base + (uint64_t)t.d.x * job.record_bytes + job.cb_off[t.m];
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                (uint32_t)__cvta_generic_to_shared(cb_s)),
+            "l"(cb), "r"((uint32_t)kCbBytes), "r"(bar)
+            : "memory");
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, const int4 *pd) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *lut = smem;
+    uint8_t *cb_s = smem + kLutBytes;
+    uint8_t *xs_s = cb_s + kCbBytes;
+    const uint32_t inbar = (uint32_t)__cvta_generic_to_shared(xs_s + IL_XS);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int S = job.rows / IL_ROWS;
+    const int U = job.n_mat * job.n_pairs * job.G * S;
+    const int w0 = (int)((int64_t)blockIdx.x * U / gridDim.x);
+    const int w1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
+    const int RB = job.rows / 32;
+    const int nslot = job.G;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(inbar));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    // table walk (identical in every thread) and this warp's tile walk
+    IlWalk tw = il_start(job, S, w0), gw = tw;
+    IlTab cur, nxt, gt;
+    bool has_cur = il_next(job, S, w1, pd, tw, cur);
+    bool has_nxt = has_cur && il_next(job, S, w1, pd, tw, nxt);
+    int gi = 0, gn = 0;  // tile walk: index within table gt, its unit count
+    auto gen = [&](const uint8_t *&tile, float *&out) -> bool {
+        if (gi == gn) {
+            if (!il_next(job, S, w1, pd, gw, gt)) return false;
+            gi = 0;
+            gn = gt.nr;
+        }
+        const int rb = (gt.r0 + gi) * (IL_ROWS / 32) + warp;
+        ++gi;
+        const uint8_t *rec = job.base + (uint64_t)gt.d.x * job.record_bytes;
+        tile = rec + job.codes_off[gt.m] + ((size_t)gt.g * RB + rb) * kTileBytes + lane * 16;
+        out = job.part[gt.m] + ((size_t)gt.d.y * nslot + gt.g) * job.rows + rb * 32 + lane;
+        return true;
+    };
+    uint4 buf[2][6];
+    float *outp[2] = {nullptr, nullptr};
+    bool have[2] = {false, false};
+#pragma unroll
+    for (int dd = 0; dd < 2; ++dd) {
+        const uint8_t *t;
+        if (gen(t, outp[dd])) {
+            load_tile(buf[dd], t);
+            have[dd] = true;
+        }
+    }
+
+    uint32_t inph = 0;  // phase of the input barrier
+    bool alive = true;  // false after a timed-out wait: no more reads, barriers still met
+    int cb_m = -1, cb_e = -1;
+    if (has_cur) {
+        // the first table: fetched and built by all warps before streaming
+        if (threadIdx.x == 0) {
+            il_fetch(job, cur, false, cb_s, xs_s, inbar);
+            const uint8_t *t0 = job.base + (uint64_t)cur.d.x * job.record_bytes +
+                                job.codes_off[cur.m] +
+                                ((size_t)cur.g * RB + cur.r0 * (IL_ROWS / 32)) * kTileBytes;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(t0),
+                         "r"((uint32_t)(cur.nr * (IL_ROWS / 32) * kTileBytes))
+                         : "memory");
+        }
+        cb_m = cur.m;
+        cb_e = cur.d.x;
+        alive = il_wait(inbar, inph, job.status);
+        ++inph;
+        if (alive) il_build(lut, 0, cb_s, xs_s, job.x_dtype, warp, lane);
+    }
+    __syncthreads();
+
+    uint32_t aux2[16];
+    int sp = 0;  // ring slot holding this warp's next tile
+    for (int b = 0; has_cur; ++b) {
+        const int h = b & 1;
+        if (has_nxt && threadIdx.x == 0) {
+            const bool same = nxt.m == cb_m && nxt.d.x == cb_e;
+            il_fetch(job, nxt, same, cb_s, xs_s, inbar);
+            // the next table's code tiles (its units are adjacent row slices,
+            // one contiguous range) into L2 while this table streams
+            const uint8_t *t0 = job.base + (uint64_t)nxt.d.x * job.record_bytes +
+                                job.codes_off[nxt.m] +
+                                ((size_t)nxt.g * RB + nxt.r0 * (IL_ROWS / 32)) * kTileBytes;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(t0),
+                         "r"((uint32_t)(nxt.nr * (IL_ROWS / 32) * kTileBytes))
+                         : "memory");
+        }
+        if (has_nxt) {
+            cb_m = nxt.m;
+            cb_e = nxt.d.x;
+        }
+#pragma unroll
+        for (int p2 = 0; p2 < 16; ++p2) {
+            const uint32_t c0 = (((lane + 2 * p2) & 31) << 2) | ((uint32_t)h << 7);
+            const uint32_t c1 = (((lane + 2 * p2 + 1) & 31) << 2) | ((uint32_t)h << 7);
+            aux2[p2] = c0 | (c1 << 8);
+        }
+        // this warp's tiles of the current table (one per unit); the ring
+        // slots alternate along the warp's whole tile sequence
+        auto step = [&](auto slot, int i) {
+            constexpr int dd = decltype(slot)::value;
+            if (!have[dd]) return;
+            if (alive) *outp[dd] = tile_lookups1_ilp(buf[dd], aux2, lut);
+            if (i == cur.nr - 1 && has_nxt) {
+                // build this warp's share of the next table into the other
+                // half after its last tile of this one (the inputs were
+                // fetched at phase start, so the fetch hides behind the tiles)
+                if (alive) alive = il_wait(inbar, inph, job.status);
+                if (alive) il_build(lut, h ^ 1, cb_s, xs_s, job.x_dtype, warp, lane);
+            }
+            const uint8_t *t;
+            have[dd] = gen(t, outp[dd]);
+            if (have[dd]) load_tile(buf[dd], t);
+        };
+        for (int i = 0; i < cur.nr; ++i) {
+            if (sp == 0)
+                step(std::integral_constant<int, 0>{}, i);
+            else
+                step(std::integral_constant<int, 1>{}, i);
+            sp ^= 1;
+        }
+        if (has_nxt) ++inph;
+        __syncthreads();  // the next table is complete; this half is free
+        cur = nxt;
+        has_cur = has_nxt;
+        has_nxt = has_cur && il_next(job, S, w1, pd, tw, nxt);
+    }
+}
+
 // ---------------------------------------------------------------- reductions
 
 // h[p][r..r+3] = silu(sum_s g) * sum_s u over the split-K slots.  Four
@@ -673,6 +1087,38 @@ rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl) {
     const int grid = work < num_sms() ? work : num_sms();
     RVQ_CUDA(launch_ex(lut_gemv_kernel, dim3(grid), dim3(NT), (size_t)kSmemBytes, stream, pdl,
                        job));
+    return RVQ_OK;
+}
+
+rvq_status launch_lut_plan_pairs(const LutJob &job, int4 *pd, cudaStream_t stream, bool pdl) {
+    if (job.n_pairs == 0) return RVQ_OK;
+    if (!job.offsets || !job.pairs || !job.base || job.E > 256) {
+        set_error("lut_plan_pairs: needs a bank, offsets and pairs (E %d)", job.E);
+        return RVQ_EINVAL;
+    }
+    RVQ_CUDA(launch_ex(plan_pairs_kernel, dim3((job.n_pairs + 255) / 256), dim3(256), 0, stream,
+                       pdl, job, pd));
+    return RVQ_OK;
+}
+
+rvq_status launch_lut_gemv_il(const LutJob &job, const int4 *pd, cudaStream_t stream, bool pdl) {
+    static int attr_done[64] = {0};
+    int dev = 0;
+    RVQ_CUDA(cudaGetDevice(&dev));
+    if (dev < 64 && !attr_done[dev]) {
+        RVQ_CUDA(cudaFuncSetAttribute(lut_gemv_il_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kIlSmemBytes));
+        attr_done[dev] = 1;
+    }
+    if (job.rows % IL_ROWS || job.cols % 256 || job.G != job.cols / 256 || !job.base || !pd) {
+        set_error("lut_gemv_il: rows %d / cols %d not supported", job.rows, job.cols);
+        return RVQ_EINVAL;
+    }
+    const int64_t units = (int64_t)job.n_mat * job.n_pairs * job.G * (job.rows / IL_ROWS);
+    if (units == 0) return RVQ_OK;
+    const int grid = units < num_sms() ? (int)units : num_sms();
+    RVQ_CUDA(launch_ex(lut_gemv_il_kernel, dim3(grid), dim3(NT), (size_t)kIlSmemBytes, stream, pdl,
+                       job, pd));
     return RVQ_OK;
 }
 
