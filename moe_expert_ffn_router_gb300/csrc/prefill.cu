@@ -226,6 +226,17 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                  "r"(v.z), "r"(v.w));
 }
 
+// 128-bit shared load through a 32-bit shared address (no generic address
+// arithmetic).  Not volatile: its address depends on code bytes loaded after
+// every codebook swap, which keeps it behind the swap's barrier.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
         // r0+4..r0+7, type 1 the other halves: (row mod 8) differs per lane
         const int rit = (b8 & 1) == 0 ? r0 + q : (tile == 0 ? r0 + 4 + q : r0 + q - 4);
         const int sw = rit & 7;
-        const uint8_t *cbl = smem + OFF_CB + q * 16;  // this lane's bank group
+        const uint32_t cbl = sbase + OFF_CB + q * 16;  // this lane's bank group
         const int RB = job.rows / 32;
         const int G = KS / 4;                    // 32-chunk groups along K
         int cur_e = -1;
@@ -576,11 +587,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                         const uint32_t k0 = (U[0][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
                         const uint32_t k1 = (U[1][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
                         const uint32_t k2 = (U[2][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
-                        const uint4 w0 = *reinterpret_cast<const uint4 *>(cbl + k0 * kCbLine);
-                        const uint4 w1 =
-                            *reinterpret_cast<const uint4 *>(cbl + (256 + k1) * kCbLine);
-                        const uint4 w2 =
-                            *reinterpret_cast<const uint4 *>(cbl + (512 + k2) * kCbLine);
+                        const uint4 w0 = lds128(cbl + k0 * kCbLine);
+                        const uint4 w1 = lds128(cbl + (256 + k1) * kCbLine);
+                        const uint4 w2 = lds128(cbl + (512 + k2) * kCbLine);
                         uint4 o;
                         o.x = sum3_bf16x2(w0.x, w1.x, w2.x);
                         o.y = sum3_bf16x2(w0.y, w1.y, w2.y);
