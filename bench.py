@@ -50,6 +50,8 @@ WORKLOADS = {
     "decode_d2048_b4": (1, 4),
     "decode_d2048_b16": (1, 16),
     "k3_prefill2048": (4, 2048),
+    "k3_stack8_b1": (3, 1),
+    "k3_stack8_b32": (3, 32),
     "k3_prefill512_e64": (4, 512, 64),  # profiling case: ~128 tokens per expert, 1.06 GB bank
 }
 KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
@@ -177,11 +179,11 @@ def router_bias(config, src):
     return W.zipf_bias(src.lseed, src.shape.E, wl.zipf_beta)
 
 
-def build_layer(config, device, k=None, shape=None):
+def build_layer(config, device, k=None, shape=None, layer=0):
     from moe_expert_ffn_router_gb300.layer import MoeLayer
     s = shape or W.WORKLOADS[config].shape
-    src = W.ExpertSource(config, 0, s)
-    L = MoeLayer(s.E, s.d, s.f, k or s.k, layer=0, device=device)
+    src = W.ExpertSource(config, layer, s)
+    L = MoeLayer(s.E, s.d, s.f, k or s.k, layer=layer, device=device)
     for e in range(s.E):
         mats = [(src.codes(e, m), src.codebooks(e, m)) for m in range(3)]
         L.load_expert(e, mats[0][0], mats[1][0], mats[2][0], np.stack([c for _, c in mats]))
@@ -200,7 +202,11 @@ def run_gpu(args, rank, world, local_rank):
     prefill = W.WORKLOADS[config].kind == "prefill"
     tc_min = 1 if prefill else 0
     kernels = KERNELS_TC if prefill else KERNELS
-    L, src = build_layer(config, dev, shape=s)
+    n_layers = W.WORKLOADS[config].layers if W.WORKLOADS[config].kind == "stack" else 1
+    built = [build_layer(config, dev, shape=s, layer=i) for i in range(n_layers)]
+    L, src = built[0]
+    from moe_expert_ffn_router_gb300.layer import MoeStack
+    stack = MoeStack([b[0] for b in built])
     if prefill:
         pool_bits = src.tokens_bf16(2 * batch)          # two chunks, alternating
     else:
@@ -209,24 +215,28 @@ def run_gpu(args, rank, world, local_rank):
     xs = torch.from_numpy(pool_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     xs = xs.reshape(-1, batch, s.d)
     nsteps = xs.shape[0]
-    bufs = L.buffers(batch)
+    bufs = stack.buffers(batch)[0]
     weights_per_expert = 3 * s.d * s.f
     code_bytes_per_expert = 3 * (3 * s.d * s.f // 8)
     cb_bytes_per_expert = 3 * rvq.RVQ_CODEBOOK_BYTES
 
     def step(i, events=None):
-        return L.forward(xs[i % nsteps], bufs, events=events, tc_min_tokens=tc_min)
+        return stack.forward(xs[i % nsteps], events=events, tc_min_tokens=tc_min)
 
-    # unique experts per step (from the routing the GPU computed); the pool
-    # is replayed identically in the timed loop, so count once per pool entry
-    uniq = []
+    # unique experts per step, summed over the layers (from the routing the
+    # GPU computed); the pool is replayed identically in the timed loop, so
+    # count once per pool entry
+    uniq, uniq0 = [], []
     for i in range(nsteps):
-        step(i)
+        bl = step(i)
         torch.cuda.synchronize()
-        uniq.append(len(set(bufs["idx"].cpu().numpy().reshape(-1).tolist())))
-    rc, bits = L.status(batch)
-    if rc != 0:
-        raise RuntimeError(f"device status {rc} bits {bits:#x}")
+        per = [len(set(b["idx"].cpu().numpy().reshape(-1).tolist())) for b in bl]
+        uniq.append(sum(per))
+        uniq0.append(per[0])
+    for Lx in stack.layers:
+        rc, bits = Lx.status(batch)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} bits {bits:#x}")
 
     def barrier():
         if world > 1:
@@ -297,14 +307,15 @@ def run_gpu(args, rank, world, local_rank):
     else:
         # algorithmic bytes of the gate/up launch: gate + up codes and
         # codebooks of every unique selected expert
-        gu_bytes = np.mean([uniq[j] for j in steps_idx]) * 2 * (
+        gu_bytes = np.mean([uniq0[j] for j in steps_idx]) * 2 * (
             3 * s.d * s.f // 8 + rvq.RVQ_CODEBOOK_BYTES)
         peak, peak_kind = load_peaks()
         achieved = gu_bytes / (avg[DOMINANT] / 1e3) / 1e9
         roofline = {"kernel": DOMINANT, "bound": "hbm", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                     "peak_source": peak_kind,
-                    "traffic": load_traffic(DOMINANT) if s.E == 256 and batch == 1 else None,
+                    "traffic": load_traffic(DOMINANT) if (s.E == 256 and batch == 1
+                                                          and n_layers == 1) else None,
                     "algorithmic_bytes_per_launch": int(gu_bytes),
                     "avg_launch_us": round(avg[DOMINANT] * 1e3, 2)}
 
@@ -313,17 +324,18 @@ def run_gpu(args, rank, world, local_rank):
     pinned_in = pinned_in.pin_memory()
     pinned_out = torch.empty((batch, s.d), dtype=torch.float32).pin_memory()
     xbuf = torch.empty((batch, s.d), dtype=torch.bfloat16, device=dev)
+    out_last = stack.buffers(batch)[-1]["out"]
     for i in range(args.warmup):
         xbuf.view(torch.int16).copy_(pinned_in[i % nsteps], non_blocking=True)
-        L.forward(xbuf, bufs, tc_min_tokens=tc_min)
-        pinned_out.copy_(bufs["out"], non_blocking=True)
+        stack.forward(xbuf, tc_min_tokens=tc_min)
+        pinned_out.copy_(out_last, non_blocking=True)
     barrier()
     e0.record()
     for i in range(args.steps):
         j = (args.warmup + i) % nsteps
         xbuf.view(torch.int16).copy_(pinned_in[j], non_blocking=True)
-        L.forward(xbuf, bufs, tc_min_tokens=tc_min)
-        pinned_out.copy_(bufs["out"], non_blocking=True)
+        stack.forward(xbuf, tc_min_tokens=tc_min)
+        pinned_out.copy_(out_last, non_blocking=True)
     e1.record()
     barrier()
     ms_e2e = e0.elapsed_time(e1)
@@ -334,15 +346,16 @@ def run_gpu(args, rank, world, local_rank):
         ms_e2e = float(tt.item())
     e2e = {"value": round(weights / (ms_e2e / 1e3) / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": batch * s.d * 2, "d2h_bytes_per_step": batch * s.d * 4}
-    rc, bits = L.status(batch)
-    if rc != 0:
-        raise RuntimeError(f"device status {rc} bits {bits:#x}")
+    for Lx in stack.layers:
+        rc, bits = Lx.status(batch)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} bits {bits:#x}")
     res = dict(value=value, ms=ms, code_gbs=code_gbs, tok_s=tok_s, roofline=roofline, e2e=e2e,
                clocks=clocks, kernels_us={k: round(v * 1e3, 2) for k, v in avg.items()},
                uniq_mean=float(np.mean([uniq[j] for j in steps_idx])),
-               launches=(TC_LAUNCHES_PER_STEP if prefill else len(KERNELS)) * args.steps,
-               config=config, batch=batch, shape=s, prefill=prefill)
-    del L
+               launches=(TC_LAUNCHES_PER_STEP if prefill else len(KERNELS)) * args.steps * n_layers,
+               config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
+    del L, stack, built
     return res
 
 
@@ -399,7 +412,10 @@ def reference_arm(args, rank):
     x64 = synth.bf16_to_f32(src.tokens_bf16(ntok)).astype(np.float64)
     idx, _, _ = oracle.route(oracle.router_logits(wr, x64, bias).astype(np.float32), s.k)
     work = [(t, int(e)) for t in range(ntok) for e in idx[t]]
-    uniq = s.k if batch == 1 else oracle_unique_experts(config, batch, src, s)
+    layers = W.WORKLOADS[config].layers if W.WORKLOADS[config].kind == "stack" else 1
+    # distinct experts per batch: exact for one token; for a stack the first
+    # layer's count stands for every layer (independent seeds, same shape)
+    uniq = layers * (s.k if batch == 1 else oracle_unique_experts(config, batch, src, s))
     times, npairs, pos = 0.0, 0, 0
     for i in range(args.warmup + args.steps):
         chunk = work[pos:pos + m]
@@ -413,14 +429,14 @@ def reference_arm(args, rank):
         if i >= args.warmup:
             times += dt
             npairs += len(chunk)
-    step_s = times / npairs * batch * s.k
+    step_s = times / npairs * batch * s.k * layers
     value = uniq * 3 * s.d * s.f / step_s / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(step_s * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload + ":" + W.WORKLOADS[config].name,
-                       "batch": batch, "experts": s.E},
+                       "batch": batch, "experts": s.E, "layers": layers},
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1,
                              "kind": "oracle",
                              "sample": f"{m} (token, expert) pairs of the {batch * s.k} per "
@@ -462,11 +478,11 @@ def main():
         cpu = None
         if not args.no_cpu_baseline:
             tok_s = oracle_sample(r["config"], args.oracle_tokens, shape=r["shape"])
-            v = r["uniq_mean"] * 3 * s.d * s.f / (tok_s * r["batch"]) / 1e9
+            v = r["uniq_mean"] * 3 * s.d * s.f / (tok_s * r["batch"] * r["layers"]) / 1e9
             cpu = {"value": round(v, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{args.oracle_tokens} tokens through the whole oracle layer "
                              f"({tok_s:.2f} s per token), scaled to the {r['batch']}-token "
-                             "batch and its distinct experts"}
+                             f"batch, {r['layers']} layer(s) and their distinct experts"}
         line = {
             "metric": METRIC, "value": round(r["value"], 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4),
@@ -474,10 +490,11 @@ def main():
             "dtype": "bf16" if r["prefill"] else "f32",
             "data": "synthetic",
             "config": {"workload": args.workload + ":" + W.WORKLOADS[r["config"]].name,
-                       "batch": r["batch"],
+                       "batch": r["batch"], "layers": r["layers"],
                        "d": s.d, "f": s.f, "experts": s.E, "top_k": s.k,
-                       "codes_bytes": 3 * (3 * s.d * s.f // 8) * s.E,
-                       "l2": f"inputs larger than L2: {3 * (3 * s.d * s.f // 8) * s.E / 1e9:.2f} "
+                       "codes_bytes": 3 * (3 * s.d * s.f // 8) * s.E * r["layers"],
+                       "l2": f"inputs larger than L2: "
+                             f"{3 * (3 * s.d * s.f // 8) * s.E * r['layers'] / 1e9:.2f} "
                              "GB code bank (L2 129 MB); token pool rotates routing every step",
                        "parallelism": f"replicas{world}",
                        "path": ("tensor cores for every expert group (bf16 operands, "

@@ -110,4 +110,33 @@ class MoeLayer:
         return rvq_ws_status(self.workspace(n))
 
 
-__all__ = ["MoeLayer", "RVQ_WS_STATUS_BYTES"]
+class MoeStack:
+    """Layers applied in order to a residual stream: layer i's fp32 output is
+    layer i+1's input.  Each layer keeps its own buffers, so the stream is
+    never copied."""
+
+    def __init__(self, layers: list[MoeLayer]):
+        assert layers and all(L.d == layers[0].d for L in layers)
+        self.layers = layers
+        self._bufs = {}
+
+    def buffers(self, n: int) -> list[dict]:
+        b = self._bufs.get(n)
+        if b is None:
+            b = [L.buffers(n) for L in self.layers]
+            self._bufs[n] = b
+        return b
+
+    def forward(self, x: torch.Tensor, events=None, tc_min_tokens: int = 0) -> list[dict]:
+        """Runs every layer; returns the per-layer buffers (the last one's
+        "out" is the stack output).  `events`, if given, are layer 0's."""
+        n = x.shape[0]
+        bufs = self.buffers(n)
+        h = x
+        for i, L in enumerate(self.layers):
+            L.forward(h, bufs[i], events=events if i == 0 else None, tc_min_tokens=tc_min_tokens)
+            h = bufs[i]["out"]
+        return bufs
+
+
+__all__ = ["MoeLayer", "MoeStack", "RVQ_WS_STATUS_BYTES"]

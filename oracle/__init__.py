@@ -53,6 +53,7 @@ def _load():
                 "oracle_swiglu": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
                 "oracle_expert_ffn": (None, [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp]),
                 "oracle_combine": (None, [vp, vp, i32, i32, i32, vp, vp]),
+                "oracle_rms_norm": (None, [vp, i32, i32, ctypes.c_double, vp]),
                 "oracle_moe_layer": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp, vp]),
             }
@@ -170,6 +171,15 @@ def combine(y_pair, topk_w, residual):
     y = _c(y_pair, np.float64).reshape(n * k, d)
     out = np.empty((n, d), np.float64)
     _load().oracle_combine(_p(y), _p(w), n, k, d, _p(res), _p(out))
+    return out
+
+
+def rms_norm(x, eps=1e-6):
+    """Row-wise x / sqrt(mean(x^2) + eps), float64 [n][d] (stack pre-norm)."""
+    xx = _c(np.atleast_2d(x), np.float64)
+    n, d = xx.shape
+    out = np.empty((n, d), np.float64)
+    _load().oracle_rms_norm(_p(xx), n, d, float(eps), _p(out))
     return out
 
 

@@ -247,6 +247,21 @@ void oracle_combine(const double *y_pair, const float *topk_w, int32_t n, int32_
         }
 }
 
+/* Parameter-free RMS normalisation of each row (reading: the pages describe
+ * no normalisation; a stack of their layers applies this before each layer,
+ * as pre-norm transformer blocks do, and keeps the un-normalised stream as
+ * the residual):  out[t][c] = x[t][c] / sqrt(mean_c x[t][c]^2 + eps). */
+void oracle_rms_norm(const double *x, int32_t n, int32_t d, double eps, double *out)
+{
+    for (int32_t t = 0; t < n; ++t) {
+        const double *r = x + (size_t)t * d;
+        double ss = 0.0;
+        for (int32_t c = 0; c < d; ++c) ss += r[c] * r[c];
+        const double inv = 1.0 / sqrt(ss / (double)d + eps);
+        for (int32_t c = 0; c < d; ++c) out[(size_t)t * d + c] = r[c] * inv;
+    }
+}
+
 /* One MoE layer on n tokens, given each expert's three matrices through
  * pointer tables (entries of unselected experts may be NULL).  Routing uses
  * the fp32 logits passed in (route_logits); when that is NULL the oracle's own

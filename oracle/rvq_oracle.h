@@ -29,6 +29,7 @@ void oracle_expert_ffn(const uint8_t *gate_codes, const float *gate_cb,
                        int32_t d, int32_t f, const double *x, double *y, double *h_out);
 void oracle_combine(const double *y_pair, const float *topk_w, int32_t n, int32_t k,
                     int32_t d, const double *residual, double *out);
+void oracle_rms_norm(const double *x, int32_t n, int32_t d, double eps, double *out);
 int32_t oracle_moe_layer(const uint8_t *const *codes, const float *const *cbs,
                          const float *wr, const float *bias,
                          int32_t n, int32_t E, int32_t k, int32_t d, int32_t f,

@@ -350,3 +350,32 @@ def test_router_bias_is_added():
     x = rng.normal(size=(2, d))
     np.testing.assert_allclose(oracle.router_logits(wr, x, b) - oracle.router_logits(wr, x),
                                np.broadcast_to(b.astype(np.float64), (2, E)), atol=1e-13)
+
+
+# ------------------------------------------------------------ rms norm (stack)
+
+def test_rms_norm_closed_forms():
+    """Constant rows map to +-1/sqrt(1 + eps/c^2); a row of +-a values has unit
+    RMS after the norm; a one-hot row scales to sqrt(d) (eps = 0)."""
+    d = 64
+    c = np.array([[3.0] * d, [-0.5] * d])
+    y = oracle.rms_norm(c, eps=0.0)
+    assert np.allclose(y[0], 1.0, rtol=0, atol=1e-15) and np.allclose(y[1], -1.0, rtol=0, atol=1e-15)
+    y = oracle.rms_norm(np.array([[2.0] * d]), eps=0.25)
+    assert np.allclose(y, 2.0 / np.sqrt(4.0 + 0.25), rtol=1e-15, atol=0)
+    onehot = np.zeros((1, d))
+    onehot[0, 5] = 7.0
+    y = oracle.rms_norm(onehot, eps=0.0)
+    assert abs(y[0, 5] - np.sqrt(d)) < 1e-12 and np.count_nonzero(y) == 1
+
+
+def test_rms_norm_invariants():
+    """Unit mean square for eps = 0, invariance to positive scaling, odd
+    symmetry, rows independent of each other."""
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(6, 96)) * rng.uniform(0.1, 50, size=(6, 1))
+    y = oracle.rms_norm(x, eps=0.0)
+    assert np.allclose((y * y).mean(axis=1), 1.0, rtol=1e-13)
+    assert np.allclose(oracle.rms_norm(3.7 * x, eps=0.0), y, rtol=1e-13)
+    assert np.allclose(oracle.rms_norm(-x, eps=0.0), -y, rtol=0, atol=0)
+    assert np.allclose(oracle.rms_norm(x[2:3], eps=0.0), y[2:3], rtol=0, atol=0)
