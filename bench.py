@@ -45,6 +45,8 @@ WORKLOADS = {
     "k3_decode_b1": (2, 1),
     "k3_decode_b1_e64": (2, 1, 64),   # profiling case: same experts, 1.06 GB bank
     "k3_decode_b8": (2, 8),
+    "k3_decode_b16": (2, 16),
+    "k3_decode_b32": (2, 32),
     "k3_decode_b64": (2, 64),
     "decode_d2048_b1": (1, 1),
     "decode_d2048_b4": (1, 4),
@@ -201,7 +203,9 @@ def run_gpu(args, rank, world, local_rank):
     config, batch, s = workload_shape(args.workload)
     prefill = W.WORKLOADS[config].kind == "prefill"
     tc_min = 1 if prefill else 0
-    kernels = KERNELS_TC if prefill else KERNELS
+    if args.tc_min_tokens is not None:
+        tc_min = args.tc_min_tokens
+    kernels = KERNELS_TC if tc_min > 0 else KERNELS
     n_layers = W.WORKLOADS[config].layers if W.WORKLOADS[config].kind == "stack" else 1
     built = [build_layer(config, dev, shape=s, layer=i) for i in range(n_layers)]
     L, src = built[0]
@@ -287,7 +291,7 @@ def run_gpu(args, rank, world, local_rank):
         for j, name in enumerate(kernels):
             per[name].append(evs[j].elapsed_time(evs[j + 1]))
     avg = {k: float(np.mean(v)) for k, v in per.items() if k != "unused"}
-    if prefill:
+    if tc_min > 0:
         # useful FLOPs: 2 per multiply-add, gate + up (2 d f) then down (d f)
         # for each of the n k routed (token, expert) pairs
         pairs = batch * s.k
@@ -353,7 +357,8 @@ def run_gpu(args, rank, world, local_rank):
     res = dict(value=value, ms=ms, code_gbs=code_gbs, tok_s=tok_s, roofline=roofline, e2e=e2e,
                clocks=clocks, kernels_us={k: round(v * 1e3, 2) for k, v in avg.items()},
                uniq_mean=float(np.mean([uniq[j] for j in steps_idx])),
-               launches=(TC_LAUNCHES_PER_STEP if prefill else len(KERNELS)) * args.steps * n_layers,
+               launches=(TC_LAUNCHES_PER_STEP if tc_min == 1 else len(KERNELS) if tc_min == 0
+                         else len(KERNELS) + TC_LAUNCHES_PER_STEP - 3) * args.steps * n_layers,
                config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
     del L, stack, built
     return res
@@ -456,6 +461,9 @@ def main():
     ap.add_argument("--workload", default="k3_decode_b1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--oracle-tokens", type=int, default=4)
+    ap.add_argument("--tc-min-tokens", type=int, default=None,
+                    help="experts with at least this many tokens take the tensor-core path "
+                         "(default: 1 for the prefill workload, 0 = lookup tables only, otherwise)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (profiling runs)")
     args = ap.parse_args()

@@ -290,17 +290,33 @@ rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, cons
                              void *ws_dev, size_t ws_bytes, void **events,
                              rvq_stream_t stream);
 
-/* As moe_layer_forward, with the per-expert tensor-core dispatch of
- * moe_expert_ffn_ex (tc_min_tokens <= 0: lookup tables only).  With dispatch
- * the event marks are: 0 start, 1 router logits, 2 routing, 3 lookup-table
- * experts done, 4 tensor-core gate/up GEMM, 5 tensor-core down GEMM, 6 = 5,
- * 7 combine. */
+/* As moe_layer_forward, with two additions.
+ *  - residual_dev (dtype rdt, [n][d], 16-byte aligned; NULL: x itself) is the
+ *    stream the combine adds to: out = residual + sum_slot w * expert(x).  A
+ *    layer stack passes the normalised stream as x and the raw stream here.
+ *    A bf16 residual must not alias out (EINVAL).
+ *  - the per-expert tensor-core dispatch of moe_expert_ffn_ex (tc_min_tokens
+ *    <= 0: lookup tables only).  With dispatch the event marks are: 0 start,
+ *    1 router logits, 2 routing, 3 lookup-table experts done, 4 tensor-core
+ *    gate/up GEMM, 5 tensor-core down GEMM, 6 = 5, 7 combine. */
 rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
                                 const float *bias_dev, const void *x_dev, rvq_dtype xdt, int32_t n,
                                 int32_t k, float *logits_dev, int32_t *topk_idx_dev,
                                 float *topk_w_dev, int32_t *offsets_dev, int32_t *pairs_dev,
                                 float *out_dev, void *ws_dev, size_t ws_bytes,
-                                int32_t tc_min_tokens, void **events, rvq_stream_t stream);
+                                const void *residual_dev, rvq_dtype rdt, int32_t tc_min_tokens,
+                                void **events, rvq_stream_t stream);
+
+/* Row-wise RMS normalisation without a gain, the pre-norm of a layer stack:
+ * out[t][c] = x[t][c] / sqrt(mean_c x[t][c]^2 + eps), sums in fp32.
+ * The pages describe no normalisation: a stack of their layers (router,
+ * top-k, RVQ SwiGLU experts, combine + residual) without one grows without
+ * bound (the expert FFN is quadratic in its input), so the stack applies
+ * this before each layer, as pre-norm transformer blocks do.
+ * x: dtype xdt [n][d]; out: dtype odt [n][d]; d % 4 == 0; both 16-byte
+ * aligned (EALIGN); eps >= 0; x may alias out only when both are fp32. */
+rvq_status moe_rms_norm(const void *x_dev, rvq_dtype xdt, int32_t n, int32_t d, float eps,
+                        void *out_dev, rvq_dtype odt, rvq_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * Workspace status block.

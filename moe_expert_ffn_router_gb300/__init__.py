@@ -75,7 +75,8 @@ _SIGS = {
     "moe_layer_forward": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
                                  _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_layer_forward_ex": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp,
-                                    _vp, _vp, _vp, _vp, _sz, _i32, _vp, _vp]),
+                                    _vp, _vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp]),
+    "moe_rms_norm": (_i32, [_vp, _i32, _i32, _i32, ctypes.c_float, _vp, _i32, _vp]),
     "rvq_ws_clear": (_i32, [_vp, _vp]),
     "rvq_ws_status": (_i32, [_vp, ctypes.POINTER(_u32), _vp]),
 }
@@ -252,16 +253,22 @@ def moe_combine(y_pair, topk_w, n, k, d, residual, out, stream=None):
 
 
 def moe_layer_forward(bank, wr, bias, x, n, k, logits, topk_idx, topk_w, offsets, pairs, out,
-                      ws, events=None, stream=None, tc_min_tokens=0):
+                      ws, events=None, stream=None, tc_min_tokens=0, residual=None):
     ev = None
     if events is not None:
         assert len(events) == MOE_LAYER_EVENTS
         ev = (ctypes.c_void_p * MOE_LAYER_EVENTS)(*[e.cuda_event for e in events])
+    rdt = _dt(residual) if residual is not None else _dt(x)
     _check("moe_layer_forward",
            _lib.moe_layer_forward_ex(ctypes.byref(bank), _p(wr), _p(bias), _p(x), _dt(x), n, k,
                                      _p(logits), _p(topk_idx), _p(topk_w), _p(offsets),
-                                     _p(pairs), _p(out), _p(ws), _nbytes(ws), int(tc_min_tokens),
-                                     ev, _stream(stream)))
+                                     _p(pairs), _p(out), _p(ws), _nbytes(ws), _p(residual), rdt,
+                                     int(tc_min_tokens), ev, _stream(stream)))
+
+
+def moe_rms_norm(x, n, d, out, eps=1e-6, stream=None):
+    _check("moe_rms_norm", _lib.moe_rms_norm(_p(x), _dt(x), n, d, float(eps), _p(out), _dt(out),
+                                             _stream(stream)))
 
 
 def rvq_ws_clear(ws, stream=None):

@@ -470,9 +470,11 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     dn.pairs = pairs_dev;
     dn.desc = (ItemDesc *)(ws + P.off_desc_d);
     gu.tc_min_tokens = dn.tc_min_tokens = tc_min_tokens;
-    if (P.C_gu == 1 && P.C_d == 1 && n <= 8) {
-        // decode batches: build/stream overlapped units; the pair plan reuses
-        // the gate/up descriptor space (>= n_pairs x 16 bytes)
+    if (P.C_gu == 1 && P.C_d == 1 && n <= 16) {
+        // decode batches up to 16 tokens: one-token units with the table build
+        // interleaved into the streaming (measured faster than two-token items
+        // up to 16 tokens, slower from 32); the pair plan reuses the gate/up
+        // descriptor space (>= n_pairs x 16 bytes)
         int4 *pd = (int4 *)(ws + P.off_desc_gu);
         RVQ_TRY(launch_lut_plan_pairs(gu, pd, st, pdl));
         RVQ_TRY(mark(0));
@@ -610,13 +612,36 @@ rvq_status moe_combine(const float *y_pair_dev, const float *topk_w_dev, int32_t
                           (cudaStream_t)stream, false);
 }
 
+rvq_status moe_rms_norm(const void *x_dev, rvq_dtype xdt, int32_t n, int32_t d, float eps,
+                        void *out_dev, rvq_dtype odt, rvq_stream_t stream) {
+    CHECK_ARG(x_dev && out_dev, "moe_rms_norm: null pointer");
+    CHECK_ARG(n >= 1 && d >= 4 && d % 4 == 0, "moe_rms_norm: n %d, d %d", n, d);
+    CHECK_ARG((xdt == RVQ_F32 || xdt == RVQ_BF16) && (odt == RVQ_F32 || odt == RVQ_BF16),
+              "moe_rms_norm: dtypes %d, %d", (int)xdt, (int)odt);
+    CHECK_ARG(eps >= 0.f, "moe_rms_norm: eps %g", (double)eps);
+    CHECK_ALIGN(x_dev, "moe_rms_norm: x");
+    CHECK_ALIGN(out_dev, "moe_rms_norm: out");
+    return launch_rms_norm(x_dev, (int)xdt, n, d, eps, out_dev, (int)odt, (cudaStream_t)stream,
+                           false);
+}
+
 rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
                                 const float *bias_dev, const void *x_dev, rvq_dtype xdt, int32_t n,
                                 int32_t k, float *logits_dev, int32_t *topk_idx_dev,
                                 float *topk_w_dev, int32_t *offsets_dev, int32_t *pairs_dev,
                                 float *out_dev, void *ws_dev, size_t ws_bytes,
-                                int32_t tc_min_tokens, void **events, rvq_stream_t stream) {
+                                const void *residual_dev, rvq_dtype rdt, int32_t tc_min_tokens,
+                                void **events, rvq_stream_t stream) {
     RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_layer_forward"));
+    if (!residual_dev) {
+        residual_dev = x_dev;
+        rdt = xdt;
+    }
+    CHECK_ARG(rdt == RVQ_F32 || rdt == RVQ_BF16, "moe_layer_forward: residual dtype %d", (int)rdt);
+    CHECK_ALIGN(residual_dev, "moe_layer_forward: residual");
+    if (rdt == RVQ_BF16)
+        CHECK_ARG((const void *)out_dev != residual_dev,
+                  "moe_layer_forward: bf16 residual cannot alias out");
     CHECK_ARG(wr_dev && logits_dev && topk_idx_dev && topk_w_dev && offsets_dev && pairs_dev &&
                   out_dev,
               "moe_layer_forward: null pointer");
@@ -643,8 +668,8 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
         RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st,
                         events ? events + 3 : nullptr, pdl));
         float *dpart = (float *)((uint8_t *)ws_dev + P.off_dpart);
-        RVQ_TRY(launch_combine(dpart, P.nslot_d, topk_w_dev, n, k, bank->d, x_dev, (int)xdt,
-                               out_dev, st, pdl));
+        RVQ_TRY(launch_combine(dpart, P.nslot_d, topk_w_dev, n, k, bank->d, residual_dev,
+                               (int)rdt, out_dev, st, pdl));
         return mark(7);
     }
     // with tensor-core dispatch: marks 3 = lookup-table experts done, 4 = after the
@@ -661,7 +686,8 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
                        tc_min_tokens, st, pdl, events ? events[4] : nullptr));
     RVQ_TRY(mark(5));
     RVQ_TRY(mark(6));
-    RVQ_TRY(launch_combine(ypair, 1, topk_w_dev, n, k, bank->d, x_dev, (int)xdt, out_dev, st, pdl));
+    RVQ_TRY(launch_combine(ypair, 1, topk_w_dev, n, k, bank->d, residual_dev, (int)rdt, out_dev,
+                           st, pdl));
     return mark(7);
 }
 
@@ -671,8 +697,8 @@ rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, cons
                              int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
                              void *ws_dev, size_t ws_bytes, void **events, rvq_stream_t stream) {
     return moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
-                                topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes, 0,
-                                events, stream);
+                                topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
+                                nullptr, xdt, 0, events, stream);
 }
 
 rvq_status rvq_ws_clear(void *ws_dev, rvq_stream_t stream) {

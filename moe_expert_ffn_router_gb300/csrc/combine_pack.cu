@@ -102,6 +102,45 @@ __global__ void __launch_bounds__(256) combine1_kernel(const float *__restrict__
     *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
 }
 
+// Row-wise RMS normalisation without a gain (the layer stack's pre-norm):
+// out = x / sqrt(mean(x^2) + eps), sums in fp32, one block per row.
+__global__ void __launch_bounds__(256) rms_norm_kernel(const void *__restrict__ x, int xdt, int d,
+                                                       float eps, void *__restrict__ out,
+                                                       int odt) {
+    __shared__ float red[8];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int64_t row = (int64_t)blockIdx.x * d;
+    const int d4 = d >> 2;
+    float ss = 0.f;
+    for (int c4 = threadIdx.x; c4 < d4; c4 += blockDim.x) {
+        const float4 v = load4(x, xdt, row + c4 * 4);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)d + eps);
+    for (int c4 = threadIdx.x; c4 < d4; c4 += blockDim.x) {
+        const float4 v = load4(x, xdt, row + c4 * 4);
+        const float4 y = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+        if (odt == RVQ_BF16) {
+            uint2 b;
+            b.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
+            b.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
+            *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(out) + row + c4 * 4) = b;
+        } else {
+            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + row + c4 * 4) = y;
+        }
+    }
+}
+
 // One thread per 16-byte packed word.  Packed word (tile g,b; stage s; half h;
 // lane l) byte i <-> canonical code (row 32b+l, chunk 32g+((16h+i+l) mod 32), s).
 __global__ void pack_kernel(const uint8_t *__restrict__ src, int rows, int cols,
@@ -155,6 +194,22 @@ __global__ void write_header_kernel(uint8_t *record, rvq_expert_header h) {
 }
 
 }  // namespace
+
+rvq_status launch_rms_norm(const void *x, int xdt, int n, int d, float eps, void *out, int odt,
+                           cudaStream_t stream, bool pdl) {
+    if (n == 0) return RVQ_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, rms_norm_kernel, x, xdt, d, eps, out, odt));
+    return RVQ_OK;
+}
 
 rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
                           const void *res, int rdt, float *out, cudaStream_t stream, bool pdl) {

@@ -80,6 +80,16 @@ __device__ __forceinline__ void load8(const void *base, int dtype, int64_t idx, 
     }
 }
 
+// Four consecutive inputs (fp32 or bf16) at element idx (idx % 4 == 0) as fp32.
+__device__ __forceinline__ float4 load4(const void *base, int dtype, int64_t idx) {
+    if (dtype == RVQ_BF16) {
+        const uint2 q = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(base) + idx);
+        return make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
+                           __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
+    }
+    return *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + idx);
+}
+
 __device__ __forceinline__ float load1(const void *base, int dtype, int64_t idx) {
     if (dtype == RVQ_BF16)
         return __uint_as_float(
@@ -148,6 +158,8 @@ rvq_status launch_swiglu_reduce(const float *gpart, const float *upart, int n_pa
 // y[entry][r] = sum_slot part[entry][slot][r]
 rvq_status launch_slot_reduce(const float *part, int n_entries, int nslot, int rows, float *y,
                               cudaStream_t stream, bool pdl);
+rvq_status launch_rms_norm(const void *x, int xdt, int n, int d, float eps, void *out, int odt,
+                           cudaStream_t stream, bool pdl);
 rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
                           const void *res, int rdt, float *out, cudaStream_t stream, bool pdl);
 rvq_status launch_router_logits(const float *wr, const float *bias, const void *x, int xdt,

@@ -7,7 +7,8 @@ import torch
 
 from . import (RVQ_WS_STATUS_BYTES, moe_bank_init, moe_bank_record_bytes, moe_bank_validate,
                moe_bank_write_expert, moe_combine, moe_expert_ffn, moe_layer_forward,
-               moe_route, moe_router_logits, moe_workspace_bytes, rvq_ws_clear, rvq_ws_status)
+               moe_rms_norm, moe_route, moe_router_logits, moe_workspace_bytes, rvq_ws_clear,
+               rvq_ws_status)
 
 
 def _dev(a, device, dtype=None):
@@ -83,14 +84,15 @@ class MoeLayer:
 
     # ----------------------------------------------------------------- compute
     def forward(self, x: torch.Tensor, bufs: dict | None = None, events=None,
-                tc_min_tokens: int = 0) -> dict:
-        """Whole layer: out = x + sum_slot w * expert(x).  Experts with at
-        least tc_min_tokens tokens use the tensor-core path (0: none)."""
+                tc_min_tokens: int = 0, residual: torch.Tensor | None = None) -> dict:
+        """Whole layer: out = residual + sum_slot w * expert(x) (residual
+        defaults to x).  Experts with at least tc_min_tokens tokens use the
+        tensor-core path (0: none)."""
         n = x.shape[0]
         b = bufs or self.buffers(n)
         moe_layer_forward(self.bank, self.wr, self.bias, x, n, self.k, b["logits"], b["idx"],
                           b["w"], b["offsets"], b["pairs"], b["out"], b["ws"], events=events,
-                          tc_min_tokens=tc_min_tokens)
+                          tc_min_tokens=tc_min_tokens, residual=residual)
         return b
 
     def forward_steps(self, x: torch.Tensor) -> dict:
@@ -111,19 +113,24 @@ class MoeLayer:
 
 
 class MoeStack:
-    """Layers applied in order to a residual stream: layer i's fp32 output is
-    layer i+1's input.  Each layer keeps its own buffers, so the stream is
-    never copied."""
+    """Layers applied in order to a residual stream h (the first layer's
+    input, then each layer's fp32 output): layer i computes
+    out = h + sum_slot w * expert(rms_norm(h)), the normalised stream in
+    bf16.  Each layer keeps its own buffers (its "xn" holds the normalised
+    input), so the stream is never copied."""
 
-    def __init__(self, layers: list[MoeLayer]):
+    def __init__(self, layers: list[MoeLayer], eps: float = 1e-6):
         assert layers and all(L.d == layers[0].d for L in layers)
         self.layers = layers
+        self.eps = eps
         self._bufs = {}
 
     def buffers(self, n: int) -> list[dict]:
         b = self._bufs.get(n)
         if b is None:
             b = [L.buffers(n) for L in self.layers]
+            for L, bl in zip(self.layers, b):
+                bl["xn"] = torch.empty((n, L.d), dtype=torch.bfloat16, device=L.device)
             self._bufs[n] = b
         return b
 
@@ -134,7 +141,9 @@ class MoeStack:
         bufs = self.buffers(n)
         h = x
         for i, L in enumerate(self.layers):
-            L.forward(h, bufs[i], events=events if i == 0 else None, tc_min_tokens=tc_min_tokens)
+            moe_rms_norm(h, n, L.d, bufs[i]["xn"], eps=self.eps)
+            L.forward(bufs[i]["xn"], bufs[i], events=events if i == 0 else None,
+                      tc_min_tokens=tc_min_tokens, residual=h)
             h = bufs[i]["out"]
         return bufs
 

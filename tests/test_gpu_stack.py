@@ -1,9 +1,10 @@
-"""GPU parity for the K3-shaped layer stack (independent seeds per layer,
-fp32 residual stream between layers): each layer's routing bit-exact given
-the GPU's logits and its outputs within 1e-4 x RMS of the oracle layer fed
-with the same input; the stream is chained without copies.  Two of the
-eight layers at full size (8.5 GB of codes) keep the test within minutes;
-the bench runs all eight."""
+"""GPU parity for the K3-shaped layer stack (independent seeds per layer, an
+fp32 residual stream, each layer fed the stream's RMS norm in bf16): the
+norm within bf16 rounding of the oracle's, each layer's routing bit-exact
+given the GPU's logits, its outputs within 1e-4 x RMS of the oracle layer
+fed the same normalised input and residual.  Two of the eight layers at full
+size (8.5 GB of codes) keep the test within minutes; the bench runs all
+eight."""
 import numpy as np
 import pytest
 import torch
@@ -15,6 +16,22 @@ from tests.support import SynthLayer, assert_rms_close, bf16_bits_to_f64
 pytestmark = pytest.mark.gpu
 rvq = pytest.importorskip("moe_expert_ffn_router_gb300")
 DEV = "cuda"
+
+
+def test_rms_norm_kernel():
+    """moe_rms_norm against the oracle: bf16 and fp32 in and out, ragged
+    magnitudes, a zero row (eps keeps it finite)."""
+    rng = np.random.default_rng(3)
+    n, d = 37, 7168
+    x = (rng.normal(size=(n, d)) * rng.uniform(1e-3, 1e3, size=(n, 1))).astype(np.float32)
+    x[5] = 0.0
+    ref = oracle.rms_norm(x.astype(np.float64), eps=1e-6)
+    for odt, tol in ((torch.float32, 1e-5), (torch.bfloat16, 2.0 ** -8)):
+        out = torch.empty((n, d), dtype=odt, device=DEV)
+        rvq.moe_rms_norm(torch.from_numpy(x).to(DEV), n, d, out, eps=1e-6)
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        assert np.all(np.abs(got - ref) <= tol * np.abs(ref) + 1e-7), odt
 
 
 @pytest.mark.parametrize("n,sample", [(1, [0]), (32, [0, 31])])
@@ -32,6 +49,10 @@ def test_k3_stack_two_layers(n, sample):
         assert L.status(n) == (0, 0)
     h = bf16_bits_to_f64(bits)
     for i, (sl, b) in enumerate(zip(sls, bufs)):
+        xn = b["xn"].float().cpu().numpy().astype(np.float64)   # exact bf16 values
+        ref_xn = oracle.rms_norm(h, eps=stack.eps)
+        assert np.abs(xn - ref_xn).max() <= 2.0 ** -8 * np.abs(ref_xn).max() + 1e-30, f"layer {i} norm"
+        assert np.all(np.abs(xn - ref_xn) <= 2.0 ** -8 * np.abs(ref_xn) + 1e-6), f"layer {i} norm"
         logits = b["logits"].cpu().numpy()
         idx = b["idx"].cpu().numpy()
         ridx, _, _ = oracle.route(logits, s.k)
@@ -39,12 +60,13 @@ def test_k3_stack_two_layers(n, sample):
         roff, rpairs = oracle.group(ridx, s.E)
         assert np.array_equal(b["offsets"].cpu().numpy(), roff)
         assert np.array_equal(b["pairs"].cpu().numpy(), rpairs)
-        assert_rms_close(logits, oracle.router_logits(sl.wr, h), 1e-5, f"layer {i} logits")
+        assert_rms_close(logits, oracle.router_logits(sl.wr, xn), 1e-5, f"layer {i} logits")
         out = b["out"].cpu().numpy().astype(np.float64)
         for t in sample:
-            r = oracle.moe_layer(sl.expert, sl.wr, h[t:t + 1], s.k, s.d, s.f,
+            r = oracle.moe_layer(sl.expert, sl.wr, xn[t:t + 1], s.k, s.d, s.f,
                                  route_logits=logits[t:t + 1])
-            assert_rms_close(out[t] - h[t], r["out"][0] - h[t], 1e-4, f"layer {i} token {t}")
+            delta = r["out"][0] - xn[t]          # sum_slot w * expert(xn)
+            assert_rms_close(out[t] - h[t], delta, 1e-4, f"layer {i} token {t}")
         h = out  # next layer's input is exactly this layer's fp32 output
         sl.forget()
     del stack, bufs
