@@ -318,6 +318,18 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
 rvq_status moe_rms_norm(const void *x_dev, rvq_dtype xdt, int32_t n, int32_t d, float eps,
                         void *out_dev, rvq_dtype odt, rvq_stream_t stream);
 
+/* Self-test of the failure path of the tensor-core kernel (no counterpart in
+ * the pages): launches the prefill GEMM on one zero token routed to expert 0
+ * with its MMA role first waiting for an mbarrier arrival that nothing makes.
+ * The bounded wait (1 s) expires, every role of every block gives up, the
+ * kernel frees its tensor memory and returns; afterwards rvq_ws_status()
+ * reports RVQ_ETIMEOUT (bit RVQ_DEV_ERR_TIMEOUT) and the context stays usable.
+ * No GPU fault, trap or hang is involved.  ws: as for moe_layer_forward with
+ * n = 1, k = 1 (its contents are overwritten).  Synchronises the stream once
+ * before the launch. */
+rvq_status rvq_selftest_prefill_timeout(const rvq_moe_bank *bank, void *ws_dev, size_t ws_bytes,
+                                        rvq_stream_t stream);
+
 /* --------------------------------------------------------------------------
  * Workspace status block.
  * rvq_ws_clear: zero the status block (async).  Call once per workspace.

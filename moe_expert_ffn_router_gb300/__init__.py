@@ -77,6 +77,7 @@ _SIGS = {
     "moe_layer_forward_ex": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp,
                                     _vp, _vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp]),
     "moe_rms_norm": (_i32, [_vp, _i32, _i32, _i32, ctypes.c_float, _vp, _i32, _vp]),
+    "rvq_selftest_prefill_timeout": (_i32, [_BANKP, _vp, _sz, _vp]),
     "rvq_ws_clear": (_i32, [_vp, _vp]),
     "rvq_ws_status": (_i32, [_vp, ctypes.POINTER(_u32), _vp]),
 }
@@ -264,6 +265,12 @@ def moe_layer_forward(bank, wr, bias, x, n, k, logits, topk_idx, topk_w, offsets
                                      _p(logits), _p(topk_idx), _p(topk_w), _p(offsets),
                                      _p(pairs), _p(out), _p(ws), _nbytes(ws), _p(residual), rdt,
                                      int(tc_min_tokens), ev, _stream(stream)))
+
+
+def rvq_selftest_prefill_timeout(bank, ws, stream=None):
+    _check("rvq_selftest_prefill_timeout",
+           _lib.rvq_selftest_prefill_timeout(ctypes.byref(bank), _p(ws), _nbytes(ws),
+                                             _stream(stream)))
 
 
 def moe_rms_norm(x, n, d, out, eps=1e-6, stream=None):

@@ -701,6 +701,60 @@ rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, cons
                                 nullptr, xdt, 0, events, stream);
 }
 
+rvq_status rvq_selftest_prefill_timeout(const rvq_moe_bank *bank, void *ws_dev, size_t ws_bytes,
+                                        rvq_stream_t stream) {
+    RVQ_TRY(check_bank(bank, "rvq_selftest_prefill_timeout"));
+    CHECK_ARG(ws_dev && ((uintptr_t)ws_dev & 255u) == 0,
+              "rvq_selftest_prefill_timeout: workspace must be 256-byte aligned");
+    CHECK_ARG(ws_bytes >= moe_workspace_bytes(bank, 1, 1),
+              "rvq_selftest_prefill_timeout: workspace %zu < %zu", ws_bytes,
+              moe_workspace_bytes(bank, 1, 1));
+    const int E = bank->n_experts;
+    const FfnPlan P = plan_ffn(bank->d, bank->f, 1, E);
+    uint8_t *ws = (uint8_t *)ws_dev;
+    cudaStream_t st = (cudaStream_t)stream;
+    // one token routed to expert 0: offsets and pairs in the gate partial
+    // region, a zero input row in the y region, h16 as the output
+    int32_t host[258];
+    host[0] = 0;
+    for (int e = 1; e <= E; ++e) host[e] = 1;
+    host[E + 1] = 0;  // pairs[0]
+    int32_t *offsets = (int32_t *)(ws + P.off_gpart);
+    RVQ_CUDA(cudaMemcpyAsync(offsets, host, sizeof(int32_t) * (E + 2), cudaMemcpyHostToDevice, st));
+    void *x = ws + P.off_ypair;
+    RVQ_CUDA(cudaMemsetAsync(x, 0, (size_t)bank->d * 2, st));
+    const RecordLayout L = record_layout(bank->d, bank->f);
+    PfJob g = {};
+    g.base = bank->base;
+    g.record_bytes = bank->record_bytes;
+    g.codes_off[0] = L.gate_off;
+    g.codes_off[1] = L.up_off;
+    g.cb_off[0] = L.cb_off;
+    g.cb_off[1] = L.cb_off + RVQ_CODEBOOK_BYTES;
+    g.tile_rows = 128;
+    g.mode = PF_MODE_SWIGLU;
+    g.rows = bank->f;
+    g.cols = bank->d;
+    g.E = E;
+    g.n_pairs = 1;
+    g.min_tokens = 1;
+    g.offsets = offsets;
+    g.pairs = offsets + E + 1;
+    g.x = x;
+    g.x_dtype = RVQ_BF16;
+    g.x_stride = bank->d;
+    g.x_div = 1;
+    g.out = ws + P.off_h16;
+    g.status = (uint32_t *)ws_dev;
+    g.layer = bank->layer;
+    g.d = bank->d;
+    g.f = bank->f;
+    g.selftest_stall = 1;
+    // the host array must outlive the copy
+    RVQ_CUDA(cudaStreamSynchronize(st));
+    return launch_prefill_gemm(g, st, false);
+}
+
 rvq_status rvq_ws_clear(void *ws_dev, rvq_stream_t stream) {
     CHECK_ARG(ws_dev, "rvq_ws_clear: null workspace");
     RVQ_CUDA(cudaMemsetAsync(ws_dev, 0, RVQ_WS_STATUS_BYTES, (cudaStream_t)stream));

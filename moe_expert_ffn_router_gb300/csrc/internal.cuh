@@ -195,6 +195,7 @@ struct PfJob {
     void *out;                 // gate/up: h bf16 [n_pairs][rows]; down: y fp32 [n_pairs][rows]
     uint32_t *status;
     int32_t layer, d, f;       // record header check
+    int32_t selftest_stall;    // 1: the MMA role first waits for an arrival nothing makes
 };
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
 

@@ -69,7 +69,8 @@ constexpr int BAR_ACC_FULL = 2 * PF_NST;
 constexpr int BAR_ACC_EMPTY = 2 * PF_NST + 1;
 constexpr int BAR_DONE = 2 * PF_NST + 2;
 constexpr int BAR_CB = 2 * PF_NST + 3;           // A producers: codebook swap rendezvous
-constexpr int kNumBars = 2 * PF_NST + 4;
+constexpr int BAR_NEVER = 2 * PF_NST + 4;        // self-test: a phase nothing completes
+constexpr int kNumBars = 2 * PF_NST + 5;
 constexpr int OFF_TMEM = OFF_BAR + 8 * kNumBars;
 constexpr int OFF_FLAG = OFF_TMEM + 4;
 constexpr int OFF_Q = OFF_BAR + 128;             // pass prefix [E + 1]
@@ -326,6 +327,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
             mbar_init(bar(BAR_ACC_EMPTY), 4);
             mbar_init(bar(BAR_DONE), 1);
             mbar_init(bar(BAR_CB), kDecoders / 32);
+            mbar_init(bar(BAR_NEVER), 1);
             *abort_flag = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
@@ -344,7 +346,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
         // ================= MMA issuer =================
         if (lane == 0) {
             uint32_t st = 0, ph = 0, nacc = 0;
-            for (int it = it0; it < it1; ++it) {
+            // self-test of the failure path: wait for an arrival nothing makes,
+            // so the bounded wait expires and every role gives up
+            if (job.selftest_stall) mbar_wait(bar(BAR_NEVER), 0, abort_flag, job.status);
+            for (int it = it0; it < it1 && !*abort_flag; ++it) {
                 const PfItem I = pf_item(job, Q, MT, it);
                 if (!I.valid) continue;
                 if (!mbar_wait(bar(BAR_ACC_EMPTY), (nacc & 1u) ^ 1u, abort_flag, job.status)) break;

@@ -180,3 +180,23 @@ def test_combine_reduced_outputs_many_tokens():
         rvq.moe_combine(torch.from_numpy(y).to(DEV), torch.from_numpy(w).to(DEV), n, k, d, r, out)
         torch.cuda.synchronize()
         assert_rms_close(out.cpu().numpy(), ref, 1e-5, "combine")
+
+
+def test_stalled_pipeline_times_out_and_recovers():
+    """Failure path of the tensor-core kernel without any fault: its MMA role
+    waits for an arrival nothing makes; within a few seconds the kernel gives
+    up, reports RVQ_DEV_ERR_TIMEOUT, frees its tensor memory, and the same
+    bank and context then compute a correct layer."""
+    import time
+    sl, L, _ = layer(1)
+    ws = L.workspace(1)
+    t0 = time.time()
+    rvq.rvq_selftest_prefill_timeout(L.bank, ws)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert dt < 20.0, dt
+    rc, bits = rvq.rvq_ws_status(ws)
+    assert rc == 6 and bits & rvq.DEV_ERR_TIMEOUT, (rc, bits)   # RVQ_ETIMEOUT
+    assert rvq.rvq_ws_status(ws) == (0, 0)                      # the read cleared it
+    # the context is healthy: a full tensor-core layer is still correct
+    test_tensor_core_path_all_experts_d2048()
