@@ -511,8 +511,7 @@ static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dt
     g.codes_off[1] = L.up_off;
     g.cb_off[0] = L.cb_off;
     g.cb_off[1] = L.cb_off + RVQ_CODEBOOK_BYTES;
-    g.row_off[0] = g.row_off[1] = 0;
-    g.tile_rows = 128;
+    g.tile_rows = 64;
     g.mode = PF_MODE_SWIGLU;
     g.rows = bank->f;
     g.cols = bank->d;
@@ -535,9 +534,7 @@ static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dt
     PfJob dn = g;
     dn.codes_off[0] = dn.codes_off[1] = L.down_off;
     dn.cb_off[0] = dn.cb_off[1] = L.cb_off + 2 * RVQ_CODEBOOK_BYTES;
-    dn.row_off[0] = 0;
-    dn.row_off[1] = 128;
-    dn.tile_rows = 256;
+    dn.tile_rows = 128;
     dn.mode = PF_MODE_PLAIN;
     dn.rows = bank->d;
     dn.cols = bank->f;
@@ -731,7 +728,7 @@ rvq_status rvq_selftest_prefill_timeout(const rvq_moe_bank *bank, void *ws_dev, 
     g.codes_off[1] = L.up_off;
     g.cb_off[0] = L.cb_off;
     g.cb_off[1] = L.cb_off + RVQ_CODEBOOK_BYTES;
-    g.tile_rows = 128;
+    g.tile_rows = 64;
     g.mode = PF_MODE_SWIGLU;
     g.rows = bank->f;
     g.cols = bank->d;

@@ -174,15 +174,14 @@ rvq_status launch_pack_codebooks(const float *src, float *dst, int count, cudaSt
 rvq_status launch_write_header(uint8_t *record, const rvq_expert_header &h, cudaStream_t stream);
 
 // ------------------------------------------------- tensor-core (prefill) job
-constexpr int PF_MODE_SWIGLU = 0;  // gate/up: tiles = gate, up rows; out = h bf16
-constexpr int PF_MODE_PLAIN = 1;   // down: tiles = two row blocks; out = y fp32
+constexpr int PF_MODE_SWIGLU = 0;  // gate/up: A rows interleave gate and up; out = h bf16
+constexpr int PF_MODE_PLAIN = 1;   // down: out = y fp32
 struct PfJob {
     const uint8_t *base;       // bank
     uint64_t record_bytes;
-    uint64_t codes_off[2];     // per A tile: gate, up (SWIGLU) or down, down (PLAIN)
+    uint64_t codes_off[2];     // per matrix slot: gate, up (SWIGLU) or down, down (PLAIN)
     uint64_t cb_off[2];
-    int32_t row_off[2];        // row of each A tile within the M tile (0, 0 or 0, 128)
-    int32_t tile_rows;         // rows per M tile: 128 (SWIGLU) or 256 (PLAIN)
+    int32_t tile_rows;         // weight rows per M tile and matrix: 64 (SWIGLU) or 128 (PLAIN)
     int32_t mode;
     int32_t rows, cols;        // of each matrix
     int32_t E, n_pairs;

@@ -1,5 +1,5 @@
-// Prefill path of the expert FFN: RVQ code tiles dequantised to bf16 in
-// shared memory feed tcgen05 tensor-core GEMMs (fp32 accumulators in TMEM).
+// Prefill path of the expert FFN: RVQ code tiles dequantised to bf16 feed
+// tcgen05 tensor-core GEMMs (fp32 accumulators in TMEM).
 //
 // For prefill-sized groups (tens to hundreds of tokens per expert) the FFN is
 // a real dense contraction, so the weights are decoded once per tile --
@@ -7,38 +7,53 @@
 // decode of the pages ("WASTE Inference Engine", section "Residual Vector
 // Quantization (RVQ)") -- rounded to bf16 and multiplied on the tensor cores.
 //
-// GEMM orientation (swap-AB): A = 128 rows of W x 64 K-columns (K-major), B =
-// up to 256 tokens of one expert's group x 64 K-columns (K-major), D = W x^T
-// (128 rows x N tokens, fp32, in TMEM).  One RVQ chunk (8 weights) is exactly
-// one 16-byte unit of the 128-byte swizzle row, so a decoded chunk is stored
-// with one 128-bit shared-memory store at its swizzled position.
+// GEMM orientation (swap-AB): A = 128 weight rows x 64 K (bf16 in tensor
+// memory: row = TMEM lane, two K values per 32-bit column), B = up to 192
+// tokens of one expert's group x 64 K (K-major, 128-byte swizzle, shared
+// memory), D = W x^T (128 rows x N tokens, fp32, TMEM).  The decode warps
+// write their rows of A straight into tensor memory (tcgen05.st), so A costs
+// no shared-memory stores or operand reads, and every MMA reads B once.
 //
-// A work item is (expert, pass of <= 256 tokens, M tile) and carries two A
-// tiles that share the B tile:
-//  * gate/up launch: tile 0 = 128 rows of gate, tile 1 = the same rows of up;
-//    the epilogue computes h = silu(g) * u and writes bf16 h [pair][f].
-//  * down launch: tiles 0 and 1 = rows [256 m, 256 m + 128) and the next 128
-//    rows of down; the epilogue writes fp32 y [pair][d].
+// A work item is (expert, pass of <= 192 tokens, M tile of 128 A rows):
+//  * gate/up launch: the A rows are 64 weight rows of gate and the same 64
+//    rows of up, interleaved in fours (A row r holds weight row
+//    64 m + 4 (r / 8) + r % 4, of gate if r % 8 < 4, of up otherwise), so a
+//    row's gate and up accumulators sit four TMEM lanes apart and the epilogue
+//    pairs them with one shuffle: h = silu(g) * u -> bf16 [pair][f].
+//  * down launch: the A rows are down rows [128 m, 128 m + 128); the epilogue
+//    writes fp32 y [pair][d].
 // Items are split into contiguous ranges over a persistent grid (one CTA per
 // SM), so consecutive items of a CTA mostly share the expert and its codebooks.
 //
 // Warp roles (512 threads):
-//  warp 0      TMEM owner; lane 0 issues the MMAs (8 per K step) and commits
-//  warps 1-3   B producers: cp.async gathers of token rows into the B stage
+//  warp 0      TMEM owner; lane 0 issues the MMAs (4 per K step) and commits
+//  warps 1-2   B producers: cp.async gathers of token rows into the B slot
+//              (fp32 inputs: converted to bf16 and stored)
+//  warp 3      B relay (lane 0): once a slot's rows have landed, fences them
+//              into the async proxy and signals the K step (the fence costs
+//              the MMA thread nothing)
 //  warps 4-7   epilogue: TMEM -> registers -> global (lane quarter = warp % 4)
-//  warps 8-15  A producers: decode code bytes into the two bf16 A tiles
-// The stages (A0, A1, B) form a two-deep ring guarded by full/empty mbarriers;
-// the accumulators (512 TMEM columns: tile 0 at 0, tile 1 at 256) by acc_full
-// and acc_empty.
+//  warps 8-15  A producers: decode code bytes into TMEM (lane quarter =
+//              warp % 4); warps 8-11 take the even K steps, 12-15 the odd ones
+// K step t of the CTA's sequence uses A stage t % 4 (TMEM columns
+// 384 + 32 s), B slot t % 5 (shared memory; five slots keep up to 120 KiB of
+// token rows in flight against the L2 latency of the row gathers) and the
+// full/empty mbarrier pair t % 8.  full[t % 8] completes once the four decode
+// warps of the K step and every B producer have arrived, so the MMA thread
+// waits once and commits once per K step: its instruction stream, not the
+// tensor pipe, is the limit at the group sizes of a prefill chunk.  A decode
+// warp reuses a stage after empty[(t - 4) % 8], a B producer a slot after
+// empty[(t - 5) % 8].  Two accumulators (TMEM columns 0 and 192, guarded by
+// acc_full / acc_empty) let the epilogue of one item overlap the main loop of
+// the next.
 //
 // Decoding is bound by shared-memory gathers of codewords, so the codebooks
 // sit in shared memory as fp16 (summed in fp16, then rounded once to bf16) in
 // a bank-private layout: line (stage s, codeword k) is 128 bytes, and 16-byte
-// group q of every line serves lane q of each quarter-warp.  Groups 0-3 hold
-// tile 0's codebook, groups 4-7 tile 1's.  A quarter-warp thus reads eight
-// codewords from eight distinct bank groups whatever the codes are, and the
-// eight rows it decodes have distinct (row mod 8), so its swizzled stores are
-// conflict-free as well.
+// group q of every line serves lane q of each quarter-warp.  For gate/up,
+// groups 0-3 hold gate's codebook and 4-7 up's (lanes with r % 8 < 4 decode
+// gate rows); for down all eight hold down's.  A quarter-warp thus reads
+// eight codewords from eight distinct bank groups whatever the codes are.
 //
 // Every wait is bounded (1 s); on expiry the CTA records RVQ_DEV_ERR_TIMEOUT,
 // every role leaves its loop, the MMAs in flight are drained and TMEM is freed.
@@ -51,37 +66,48 @@ namespace rvq {
 namespace {
 
 constexpr int PF_THREADS = 512;
-constexpr int PF_NMAX = 256;                     // tokens per pass (MMA N)
+constexpr int PF_NMAX = 192;                     // tokens per pass (MMA N)
 constexpr int PF_KC = 64;                        // K columns per stage (one 128-byte swizzle row)
-constexpr int PF_NST = 2;                        // ring depth
-constexpr int kTileA = 128 * PF_KC * 2;          // 16 KiB
-constexpr int kTileB = PF_NMAX * PF_KC * 2;      // 32 KiB
-constexpr int kStage = 2 * kTileA + kTileB;      // 64 KiB
+constexpr int PF_NST = 4;                        // A stages (TMEM)
+constexpr int PF_NSLOT = 5;                      // B slots (shared memory)
+constexpr int PF_NBAR = 8;                       // full/empty barrier pairs (K steps in flight)
+constexpr int PF_MROWS = 128;                    // A rows per item (MMA M)
+constexpr int kSlotB = PF_NMAX * PF_KC * 2;      // 24 KiB of B per slot
 constexpr int kCbLine = 128;                     // one (stage, codeword) line
 constexpr int kCbBytes = 3 * 256 * kCbLine;      // 96 KiB
 constexpr int OFF_CB = 0;
 constexpr int OFF_ST = kCbBytes;
-constexpr int OFF_BAR = OFF_ST + PF_NST * kStage;
+constexpr int OFF_BAR = OFF_ST + PF_NSLOT * kSlotB;
 // mbarriers, 8 bytes each from OFF_BAR
-constexpr int BAR_FULL = 0;                      // [PF_NST]
-constexpr int BAR_EMPTY = PF_NST;                // [PF_NST]
-constexpr int BAR_ACC_FULL = 2 * PF_NST;
-constexpr int BAR_ACC_EMPTY = 2 * PF_NST + 1;
-constexpr int BAR_DONE = 2 * PF_NST + 2;
-constexpr int BAR_CB = 2 * PF_NST + 3;           // A producers: codebook swap rendezvous
-constexpr int BAR_NEVER = 2 * PF_NST + 4;        // self-test: a phase nothing completes
-constexpr int kNumBars = 2 * PF_NST + 5;
+constexpr int BAR_FULL = 0;                      // [PF_NBAR]
+constexpr int BAR_EMPTY = BAR_FULL + PF_NBAR;    // [PF_NBAR]
+constexpr int BAR_LANDED = BAR_EMPTY + PF_NBAR;  // [PF_NBAR] B rows of the K step in shared memory
+constexpr int BAR_ACC_FULL = BAR_LANDED + PF_NBAR;    // [2]
+constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;       // [2]
+constexpr int BAR_DONE = BAR_ACC_EMPTY + 2;
+constexpr int BAR_CB = BAR_DONE + 1;             // A producers: codebook swap rendezvous
+constexpr int BAR_NEVER = BAR_CB + 1;            // self-test: a phase nothing completes
+constexpr int kNumBars = BAR_NEVER + 1;
 constexpr int OFF_TMEM = OFF_BAR + 8 * kNumBars;
 constexpr int OFF_FLAG = OFF_TMEM + 4;
-constexpr int OFF_Q = OFF_BAR + 128;             // pass prefix [E + 1]
+constexpr int OFF_Q = OFF_BAR + 256;             // pass prefix [E + 1]
 constexpr int kMaxE = 256;
-constexpr int kPfSmem = OFF_Q + 4 * (kMaxE + 1) + 1024;  // + slack to align the base to 1 KiB
+constexpr int OFF_W = OFF_Q + 4 * (kMaxE + 2);   // cost prefix [E + 1] (int64)
+constexpr int kPfSmem = OFF_W + 8 * (kMaxE + 1) + 1024;  // + slack to align the base to 1 KiB
 static_assert(OFF_FLAG + 4 <= OFF_Q, "control block overlaps the pass prefix");
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemD = 0;                   // accumulator b: columns [PF_NMAX b, + PF_NMAX)
+constexpr uint32_t kTmemA = 2 * PF_NMAX;         // A stage s: columns [kTmemA + 32 s, + 32)
+static_assert(kTmemA + PF_NST * (PF_KC / 2) <= kTmemCols, "TMEM columns");
+static_assert(PF_NBAR >= PF_NSLOT + 1 && PF_NBAR >= PF_NST + 1, "a barrier pair outlives its stage");
+static_assert(kSlotB % 1024 == 0 && OFF_ST % 1024 == 0, "swizzled slots start on 1 KiB");
 
-constexpr int kLoaders = 96;                     // B producer threads (warps 1-3)
-constexpr int kDecoders = 256;                   // A producer threads (warps 8-15)
-constexpr uint32_t kFullCount = kLoaders + kDecoders / 32;
+constexpr int kLoaders = 64;                     // B producer threads (warps 1-2)
+constexpr int kLoaderRows = 3;                   // token rows per producer thread (192 / 64)
+constexpr int kDecodeWarps = 8;                  // A producer warps (8-15)
+// full[] arrivals: one half's decode warps + the B relay
+constexpr uint32_t kFullCount = kDecodeWarps / 2 + 1;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: a bounded wait, never a hang
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -106,12 +132,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D (TMEM) (+)= A (TMEM, 128 lanes x 16 K) x B (shared memory descriptor).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
@@ -158,6 +185,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volati
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try(mbar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            set_dev_error(status, RVQ_DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// The MMA thread's wait: polls without a suspend hint (its waits are short
+// and on its critical path), same bound and abort protocol as mbar_wait.
+__device__ __forceinline__ bool mbar_try_now(uint32_t mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.b32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t mbar, uint32_t parity,
+                                               volatile int *abort_flag, uint32_t *status) {
+    if (mbar_try_now(mbar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try_now(mbar, parity)) return true;
         if (*abort_flag) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -218,13 +273,13 @@ __device__ __forceinline__ void derotate(uint32_t (&w)[8], int l) {
     for (int i = 0; i < 8; ++i) w[i] = __funnelshift_l(a[(i + 7) & 7], a[i], bl);
 }
 
-// 128-bit shared store issued as volatile asm without a memory clobber: the
-// compiler keeps it in order with the fences and barrier arrivals (also
-// volatile asm) but may schedule the codebook loads of later chunks ahead of
-// it -- the A tiles and the codebooks never overlap.
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w));
+// Eight 32-bit columns of this warp's 32 TMEM lanes (one register per column).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
 }
 
 // 128-bit shared load through a 32-bit shared address (no generic address
@@ -246,6 +301,51 @@ struct PfItem {
     int e, o, j0, n, npad, mt;
     bool valid;
 };
+
+// Cost of one item in token-row units: a K step takes about max(decode
+// floor, fixed + B rows) cycles (measured: ~770 cycles with no B rows, ~7 per
+// row above that, so a floor of 112 and a fixed part of 32 rows).  CTAs get
+// contiguous item ranges of equal total cost: item costs differ by 2x or more
+// across a Zipf-skewed chunk, and equal item counts left the slowest CTA 1.5x
+// behind the median.
+constexpr int64_t kCostFloor = 112, kCostFixed = 32;
+__device__ __forceinline__ int64_t pf_cost(int npad) {
+    return max(kCostFloor, kCostFixed + (int64_t)npad);
+}
+
+// Passes of expert e (0 when its group is below min_tokens) and their cost.
+__device__ __forceinline__ void pf_expert_cost(const PfJob &job, int ne, int MT, int &passes,
+                                               int64_t &cost) {
+    passes = ne >= job.min_tokens && ne > 0 ? (ne + PF_NMAX - 1) / PF_NMAX : 0;
+    cost = 0;
+    if (passes > 0) {
+        const int last = ne - (passes - 1) * PF_NMAX;
+        cost = (int64_t)MT * ((passes - 1) * pf_cost(PF_NMAX) + pf_cost((last + 15) & ~15));
+    }
+}
+
+// First item whose cumulative cost start is >= t (W[e] = cost before expert e).
+__device__ int pf_first_item(const PfJob &job, const int32_t *Q, const int64_t *W, int MT,
+                             int64_t t) {
+    const int E = job.E;
+    if (t >= W[E]) return Q[E] * MT;
+    int lo = 0, hi = E;  // largest e with W[e] <= t: W[e + 1] > t, so e has work
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (W[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int ne = job.offsets[lo + 1] - job.offsets[lo];
+    const int P = (ne + PF_NMAX - 1) / PF_NMAX;
+    const int64_t cf = pf_cost(PF_NMAX);
+    const int64_t cl = pf_cost((ne - (P - 1) * PF_NMAX + 15) & ~15);
+    int64_t rem = t - W[lo];
+    const int64_t pq = rem / ((int64_t)MT * cf);
+    const int pi = (int)(pq < (int64_t)P - 1 ? pq : (int64_t)P - 1);
+    rem -= (int64_t)pi * MT * cf;
+    const int64_t c = pi < P - 1 ? cf : cl;
+    // mt may equal MT: the first item of the next pass
+    return (Q[lo] + pi) * MT + (int)((rem + c - 1) / c);
+}
 
 // Work item `it` -> (expert, pass, M tile).  Q[e] = passes before expert e.
 __device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, int MT, int it) {
@@ -272,7 +372,7 @@ __device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, in
 
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob job) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // the 128-byte swizzle is a function of shared-address bits 4..9: tiles
+    // the 128-byte swizzle is a function of shared-address bits 4..9: B stages
     // must start on 1024-byte boundaries of the shared window
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
@@ -280,53 +380,78 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
     int32_t *Q = reinterpret_cast<int32_t *>(smem + OFF_Q);
+    int64_t *W = reinterpret_cast<int64_t *>(smem + OFF_W);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool swiglu = job.mode == PF_MODE_SWIGLU;
     const int MT = job.rows / job.tile_rows;
-    const int KS = job.cols / PF_KC;
+    const int KS = job.cols / PF_KC;             // a multiple of 4: K step t uses stage t % 4
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- setup: pass prefix (warp 1), barriers + TMEM (warp 0) ----------
     if (warp == 1) {
+        // pass prefix Q and cost prefix W over the experts (lane: a run of them)
         const int E = job.E;
         const int per = (E + 31) / 32;
         const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
         int cnt = 0;
+        int64_t cst = 0;
         bool ok = true;
         for (int e = e0; e < e1; ++e) {
             const int ne = job.offsets[e + 1] - job.offsets[e];
             ok = ok && ne >= 0;
-            cnt += (ne >= job.min_tokens) ? (ne + PF_NMAX - 1) / PF_NMAX : 0;
+            int P;
+            int64_t c;
+            pf_expert_cost(job, ne, MT, P, c);
+            cnt += P;
+            cst += c;
         }
         int incl = cnt;
+        int64_t cincl = cst;
 #pragma unroll
         for (int s = 1; s < 32; s <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, incl, s);
-            if (lane >= s) incl += v;
+            const int64_t cv = __shfl_up_sync(0xffffffffu, cincl, s);
+            if (lane >= s) {
+                incl += v;
+                cincl += cv;
+            }
         }
         int pre = incl - cnt;
+        int64_t cpre = cincl - cst;
         for (int e = e0; e < e1; ++e) {
             Q[e] = pre;
+            W[e] = cpre;
             const int ne = job.offsets[e + 1] - job.offsets[e];
-            pre += (ne >= job.min_tokens) ? (ne + PF_NMAX - 1) / PF_NMAX : 0;
+            int P;
+            int64_t c;
+            pf_expert_cost(job, ne, MT, P, c);
+            pre += P;
+            cpre += c;
         }
         ok = __all_sync(0xffffffffu, ok) && job.offsets[0] == 0 && job.offsets[E] == job.n_pairs;
-        if (lane == 31) Q[E] = ok ? incl : 0;
+        if (lane == 31) {
+            Q[E] = ok ? incl : 0;
+            W[E] = ok ? cincl : 0;
+        }
         if (!ok && lane == 0) set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
     } else if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          sbase + OFF_TMEM),
-                     "r"(512));
+                     "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
         if (lane == 0) {
-            for (int s = 0; s < PF_NST; ++s) {
+            for (int s = 0; s < PF_NBAR; ++s) {
                 mbar_init(bar(BAR_FULL + s), kFullCount);
                 mbar_init(bar(BAR_EMPTY + s), 1);
+                mbar_init(bar(BAR_LANDED + s), kLoaders);
             }
-            mbar_init(bar(BAR_ACC_FULL), 1);
-            mbar_init(bar(BAR_ACC_EMPTY), 4);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(bar(BAR_ACC_FULL + b), 1);
+                mbar_init(bar(BAR_ACC_EMPTY + b), 4);
+            }
             mbar_init(bar(BAR_DONE), 1);
-            mbar_init(bar(BAR_CB), kDecoders / 32);
+            mbar_init(bar(BAR_CB), kDecodeWarps);
             mbar_init(bar(BAR_NEVER), 1);
             *abort_flag = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -338,50 +463,49 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
     asm volatile("griddepcontrol.launch_dependents;");
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM);
 
-    const int total = Q[job.E] * MT;
-    const int it0 = (int)((int64_t)blockIdx.x * total / gridDim.x);
-    const int it1 = (int)((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+    // this CTA's items: an equal share of the total cost
+    const int64_t T = W[job.E];
+    const int it0 = pf_first_item(job, Q, W, MT, (int64_t)blockIdx.x * T / gridDim.x);
+    const int it1 = pf_first_item(job, Q, W, MT, (int64_t)(blockIdx.x + 1) * T / gridDim.x);
 
     if (warp == 0) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            uint32_t st = 0, ph = 0, nacc = 0;
+            uint32_t kg = 0, slot = 0, nacc = 0;  // K steps, B slot, items consumed
+            const uint64_t bdesc0 = smem_desc(sbase + OFF_ST);
             // self-test of the failure path: wait for an arrival nothing makes,
             // so the bounded wait expires and every role gives up
             if (job.selftest_stall) mbar_wait(bar(BAR_NEVER), 0, abort_flag, job.status);
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
                 const PfItem I = pf_item(job, Q, MT, it);
                 if (!I.valid) continue;
-                if (!mbar_wait(bar(BAR_ACC_EMPTY), (nacc & 1u) ^ 1u, abort_flag, job.status)) break;
+                const uint32_t ab = nacc & 1u, use = nacc >> 1;
+                if (!mbar_wait(bar(BAR_ACC_EMPTY + ab), (use & 1u) ^ 1u, abort_flag, job.status))
+                    break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t idesc = idesc_bf16(128, I.npad);
+                const uint32_t idesc = idesc_bf16(PF_MROWS, I.npad);
+                const uint32_t td = tmem + kTmemD + ab * PF_NMAX;
                 bool ok = true;
-                for (int ks = 0; ks < KS; ++ks) {
-                    if (!mbar_wait(bar(BAR_FULL + st), ph, abort_flag, job.status)) {
+                for (int ks = 0; ks < KS; ++ks, ++kg) {
+                    if (!mbar_wait_spin(bar(BAR_FULL + (kg & (PF_NBAR - 1))),
+                                        (kg / PF_NBAR) & 1u, abort_flag, job.status)) {
                         ok = false;
                         break;
                     }
-                    // the B stage was written through the generic proxy (cp.async)
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    // (the B producers fenced their slot writes into the async proxy)
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t sa = sbase + OFF_ST + st * kStage;
+                    const uint32_t ta = tmem + kTmemA + (kg & (PF_NST - 1)) * (PF_KC / 2);
+                    // start-address field: +1 per 16 bytes (32 bytes per 16 K)
+                    const uint64_t bd = bdesc0 + slot * (uint32_t)(kSlotB >> 4);
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            mma_bf16(tmem + t * 256, smem_desc(sa + t * kTileA + kk * 32),
-                                     smem_desc(sa + 2 * kTileA + kk * 32), idesc,
-                                     (ks > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(bar(BAR_EMPTY + st));
-                    if (++st == PF_NST) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ts(td, ta + kk * 8, bd + 2 * kk, idesc,
+                                    (ks > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(BAR_EMPTY + (kg & (PF_NBAR - 1))));
+                    slot = slot == PF_NSLOT - 1 ? 0 : slot + 1;
                 }
                 if (!ok) break;
-                mma_commit(bar(BAR_ACC_FULL));
+                mma_commit(bar(BAR_ACC_FULL + ab));
                 ++nacc;
             }
             // drain: every MMA issued has completed before TMEM is released
@@ -391,132 +515,172 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
         }
         __syncwarp();
     } else if (warp < 4) {
-        // ================= B producers =================
-        const int lt = tid - 32;
-        const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
-        uint32_t st = 0, ph = 0;
-        for (int it = it0; it < it1 && !*abort_flag; ++it) {
-            const PfItem I = pf_item(job, Q, MT, it);
-            if (!I.valid) continue;
-            const uint8_t *src[3];
+        // ================= B producers and relay =================
+        uint32_t kg = 0, slot = 0;
+        if (warp < 3) {
+            const int lt = tid - 32;
+            const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
+            for (int it = it0; it < it1 && !*abort_flag; ++it) {
+                const PfItem I = pf_item(job, Q, MT, it);
+                if (!I.valid) continue;
+                const uint8_t *src[kLoaderRows];
 #pragma unroll
-            for (int r = 0; r < 3; ++r) {
-                const int j = lt + kLoaders * r;
-                src[r] = nullptr;
-                if (j < I.n) {
-                    const int p = job.pairs[I.o + I.j0 + j];
-                    if (p >= 0 && p < job.n_pairs)
-                        src[r] = reinterpret_cast<const uint8_t *>(job.x) +
-                                 ((int64_t)(p / job.x_div) * job.x_stride) * esz;
-                    else
-                        set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+                for (int r = 0; r < kLoaderRows; ++r) {
+                    const int j = lt + kLoaders * r;
+                    src[r] = nullptr;
+                    if (j < I.n) {
+                        const int p = job.pairs[I.o + I.j0 + j];
+                        if (p >= 0 && p < job.n_pairs)
+                            src[r] = reinterpret_cast<const uint8_t *>(job.x) +
+                                     ((int64_t)(p / job.x_div) * job.x_stride) * esz;
+                        else
+                            set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+                    }
                 }
-            }
-            bool ok = true;
-            for (int ks = 0; ks < KS; ++ks) {
-                if (!mbar_wait(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, job.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t sb = sbase + OFF_ST + st * kStage + 2 * kTileA;
-                const uint32_t full = bar(BAR_FULL + st);
-                if (esz == 2) {
-#pragma unroll
-                    for (int r = 0; r < 3; ++r) {
-                        const int j = lt + kLoaders * r;
-                        if (src[r] != nullptr) {
-                            const uint8_t *s = src[r] + ks * PF_KC * 2;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                cp_async16(sb + j * 128 + ((c ^ (j & 7)) << 4), s + c * 16);
+                bool ok = true;
+                for (int ks = 0; ks < KS; ++ks, ++kg) {
+                    // the slot's previous K step (5 back) has been consumed
+                    if (kg >= (uint32_t)PF_NSLOT) {
+                        const uint32_t kp = kg - PF_NSLOT;
+                        if (!mbar_wait(bar(BAR_EMPTY + (kp & (PF_NBAR - 1))), (kp / PF_NBAR) & 1u,
+                                       abort_flag, job.status)) {
+                            ok = false;
+                            break;
                         }
                     }
-                    // arrives once this thread's copies have landed
-                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full)
-                                 : "memory");
-                } else {
-                    uint8_t *bt = smem + OFF_ST + st * kStage + 2 * kTileA;
+                    const uint32_t sb = sbase + OFF_ST + slot * kSlotB;
+                    const uint32_t landed = bar(BAR_LANDED + (kg & (PF_NBAR - 1)));
+                    if (esz == 2) {
 #pragma unroll
-                    for (int r = 0; r < 3; ++r) {
-                        const int j = lt + kLoaders * r;
-                        if (src[r] != nullptr) {
-                            const float4 *s =
-                                reinterpret_cast<const float4 *>(src[r] + ks * PF_KC * 4);
-                            for (int c = 0; c < 8; ++c) {
-                                const float4 f0 = s[2 * c], f1 = s[2 * c + 1];
-                                *reinterpret_cast<uint4 *>(bt + j * 128 + ((c ^ (j & 7)) << 4)) =
-                                    make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f0.z, f0.w),
-                                               pack_bf16x2(f1.x, f1.y), pack_bf16x2(f1.z, f1.w));
+                        for (int r = 0; r < kLoaderRows; ++r) {
+                            const int j = lt + kLoaders * r;
+                            if (src[r] != nullptr) {
+                                const uint8_t *s = src[r] + ks * PF_KC * 2;
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    cp_async16(sb + j * 128 + ((c ^ (j & 7)) << 4), s + c * 16);
                             }
                         }
+                        // arrives once this thread's copies have landed
+                        asm volatile(
+                            "cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(landed)
+                            : "memory");
+                    } else {
+                        uint8_t *bt = smem + OFF_ST + slot * kSlotB;
+#pragma unroll
+                        for (int r = 0; r < kLoaderRows; ++r) {
+                            const int j = lt + kLoaders * r;
+                            if (src[r] != nullptr) {
+                                const float4 *s =
+                                    reinterpret_cast<const float4 *>(src[r] + ks * PF_KC * 4);
+                                for (int c = 0; c < 8; ++c) {
+                                    const float4 f0 = s[2 * c], f1 = s[2 * c + 1];
+                                    *reinterpret_cast<uint4 *>(bt + j * 128 +
+                                                               ((c ^ (j & 7)) << 4)) =
+                                        make_uint4(pack_bf16x2(f0.x, f0.y),
+                                                   pack_bf16x2(f0.z, f0.w),
+                                                   pack_bf16x2(f1.x, f1.y),
+                                                   pack_bf16x2(f1.z, f1.w));
+                                }
+                            }
+                        }
+                        mbar_arrive(landed);
+                    }
+                    slot = slot == PF_NSLOT - 1 ? 0 : slot + 1;
+                }
+                if (!ok) break;
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+        } else if (lane == 0) {
+            // relay: every producer's rows of the K step are in shared memory
+            // (their arrivals release them); the fence orders them before the
+            // MMA's async-proxy reads, which acquire through full[]
+            for (int it = it0; it < it1 && !*abort_flag; ++it) {
+                const PfItem I = pf_item(job, Q, MT, it);
+                if (!I.valid) continue;
+                bool ok = true;
+                for (int ks = 0; ks < KS; ++ks, ++kg) {
+                    if (!mbar_wait_spin(bar(BAR_LANDED + (kg & (PF_NBAR - 1))),
+                                        (kg / PF_NBAR) & 1u, abort_flag, job.status)) {
+                        ok = false;
+                        break;
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_arrive(full);
+                    mbar_arrive(bar(BAR_FULL + (kg & (PF_NBAR - 1))));
                 }
-                if (++st == PF_NST) {
-                    st = 0;
-                    ph ^= 1u;
-                }
+                if (!ok) break;
             }
-            if (!ok) break;
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp < 8) {
         // ================= epilogue =================
         const int ew = warp - 4;                 // TMEM lanes 32 ew .. 32 ew + 31
-        const int rit = ew * 32 + lane;          // row within the tile
-        const uint32_t tl = tmem + ((uint32_t)(ew * 32) << 16);
+        const int ar = ew * 32 + lane;           // A row
+        const int q = lane & 7;
+        // weight row of this lane within the M tile (gate/up: gate lanes q < 4)
+        const int rin = swiglu ? (ar >> 3) * 4 + (q & 3) : ar;
+        const uint32_t tl = tmem + ((uint32_t)(ew * 32) << 16) + kTmemD;
         uint32_t nacc = 0;
         for (int it = it0; it < it1; ++it) {
             const PfItem I = pf_item(job, Q, MT, it);
             if (!I.valid) continue;
-            if (!mbar_wait(bar(BAR_ACC_FULL), nacc & 1u, abort_flag, job.status)) break;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int R0 = I.mt * job.tile_rows;
-            for (int c0 = 0; c0 < I.n; c0 += 32) {
-                const int jl = c0 + lane;
-                const int pl = jl < I.n ? job.pairs[I.o + I.j0 + jl] : -1;
-                float a0[32], a1[32];
-                tmem_ld32(tl + c0, a0);
-                tmem_ld32(tl + 256 + c0, a1);
+            // the item's pair ids, one per lane and 32-token chunk, fetched
+            // before the accumulator is ready; -1 marks no token
+            constexpr int kChunks = PF_NMAX / 32;
+            int pl[kChunks];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int p = __shfl_sync(0xffffffffu, pl, q);
-                    if (c0 + q < I.n && p >= 0 && p < job.n_pairs) {
-                        if (job.mode == PF_MODE_SWIGLU) {
-                            const float g = a0[q];
-                            const float hv = g / (1.0f + expf(-g)) * a1[q];
-                            reinterpret_cast<uint16_t *>(job.out)[(size_t)p * job.rows + R0 + rit] =
-                                (uint16_t)bf16_bits(hv);
-                        } else {
-                            float *y = reinterpret_cast<float *>(job.out) + (size_t)p * job.rows + R0;
-                            y[job.row_off[0] + rit] = a0[q];
-                            y[job.row_off[1] + rit] = a1[q];
-                        }
+            for (int c = 0; c < kChunks; ++c) {
+                const int j = 32 * c + lane;
+                int p = j < I.n ? job.pairs[I.o + I.j0 + j] : -1;
+                pl[c] = (p >= 0 && p < job.n_pairs) ? p : -1;
+            }
+            const uint32_t ab = nacc & 1u, use = nacc >> 1;
+            if (!mbar_wait(bar(BAR_ACC_FULL + ab), use & 1u, abort_flag, job.status)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int R = I.mt * job.tile_rows + rin;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+                if (32 * c >= I.n) break;
+                float a[32];
+                tmem_ld32(tl + ab * PF_NMAX + 32 * c, a);
+                if (swiglu) {
+                    uint16_t *hrow = reinterpret_cast<uint16_t *>(job.out) + R;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int p = __shfl_sync(0xffffffffu, pl[c], t);
+                        const float u = __shfl_xor_sync(0xffffffffu, a[t], 4);
+                        const float g = a[t];
+                        const float hv = __fdividef(g * u, 1.0f + __expf(-g));
+                        if (q < 4 && p >= 0) hrow[(size_t)p * job.rows] = (uint16_t)bf16_bits(hv);
+                    }
+                } else {
+                    float *yrow = reinterpret_cast<float *>(job.out) + R;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int p = __shfl_sync(0xffffffffu, pl[c], t);
+                        if (p >= 0) yrow[(size_t)p * job.rows] = a[t];
                     }
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY));
+            if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + ab));
             ++nacc;
         }
     } else {
-        // ================= A producers (decode) =================
+        // ================= A producers (decode into TMEM) =================
         const int dt = tid - 256;
-        const int dw = dt >> 5, qw = lane >> 3, q = lane & 7;
-        const int b8 = dw * 4 + qw;              // quarter-warp 0..31
-        const int r0 = (b8 >> 1) * 8;
-        const int tile = q >> 2;
-        // quarter-warps of type 0 decode tile-0 rows r0..r0+3 and tile-1 rows
-        // r0+4..r0+7, type 1 the other halves: (row mod 8) differs per lane
-        const int rit = (b8 & 1) == 0 ? r0 + q : (tile == 0 ? r0 + 4 + q : r0 + q - 4);
-        const int sw = rit & 7;
+        const int quarter = warp & 3;            // TMEM lanes 32 quarter .. + 31
+        const int half = (warp - 8) >> 2;        // K steps t with t % 2 == half
+        const int ar = quarter * 32 + lane;      // A row
+        const int q = lane & 7;
+        const int mat = swiglu ? (q >> 2) : 0;   // gate / up (down: both slots hold down)
+        const int rin = swiglu ? (ar >> 3) * 4 + (q & 3) : ar;
         const uint32_t cbl = sbase + OFF_CB + q * 16;  // this lane's bank group
+        const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kTmemA;
         const int RB = job.rows / 32;
         const int G = KS / 4;                    // 32-chunk groups along K
         int cur_e = -1;
-        uint32_t st = 0, ph = 0, ncb = 0;
+        uint32_t kg = 0, ncb = 0;
         for (int it = it0; it < it1 && !*abort_flag; ++it) {
             const PfItem I = pf_item(job, Q, MT, it);
             if (!I.valid) continue;
@@ -530,7 +694,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                     ++ncb;
                 }
                 // record fp32 [s][k/2][i][k&1] -> fp16 lines, one 16-byte group per unit
-                for (int u = dt; u < 3 * 256 * 8; u += kDecoders) {
+                for (int u = dt; u < 3 * 256 * 8; u += kDecodeWarps * 32) {
                     const int L = u >> 3, g = u & 7;
                     const int s = L >> 8, k = L & 255;
                     const float *cb = reinterpret_cast<const float *>(rec + job.cb_off[g >> 2]) +
@@ -550,10 +714,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                 ++ncb;
                 cur_e = I.e;
             }
-            const int R = I.mt * job.tile_rows + job.row_off[tile] + rit;
+            const int R = I.mt * job.tile_rows + rin;
             const int l = R & 31;
+            // Chunk j of this row sits at byte (j - l) mod 32 of each stage
+            // plane; rotating by l - 8 half puts chunks 8 half .. 8 half + 7 (K
+            // step 4 g + half) in bytes 0..7 and chunks 8 half + 16 .. + 23 (K
+            // step 4 g + half + 2) in bytes 16..23.
+            const int rot = (l - 8 * half) & 31;
             // this row's code planes of 32-chunk group g: 6 x 16 bytes (stage s, half h)
-            const uint8_t *cp = rec + job.codes_off[tile] + (size_t)(R >> 5) * kTileBytes + l * 16;
+            const uint8_t *cp = rec + job.codes_off[mat] + (size_t)(R >> 5) * kTileBytes + l * 16;
             uint4 nxt[6];
 #pragma unroll
             for (int v = 0; v < 6; ++v) nxt[v] = *reinterpret_cast<const uint4 *>(cp + v * 512);
@@ -571,6 +740,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                     U[s][6] = nxt[2 * s + 1].z;
                     U[s][7] = nxt[2 * s + 1].w;
                 }
+#pragma unroll
+                for (int s = 0; s < 3; ++s) derotate(U[s], rot);
+                // the next group's planes load while this one decodes
                 if (g + 1 < G) {
                     const uint8_t *cpn = cp + (size_t)(g + 1) * RB * kTileBytes;
 #pragma unroll
@@ -578,40 +750,47 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                         nxt[v] = *reinterpret_cast<const uint4 *>(cpn + v * 512);
                 }
 #pragma unroll
-                for (int s = 0; s < 3; ++s) derotate(U[s], l);
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    if (!mbar_wait(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, job.status)) {
-                        ok = false;
-                        break;
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t kt = kg + 4 * g + 2 * j + half;  // this K step
+                    const uint32_t st = kt & (PF_NST - 1);
+                    // the stage's previous K step (4 back) has been consumed
+                    if (kt >= (uint32_t)PF_NST) {
+                        const uint32_t kp = kt - PF_NST;
+                        if (!mbar_wait(bar(BAR_EMPTY + (kp & (PF_NBAR - 1))),
+                                       (kp / PF_NBAR) & 1u, abort_flag, job.status)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    const uint32_t A = sbase + OFF_ST + st * kStage + tile * kTileA + rit * 128;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int cg = k4 * 8 + c;
-                        const uint32_t k0 = (U[0][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
-                        const uint32_t k1 = (U[1][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
-                        const uint32_t k2 = (U[2][cg >> 2] >> (8 * (cg & 3))) & 0xFFu;
-                        const uint4 w0 = lds128(cbl + k0 * kCbLine);
-                        const uint4 w1 = lds128(cbl + (256 + k1) * kCbLine);
-                        const uint4 w2 = lds128(cbl + (512 + k2) * kCbLine);
-                        uint4 o;
-                        o.x = sum3_bf16x2(w0.x, w1.x, w2.x);
-                        o.y = sum3_bf16x2(w0.y, w1.y, w2.y);
-                        o.z = sum3_bf16x2(w0.z, w1.z, w2.z);
-                        o.w = sum3_bf16x2(w0.w, w1.w, w2.w);
-                        sts128(A + ((c ^ sw) << 4), o);
+                    for (int hq = 0; hq < 4; ++hq) {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            // chunk 2 hq + c of the K step: word 4 j + hq / 2, byte 2 (hq % 2) + c
+                            const int w = 4 * j + (hq >> 1), b = 8 * (2 * (hq & 1) + c);
+                            const uint32_t k0 = (U[0][w] >> b) & 0xFFu;
+                            const uint32_t k1 = (U[1][w] >> b) & 0xFFu;
+                            const uint32_t k2 = (U[2][w] >> b) & 0xFFu;
+                            const uint4 w0 = lds128(cbl + k0 * kCbLine);
+                            const uint4 w1 = lds128(cbl + (256 + k1) * kCbLine);
+                            const uint4 w2 = lds128(cbl + (512 + k2) * kCbLine);
+                            o[4 * c + 0] = sum3_bf16x2(w0.x, w1.x, w2.x);
+                            o[4 * c + 1] = sum3_bf16x2(w0.y, w1.y, w2.y);
+                            o[4 * c + 2] = sum3_bf16x2(w0.z, w1.z, w2.z);
+                            o[4 * c + 3] = sum3_bf16x2(w0.w, w1.w, w2.w);
+                        }
+                        tmem_st8(ta + st * (PF_KC / 2) + 8 * hq, o);
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(BAR_FULL + st));
-                    if (++st == PF_NST) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
+                    if (lane == 0) mbar_arrive(bar(BAR_FULL + (kt & (PF_NBAR - 1))));
                 }
             }
             if (!ok) break;
+            kg += KS;
         }
     }
 
@@ -619,7 +798,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
     __syncthreads();
     if (warp == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
     }
 }
 
@@ -634,9 +814,11 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem));
         attr_done[dev] = 1;
     }
-    if ((job.tile_rows != 128 && job.tile_rows != 256) || job.rows % job.tile_rows ||
-        job.cols % (4 * PF_KC) || job.E < 1 || job.E > kMaxE || job.min_tokens < 1 ||
-        (job.mode != PF_MODE_SWIGLU && job.mode != PF_MODE_PLAIN)) {
+    // gate/up items cover 64 weight rows of each matrix, down items 128 rows
+    const int want_rows = job.mode == PF_MODE_SWIGLU ? PF_MROWS / 2 : PF_MROWS;
+    if ((job.mode != PF_MODE_SWIGLU && job.mode != PF_MODE_PLAIN) || job.tile_rows != want_rows ||
+        job.rows % job.tile_rows || job.cols % (4 * PF_KC) || job.E < 1 || job.E > kMaxE ||
+        job.min_tokens < 1) {
         set_error("prefill: rows %d / cols %d / tile %d / E %d not supported", job.rows, job.cols,
                   job.tile_rows, job.E);
         return RVQ_EINVAL;
