@@ -224,8 +224,15 @@ def run_gpu(args, rank, world, local_rank):
     code_bytes_per_expert = 3 * (3 * s.d * s.f // 8)
     cb_bytes_per_expert = 3 * rvq.RVQ_CODEBOOK_BYTES
 
+    def forward(x, events=None):
+        # one layer: the layer itself (router -> top-k -> FFN -> combine +
+        # residual); a stack: pre-norm + layer, per layer
+        if n_layers == 1:
+            return [L.forward(x, bufs, events=events, tc_min_tokens=tc_min)]
+        return stack.forward(x, events=events, tc_min_tokens=tc_min)
+
     def step(i, events=None):
-        return stack.forward(xs[i % nsteps], events=events, tc_min_tokens=tc_min)
+        return forward(xs[i % nsteps], events=events)
 
     # unique experts per step, summed over the layers (from the routing the
     # GPU computed); the pool is replayed identically in the timed loop, so
@@ -331,14 +338,14 @@ def run_gpu(args, rank, world, local_rank):
     out_last = stack.buffers(batch)[-1]["out"]
     for i in range(args.warmup):
         xbuf.view(torch.int16).copy_(pinned_in[i % nsteps], non_blocking=True)
-        stack.forward(xbuf, tc_min_tokens=tc_min)
+        forward(xbuf)
         pinned_out.copy_(out_last, non_blocking=True)
     barrier()
     e0.record()
     for i in range(args.steps):
         j = (args.warmup + i) % nsteps
         xbuf.view(torch.int16).copy_(pinned_in[j], non_blocking=True)
-        stack.forward(xbuf, tc_min_tokens=tc_min)
+        forward(xbuf)
         pinned_out.copy_(out_last, non_blocking=True)
     e1.record()
     barrier()
@@ -357,8 +364,9 @@ def run_gpu(args, rank, world, local_rank):
     res = dict(value=value, ms=ms, code_gbs=code_gbs, tok_s=tok_s, roofline=roofline, e2e=e2e,
                clocks=clocks, kernels_us={k: round(v * 1e3, 2) for k, v in avg.items()},
                uniq_mean=float(np.mean([uniq[j] for j in steps_idx])),
-               launches=(TC_LAUNCHES_PER_STEP if tc_min == 1 else len(KERNELS) if tc_min == 0
-                         else len(KERNELS) + TC_LAUNCHES_PER_STEP - 3) * args.steps * n_layers,
+               launches=((TC_LAUNCHES_PER_STEP if tc_min == 1 else len(KERNELS) if tc_min == 0
+                          else len(KERNELS) + TC_LAUNCHES_PER_STEP - 3)
+                         + (1 if n_layers > 1 else 0)) * args.steps * n_layers,
                config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
     del L, stack, built
     return res

@@ -103,7 +103,7 @@ def test_mixed_dispatch_by_group_size():
 
 def test_prefill_chunk_full_size_zipf():
     """2048 tokens of the K3-shaped layer with the Zipf-skewed router bias
-    (tokens per expert ~50-600, several 256-token passes for the largest
+    (tokens per expert ~50-600, several 192-token passes for the largest
     groups); sampled pairs from the largest, a middle and the smallest group."""
     wl = W.WORKLOADS[4]
     sl, L, bias = layer(2, wl.zipf_beta)
