@@ -187,11 +187,11 @@ struct PfJob {
     int32_t E, n_pairs;
     int32_t min_tokens;        // experts with fewer tokens are not this launch's work
     const int32_t *offsets, *pairs;
-    const void *x;             // B rows: x[entry / x_div] (gate/up) or h[entry] (down, bf16)
+    const void *x;             // B rows: x[entry / x_div] (gate/up) or h[grouped position] (down, bf16)
     int32_t x_dtype;
     int64_t x_stride;
     int32_t x_div;
-    void *out;                 // gate/up: h bf16 [n_pairs][rows]; down: y fp32 [n_pairs][rows]
+    void *out;                 // gate/up: h bf16 [grouped position][rows]; down: y fp32 [entry][rows]
     uint32_t *status;
     int32_t layer, d, f;       // record header check
     int32_t selftest_stall;    // 1: the MMA role first waits for an arrival nothing makes

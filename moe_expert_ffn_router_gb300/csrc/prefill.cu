@@ -19,19 +19,23 @@
 //    rows of up, interleaved in fours (A row r holds weight row
 //    64 m + 4 (r / 8) + r % 4, of gate if r % 8 < 4, of up otherwise), so a
 //    row's gate and up accumulators sit four TMEM lanes apart and the epilogue
-//    pairs them with one shuffle: h = silu(g) * u -> bf16 [pair][f].
-//  * down launch: the A rows are down rows [128 m, 128 m + 128); the epilogue
-//    writes fp32 y [pair][d].
+//    pairs them with one shuffle: h = silu(g) * u -> bf16, row = the token's
+//    position in the expert-grouped order, so each pass's rows are contiguous.
+//  * down launch: the A rows are down rows [128 m, 128 m + 128); B is the
+//    pass's contiguous h rows, loaded by TMA; the epilogue writes fp32 y
+//    [pair][d].
 // Items are split into contiguous ranges over a persistent grid (one CTA per
 // SM), so consecutive items of a CTA mostly share the expert and its codebooks.
 //
 // Warp roles (512 threads):
 //  warp 0      TMEM owner; lane 0 issues the MMAs (4 per K step) and commits
-//  warps 1-2   B producers: cp.async gathers of token rows into the B slot
-//              (fp32 inputs: converted to bf16 and stored)
-//  warp 3      B relay (lane 0): once a slot's rows have landed, fences them
-//              into the async proxy and signals the K step (the fence costs
-//              the MMA thread nothing)
+//  warps 1-2   gate/up B producers: cp.async gathers of token rows into the
+//              B slot (fp32 inputs: converted to bf16 and stored)
+//  warp 3      gate/up B relay (lane 0): once a slot's rows have landed,
+//              fences them into the async proxy and signals the K step (the
+//              fence costs the MMA thread nothing)
+//  warp 1 l.0  down B producer: tiled TMA loads of the pass's h rows (async
+//              proxy, completion counted on the K step's full barrier)
 //  warps 4-7   epilogue: TMEM -> registers -> global (lane quarter = warp % 4)
 //  warps 8-15  A producers: decode code bytes into TMEM (lane quarter =
 //              warp % 4); warps 8-11 take the even K steps, 12-15 the odd ones
@@ -59,8 +63,11 @@
 // every role leaves its loop, the MMAs in flight are drained and TMEM is freed.
 #include "internal.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <string.h>
 
 namespace rvq {
 namespace {
@@ -103,10 +110,12 @@ static_assert(kTmemA + PF_NST * (PF_KC / 2) <= kTmemCols, "TMEM columns");
 static_assert(PF_NBAR >= PF_NSLOT + 1 && PF_NBAR >= PF_NST + 1, "a barrier pair outlives its stage");
 static_assert(kSlotB % 1024 == 0 && OFF_ST % 1024 == 0, "swizzled slots start on 1 KiB");
 
-constexpr int kLoaders = 64;                     // B producer threads (warps 1-2)
+constexpr int kLoaders = 64;                     // gate/up B producer threads (warps 1-2)
+constexpr int kTmaRows = 32;                     // token rows per down B TMA box
 constexpr int kLoaderRows = 3;                   // token rows per producer thread (192 / 64)
 constexpr int kDecodeWarps = 8;                  // A producer warps (8-15)
-// full[] arrivals: one half's decode warps + the B relay
+// full[] arrivals: one half's decode warps + the B side (the relay, or the
+// TMA producer's expect_tx arrival)
 constexpr uint32_t kFullCount = kDecodeWarps / 2 + 1;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: a bounded wait, never a hang
 
@@ -293,6 +302,23 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
+                 : "memory");
+}
+
+// Tiled TMA load of one box (64 bf16 columns from col x kTmaRows rows from
+// row) to dst, 128-byte swizzled by shared-address bits (the layout the MMA's
+// B descriptor reads); completes its bytes on mbar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int col, int row,
+                                            uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(mbar)
+        : "memory");
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -370,7 +396,8 @@ __device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, in
     return I;
 }
 
-__global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob job) {
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    prefill_gemm_kernel(const PfJob job, const __grid_constant__ CUtensorMap tmap_b) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle is a function of shared-address bits 4..9: B stages
     // must start on 1024-byte boundaries of the shared window
@@ -517,7 +544,38 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
     } else if (warp < 4) {
         // ================= B producers and relay =================
         uint32_t kg = 0, slot = 0;
-        if (warp < 3) {
+        if (!swiglu) {
+            // down: the pass's h rows are contiguous (grouped order); one
+            // thread loads kTmaRows-row boxes per K step
+            if (warp == 1 && lane == 0) {
+                for (int it = it0; it < it1 && !*abort_flag; ++it) {
+                    const PfItem I = pf_item(job, Q, MT, it);
+                    if (!I.valid) continue;
+                    const int nbox = (I.npad + kTmaRows - 1) / kTmaRows;
+                    const uint32_t bytes = (uint32_t)nbox * kTmaRows * (PF_KC * 2);
+                    const int q0 = I.o + I.j0;
+                    bool ok = true;
+                    for (int ks = 0; ks < KS; ++ks, ++kg) {
+                        if (kg >= (uint32_t)PF_NSLOT) {
+                            const uint32_t kp = kg - PF_NSLOT;
+                            if (!mbar_wait(bar(BAR_EMPTY + (kp & (PF_NBAR - 1))),
+                                           (kp / PF_NBAR) & 1u, abort_flag, job.status)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        const uint32_t sb = sbase + OFF_ST + slot * kSlotB;
+                        const uint32_t full = bar(BAR_FULL + (kg & (PF_NBAR - 1)));
+                        mbar_arrive_expect_tx(full, bytes);
+                        for (int i = 0; i < nbox; ++i)
+                            tma_load_2d(sb + i * kTmaRows * (PF_KC * 2), &tmap_b, ks * PF_KC,
+                                        q0 + i * kTmaRows, full);
+                        slot = slot == PF_NSLOT - 1 ? 0 : slot + 1;
+                    }
+                    if (!ok) break;
+                }
+            }
+        } else if (warp < 3) {
             const int lt = tid - 32;
             const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
@@ -643,14 +701,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
                 float a[32];
                 tmem_ld32(tl + ab * PF_NMAX + 32 * c, a);
                 if (swiglu) {
-                    uint16_t *hrow = reinterpret_cast<uint16_t *>(job.out) + R;
+                    // row of token t: its position in the grouped order
+                    uint16_t *hrow = reinterpret_cast<uint16_t *>(job.out) +
+                                     (size_t)(I.o + I.j0 + 32 * c) * job.rows + R;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const int p = __shfl_sync(0xffffffffu, pl[c], t);
                         const float u = __shfl_xor_sync(0xffffffffu, a[t], 4);
                         const float g = a[t];
                         const float hv = __fdividef(g * u, 1.0f + __expf(-g));
-                        if (q < 4 && p >= 0) hrow[(size_t)p * job.rows] = (uint16_t)bf16_bits(hv);
+                        if (q < 4 && p >= 0) hrow[(size_t)t * job.rows] = (uint16_t)bf16_bits(hv);
                     }
                 } else {
                     float *yrow = reinterpret_cast<float *>(job.out) + R;
@@ -803,6 +863,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gemm_kernel(const PfJob
     }
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library does not link the driver library itself).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
 }  // namespace
 
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) {
@@ -823,6 +898,37 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
                   job.tile_rows, job.E);
         return RVQ_EINVAL;
     }
+    // down: B = the pass's contiguous bf16 h rows, loaded by TMA (a 2D map
+    // over h: cols x n_pairs rows, pitch x_stride, boxes of 64 columns x
+    // kTmaRows rows, 128-byte swizzle; rows past the end read as zero)
+    CUtensorMap tmap;
+    memset(&tmap, 0, sizeof(tmap));
+    if (job.mode == PF_MODE_PLAIN) {
+        if (job.x_dtype != RVQ_BF16 || job.x_div != 1 || job.x_stride < job.cols ||
+            ((uintptr_t)job.x & 15u) != 0 || job.n_pairs < 1) {
+            set_error("prefill: down input must be bf16 rows of pitch >= %d, 16-byte aligned",
+                      job.cols);
+            return RVQ_EINVAL;
+        }
+        const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+        if (encode == nullptr) {
+            set_error("prefill: cuTensorMapEncodeTiled is not available");
+            return RVQ_ECUDA;
+        }
+        const cuuint64_t dims[2] = {(cuuint64_t)job.cols, (cuuint64_t)job.n_pairs};
+        const cuuint64_t strides[1] = {(cuuint64_t)job.x_stride * 2u};
+        const cuuint32_t box[2] = {(cuuint32_t)PF_KC, (cuuint32_t)kTmaRows};
+        const cuuint32_t estr[2] = {1u, 1u};
+        const CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                  const_cast<void *>(job.x), dims, strides, box, estr,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            set_error("prefill: cuTensorMapEncodeTiled failed (%d)", (int)r);
+            return RVQ_ECUDA;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)num_sms());
     cfg.blockDim = dim3(PF_THREADS);
@@ -833,7 +939,7 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    RVQ_CUDA(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel, job));
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel, job, tmap));
     return RVQ_OK;
 }
 
