@@ -328,15 +328,18 @@ struct PfItem {
     bool valid;
 };
 
-// Cost of one item in token-row units: a K step takes about max(decode
-// floor, fixed + B rows) cycles (measured: ~770 cycles with no B rows, ~7 per
-// row above that, so a floor of 112 and a fixed part of 32 rows).  CTAs get
-// contiguous item ranges of equal total cost: item costs differ by 2x or more
-// across a Zipf-skewed chunk, and equal item counts left the slowest CTA 1.5x
-// behind the median.
-constexpr int64_t kCostFloor = 112, kCostFixed = 32;
-__device__ __forceinline__ int64_t pf_cost(int npad) {
-    return max(kCostFloor, kCostFixed + (int64_t)npad);
+// Cost of one item per K step, in units of ~7.7 cycles (one gathered token
+// row), fitted to timestamp traces of the 2048-token chunk:
+//  * gate/up (token rows gathered by cp.async): max(decode floor ~770
+//    cycles, ~240 + 7.7 per row);
+//  * down (rows by TMA): ~800 cycles + ~1 per row, plus a start of ~3,000
+//    cycles spread over its 32 K steps.
+// CTAs get contiguous item ranges of equal total cost: item costs differ by
+// 2x or more across a Zipf-skewed chunk, and equal item counts left the
+// slowest CTA 1.5x behind the median.
+__device__ __forceinline__ int64_t pf_cost(const PfJob &job, int npad) {
+    return job.mode == PF_MODE_SWIGLU ? max((int64_t)112, (int64_t)32 + npad)
+                                      : (int64_t)116 + npad / 8;
 }
 
 // Passes of expert e (0 when its group is below min_tokens) and their cost.
@@ -346,7 +349,8 @@ __device__ __forceinline__ void pf_expert_cost(const PfJob &job, int ne, int MT,
     cost = 0;
     if (passes > 0) {
         const int last = ne - (passes - 1) * PF_NMAX;
-        cost = (int64_t)MT * ((passes - 1) * pf_cost(PF_NMAX) + pf_cost((last + 15) & ~15));
+        cost = (int64_t)MT *
+               ((passes - 1) * pf_cost(job, PF_NMAX) + pf_cost(job, (last + 15) & ~15));
     }
 }
 
@@ -362,8 +366,8 @@ __device__ int pf_first_item(const PfJob &job, const int32_t *Q, const int64_t *
     }
     const int ne = job.offsets[lo + 1] - job.offsets[lo];
     const int P = (ne + PF_NMAX - 1) / PF_NMAX;
-    const int64_t cf = pf_cost(PF_NMAX);
-    const int64_t cl = pf_cost((ne - (P - 1) * PF_NMAX + 15) & ~15);
+    const int64_t cf = pf_cost(job, PF_NMAX);
+    const int64_t cl = pf_cost(job, (ne - (P - 1) * PF_NMAX + 15) & ~15);
     int64_t rem = t - W[lo];
     const int64_t pq = rem / ((int64_t)MT * cf);
     const int pi = (int)(pq < (int64_t)P - 1 ? pq : (int64_t)P - 1);
