@@ -80,6 +80,21 @@ def test_tensor_core_path_all_experts_d2048():
         assert_rms_close(out.cpu().numpy()[t] - x64[t], ref - x64[t], TC_TOL, "out - x")
 
 
+def test_tensor_core_path_fp32_input():
+    """fp32 activations on the tensor-core path: the kernel's loaders convert
+    the token rows to bf16 instead of copying bf16 rows.  The values are
+    bf16-representable, so the conversion is exact and the bf16 tolerance
+    applies unchanged (general fp32 inputs add their own bf16 rounding)."""
+    sl, L, _ = layer(1)
+    n = 24
+    x32 = synth.bf16_to_f32(sl.tokens_bf16(n))
+    x = torch.from_numpy(x32).to(DEV)
+    b = route(L, x, n)
+    y = run_ffn(L, x, n, b, tc_min_tokens=1)
+    idx = b["idx"].cpu().numpy()
+    check_pairs(sl, x32.astype(np.float64), idx, y, range(0, n * L.k, 2), lambda e: TC_TOL)
+
+
 def test_mixed_dispatch_by_group_size():
     """Seven copies of each of two tokens plus ten others: their experts get
     groups of >= 7 tokens (tensor cores); the rest stay on lookup tables."""
