@@ -10,6 +10,8 @@
 // pairs grouped by (expert, token).
 #include "internal.cuh"
 
+#include <cooperative_groups.h>
+
 namespace rvq {
 namespace {
 
@@ -73,19 +75,31 @@ __global__ void __launch_bounds__(LG_NT) router_logits_kernel(
 }
 
 // Prefill-sized batches: a tiled fp32 GEMM, logits[n][E] = x Wr^T.  Each
-// block computes 64 tokens x 64 experts; 256 threads hold 4 x 4 outputs each;
-// K runs in slices of 32 staged (k-major, fp32) in shared memory with the next
-// slice prefetched into registers.  Sums run in a fixed order, so the result
+// output tile of 64 tokens x 64 experts belongs to a cluster of LT_S blocks
+// that split the hidden dimension; in a block 256 threads hold 4 x 4 outputs
+// each, and K runs in slices of 32 staged (k-major, fp32) in shared memory
+// with the next slice prefetched into registers.  (One block per tile over
+// the whole of K leaves 2048 x 256 logits at 128 blocks: most of the GPU
+// idle.)  The cluster's rank-0 block adds the partial tiles from its peers'
+// shared memory in rank order, so sums run in a fixed order and the result
 // does not depend on the launch.
-constexpr int LT_T = 64, LT_E = 64, LT_K = 32, LT_PAD = 4;
+constexpr int LT_T = 64, LT_E = 64, LT_K = 32, LT_PAD = 4, LT_S = 4;
 
 __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
     const float *__restrict__ wr, const float *__restrict__ bias, const void *__restrict__ x,
     int xdt, int n, int E, int d, float *__restrict__ logits) {
-    __shared__ __align__(16) float xs[LT_K][LT_T + LT_PAD];
-    __shared__ __align__(16) float ws[LT_K][LT_E + LT_PAD];
+    // staging for the K slices; afterwards this block's partial tile
+    __shared__ __align__(16) float stage[2 * LT_K * (LT_T + LT_PAD)];
+    static_assert(LT_E + LT_PAD == LT_T + LT_PAD && LT_T * LT_E <= 2 * LT_K * (LT_T + LT_PAD),
+                  "partial tile fits the staging area");
+    float (*xs)[LT_T + LT_PAD] = reinterpret_cast<float (*)[LT_T + LT_PAD]>(stage);
+    float (*ws)[LT_E + LT_PAD] =
+        reinterpret_cast<float (*)[LT_E + LT_PAD]>(stage + LT_K * (LT_T + LT_PAD));
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int e0 = blockIdx.x * LT_E, t0 = blockIdx.y * LT_T;
+    // this block's share of K (gridDim.z = blocks of the cluster)
+    const int dk = d / (int)gridDim.z;
+    const int kb = (int)blockIdx.z * dk, ke = kb + dk;
     // loader: row = tid / 4 (token or expert), 8 consecutive k at (tid % 4) * 8
     const int lr = tid >> 2, lk = (tid & 3) * 8;
     const bool xin = t0 + lr < n, win = e0 + lr < E;
@@ -128,8 +142,8 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    load(0);
-    for (int k0 = 0; k0 < d; k0 += LT_K) {
+    load(kb);
+    for (int k0 = kb; k0 < ke; k0 += LT_K) {
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -137,7 +151,7 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
             ws[lk + i][lr] = wv[i];
         }
         __syncthreads();
-        if (k0 + LT_K < d) load(k0 + LT_K);
+        if (k0 + LT_K < ke) load(k0 + LT_K);
         // two-level sums (a slice of 32 products, then across slices) keep the
         // rounding error of the 7168-term dot products near the tree-sum level
         float part[4][4];
@@ -160,16 +174,37 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[i][j] += part[i][j];
     }
+    // partial tile -> shared memory; rank 0 adds the peers' tiles in rank order
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    float *part = stage;  // [LT_T][LT_E]
+    __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
-        if (t >= n) continue;
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
-            if (e < E) logits[(int64_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+        for (int j = 0; j < 4; ++j) part[(ty * 4 + i) * LT_E + tx * 4 + j] = acc[i][j];
+    cluster.sync();
+    if (cluster.block_rank() == 0) {
+        for (unsigned r = 1; r < cluster.num_blocks(); ++r) {
+            const float *peer = cluster.map_shared_rank(part, r);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] += peer[(ty * 4 + i) * LT_E + tx * 4 + j];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = t0 + ty * 4 + i;
+            if (t >= n) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = e0 + tx * 4 + j;
+                if (e < E) logits[(int64_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+            }
         }
     }
+    // the peers' tiles stay in place until rank 0 has read them
+    cluster.sync();
 }
 
 // ------------------------------------------------------------------- route
@@ -393,8 +428,22 @@ rvq_status launch_router_logits(const float *wr, const float *bias, const void *
     if (n == 1) {
         router_logits_kernel<1><<<dim3(E, 1), LG_NT, 0, stream>>>(wr, bias, x, xdt, n, E, d, logits);
     } else if (n > 64 && d % LT_K == 0) {
-        router_logits_tiled_kernel<<<dim3((E + LT_E - 1) / LT_E, (n + LT_T - 1) / LT_T), 256, 0,
-                                     stream>>>(wr, bias, x, xdt, n, E, d, logits);
+        // a cluster of LT_S blocks per output tile when K splits evenly
+        const int S = d % (LT_S * LT_K) == 0 ? LT_S : 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((E + LT_E - 1) / LT_E), (unsigned)((n + LT_T - 1) / LT_T),
+                           (unsigned)S);
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)S;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        RVQ_CUDA(cudaLaunchKernelEx(&cfg, router_logits_tiled_kernel, wr, bias, x, xdt, n, E, d,
+                                    logits));
     } else {
         router_logits_kernel<8><<<dim3(E, (n + 7) / 8), LG_NT, 0, stream>>>(wr, bias, x, xdt, n, E, d,
                                                                             logits);
