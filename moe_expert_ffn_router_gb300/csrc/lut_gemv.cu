@@ -741,23 +741,28 @@ __device__ __forceinline__ bool il_next(const LutJob &job, int S, int w1, const 
 __device__ __forceinline__ void il_build(uint8_t *lut, int h, const uint8_t *cb_s,
                                          const uint8_t *xs_s, int xdt, int warp, int lane) {
     const int q = lane >> 3, r = lane & 7;
+    // slot jj of this lane holds column r + 8 ((jj + q) mod 4): the quarters
+    // rotate their column blocks, so each store instruction writes 32 banks
     float x[4][8];
+    int coff[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int c = r + 8 * j;
+    for (int jj = 0; jj < 4; ++jj) {
+        const int c = r + 8 * ((jj + q) & 3);
+        coff[jj] = c * 4;
+        float(&xj)[8] = x[jj];
         if (xdt == RVQ_BF16) {
             const uint4 v = *reinterpret_cast<const uint4 *>(xs_s + c * 16);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                x[j][2 * i] = __uint_as_float(w[i] << 16);
-                x[j][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                xj[2 * i] = __uint_as_float(w[i] << 16);
+                xj[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
             }
         } else {
             const float4 a = *reinterpret_cast<const float4 *>(xs_s + c * 32);
             const float4 b = *reinterpret_cast<const float4 *>(xs_s + c * 32 + 16);
-            x[j][0] = a.x; x[j][1] = a.y; x[j][2] = a.z; x[j][3] = a.w;
-            x[j][4] = b.x; x[j][5] = b.y; x[j][6] = b.z; x[j][7] = b.w;
+            xj[0] = a.x; xj[1] = a.y; xj[2] = a.z; xj[3] = a.w;
+            xj[4] = b.x; xj[5] = b.y; xj[6] = b.z; xj[7] = b.w;
         }
     }
     const float4 *cb4 = reinterpret_cast<const float4 *>(cb_s);
@@ -784,17 +789,8 @@ __device__ __forceinline__ void il_build(uint8_t *lut, int h, const uint8_t *cb_
         uint8_t *row0 = lut + s * kLutStageBytes + k * 256 + h * 128;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const int j = (jj + q) & 3;
-            float va = ta[0], vb = tb[0];
-#pragma unroll
-            for (int z = 1; z < 4; ++z)
-                if (j == z) {
-                    va = ta[z];
-                    vb = tb[z];
-                }
-            const int c = r + 8 * j;
-            *reinterpret_cast<float *>(row0 + c * 4) = va;
-            *reinterpret_cast<float *>(row0 + 256 + c * 4) = vb;
+            *reinterpret_cast<float *>(row0 + coff[jj]) = ta[jj];
+            *reinterpret_cast<float *>(row0 + 256 + coff[jj]) = tb[jj];
         }
     }
 }
