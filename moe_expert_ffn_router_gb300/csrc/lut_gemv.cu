@@ -844,21 +844,30 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, co
 
     // table walk (identical in every thread) and this warp's tile walk
     IlWalk tw = il_start(job, S, w0), gw = tw;
-    IlTab cur, nxt, gt;
+    IlTab cur, nxt;
     bool has_cur = il_next(job, S, w1, pd, tw, cur);
     bool has_nxt = has_cur && il_next(job, S, w1, pd, tw, nxt);
     int gi = 0, gn = 0;  // tile walk: index within table gt, its unit count
+    // this warp's next tile and output of table gt: set when the walk enters
+    // a table, then advanced by one unit (IL_ROWS rows) per tile
+    const uint8_t *gtile = nullptr;
+    float *gout = nullptr;
     auto gen = [&](const uint8_t *&tile, float *&out) -> bool {
         if (gi == gn) {
+            IlTab gt;
             if (!il_next(job, S, w1, pd, gw, gt)) return false;
             gi = 0;
             gn = gt.nr;
+            const int rb = gt.r0 * (IL_ROWS / 32) + warp;
+            const uint8_t *rec = job.base + (uint64_t)gt.d.x * job.record_bytes;
+            gtile = rec + job.codes_off[gt.m] + ((size_t)gt.g * RB + rb) * kTileBytes + lane * 16;
+            gout = job.part[gt.m] + ((size_t)gt.d.y * nslot + gt.g) * job.rows + rb * 32 + lane;
         }
-        const int rb = (gt.r0 + gi) * (IL_ROWS / 32) + warp;
         ++gi;
-        const uint8_t *rec = job.base + (uint64_t)gt.d.x * job.record_bytes;
-        tile = rec + job.codes_off[gt.m] + ((size_t)gt.g * RB + rb) * kTileBytes + lane * 16;
-        out = job.part[gt.m] + ((size_t)gt.d.y * nslot + gt.g) * job.rows + rb * 32 + lane;
+        tile = gtile;
+        out = gout;
+        gtile += (IL_ROWS / 32) * kTileBytes;
+        gout += IL_ROWS;
         return true;
     };
     uint4 buf[2][6];
