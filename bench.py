@@ -194,6 +194,24 @@ def build_layer(config, device, k=None, shape=None, layer=0):
     return L, src
 
 
+def replica_max_ms(ms, world, device):
+    """The slowest replica's time in ms: the whole job ends when its last
+    rank does (replicas only; the one collective of the bench)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (every replica runs the same seeded workload)."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import moe_expert_ffn_router_gb300 as rvq
@@ -272,19 +290,14 @@ def run_gpu(args, rank, world, local_rank):
     sampler.stop()
     clocks = sampler.summary(t0w, t1w)
 
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = replica_max_ms(ms, world, dev)
 
     steps_idx = [(args.warmup + i) % nsteps for i in range(args.steps)]
     experts_total = sum(uniq[j] for j in steps_idx)
-    weights = experts_total * weights_per_expert * world
-    sec = ms / 1e3
-    value = weights / sec / 1e9
-    code_gbs = experts_total * (code_bytes_per_expert + cb_bytes_per_expert) * world / sec / 1e9
-    tok_s = batch * args.steps * world / sec
+    value = job_rate(experts_total * weights_per_expert, world, ms) / 1e9
+    code_gbs = job_rate(experts_total * (code_bytes_per_expert + cb_bytes_per_expert), world,
+                        ms) / 1e9
+    tok_s = job_rate(batch * args.steps, world, ms)
 
     # ---- per-kernel durations (events between kernels, same steps) ----
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(rvq.MOE_LAYER_EVENTS)]
@@ -349,13 +362,9 @@ def run_gpu(args, rank, world, local_rank):
         pinned_out.copy_(out_last, non_blocking=True)
     e1.record()
     barrier()
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_e2e = float(tt.item())
-    e2e = {"value": round(weights / (ms_e2e / 1e3) / 1e9, 2), "unit": UNIT,
+    ms_e2e = replica_max_ms(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": round(job_rate(experts_total * weights_per_expert, world, ms_e2e) / 1e9, 2),
+           "unit": UNIT,
            "h2d_bytes_per_step": batch * s.d * 2, "d2h_bytes_per_step": batch * s.d * 4}
     for Lx in stack.layers:
         rc, bits = Lx.status(batch)
@@ -417,7 +426,7 @@ def reference_arm(args, rank):
     import synth
     config, batch, s = workload_shape(args.workload)
     src = W.ExpertSource(config, 0, s)
-    per_pair_s = 0.15 * (s.d * s.f) / (7168 * 2048)
+    per_pair_s = 1.4 * (s.d * s.f) / (7168 * 2048)  # measured on the GB300 host, one core
     m = int(max(1, min(s.k * batch, 60.0 / ((args.steps + args.warmup) * per_pair_s))))
     wr = src.router_weight()
     bias = router_bias(config, src)
@@ -464,8 +473,10 @@ def reference_arm(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 200; 10 for --impl reference, whose steps "
+                         "take about a second of CPU time each)")
+    ap.add_argument("--warmup", type=int, default=None, help="untimed steps (default 10; 3)")
     ap.add_argument("--workload", default="k3_decode_b1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--oracle-tokens", type=int, default=4)
@@ -475,6 +486,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (profiling runs)")
     args = ap.parse_args()
+    ref = args.impl == "reference"
+    if args.steps is None:
+        args.steps = 10 if ref else 200
+    if args.warmup is None:
+        args.warmup = 3 if ref else 10
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
