@@ -24,8 +24,9 @@
 //  * down launch: the A rows are down rows [128 m, 128 m + 128); B is the
 //    pass's contiguous h rows, loaded by TMA; the epilogue writes fp32 y
 //    [pair][d].
-// Items are split into contiguous ranges over a persistent grid (one CTA per
-// SM), so consecutive items of a CTA mostly share the expert and its codebooks.
+// Items are split into contiguous ranges of equal estimated cost over a
+// persistent grid (one CTA per SM), so consecutive items of a CTA mostly share
+// the expert and its codebooks.
 //
 // Warp roles (512 threads):
 //  warp 0      TMEM owner; lane 0 issues the MMAs (4 per K step) and commits
@@ -43,9 +44,11 @@
 // 384 + 32 s), B slot t % 5 (shared memory; five slots keep up to 120 KiB of
 // token rows in flight against the L2 latency of the row gathers) and the
 // full/empty mbarrier pair t % 8.  full[t % 8] completes once the four decode
-// warps of the K step and every B producer have arrived, so the MMA thread
-// waits once and commits once per K step: its instruction stream, not the
-// tensor pipe, is the limit at the group sizes of a prefill chunk.  A decode
+// warps of the K step and the B side (the relay, or the TMA producer's
+// expect_tx arrival and its bytes) have arrived, so the MMA thread waits once
+// and commits once per K step.  At the group sizes of a prefill chunk the MMA
+// thread is the limit: an M=128 MMA occupies the tensor pipe for at least ~80
+// cycles whatever N <= 160, plus the thread's wait and commit.  A decode
 // warp reuses a stage after empty[(t - 4) % 8], a B producer a slot after
 // empty[(t - 5) % 8].  Two accumulators (TMEM columns 0 and 192, guarded by
 // acc_full / acc_empty) let the epilogue of one item overlap the main loop of
