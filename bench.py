@@ -67,6 +67,13 @@ DOMINANT_TC = "prefill_gate_up"
 TC_LAUNCHES_PER_STEP = 6
 
 
+def router_launches(n, E, d):
+    """Launches of the layer's router logits: the tensor-core GEMM for a
+    prefill-sized bf16 batch (n >= 128, E % 128 == 0, d % 256 == 0) adds the
+    split of Wr into three bf16 terms."""
+    return 2 if n >= 128 and E % 128 == 0 and d % 256 == 0 else 1
+
+
 def load_traffic(name):
     """DRAM bytes per launch of `name` from the committed ncu summary, or None
     when the kernel source changed since that capture."""
@@ -375,6 +382,7 @@ def run_gpu(args, rank, world, local_rank):
                uniq_mean=float(np.mean([uniq[j] for j in steps_idx])),
                launches=((TC_LAUNCHES_PER_STEP if tc_min == 1 else len(KERNELS) if tc_min == 0
                           else len(KERNELS) + TC_LAUNCHES_PER_STEP - 3)
+                         + router_launches(batch, s.E, s.d) - 1
                          + (1 if n_layers > 1 else 0)) * args.steps * n_layers,
                config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
     del L, stack, built

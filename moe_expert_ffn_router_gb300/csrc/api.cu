@@ -89,7 +89,7 @@ static void choose_split(int rows, int cols, int n_pairs, int n_mat, int E, int 
     S_out = bs;
 }
 
-FfnPlan plan_ffn(int d, int f, int n_pairs, int E) {
+FfnPlan plan_ffn(int d, int f, int n_pairs, int E, int n_tokens) {
     FfnPlan P;
     choose_split(f, d, n_pairs, 2, E, P.C_gu, P.S_gu);
     choose_split(d, f, n_pairs, 1, E, P.C_d, P.S_d);
@@ -112,6 +112,8 @@ FfnPlan plan_ffn(int d, int f, int n_pairs, int E) {
     off = align256(off + (size_t)n_pairs * f * 2);
     P.off_ypair = off;
     off = align256(off + (size_t)n_pairs * d * 4);
+    P.off_wsplit = off;
+    if (router_tc_supported(n_tokens, E, d)) off = align256(off + router_tc_split_bytes(E, d));
     P.total = off;
     return P;
 }
@@ -395,7 +397,7 @@ rvq_status moe_route(const float *logits_dev, int32_t n, int32_t E, int32_t k,
 size_t moe_workspace_bytes(const rvq_moe_bank *bank, int32_t n, int32_t k) {
     if (!bank || n < 1 || k < 1) return 0;
     if (bank->d <= 0 || bank->f <= 0 || bank->d % 512 || bank->f % 512) return 0;
-    return plan_ffn(bank->d, bank->f, n * k, bank->n_experts).total;
+    return plan_ffn(bank->d, bank->f, n * k, bank->n_experts, n).total;
 }
 
 static LutJob ffn_job(const rvq_moe_bank *bank, const RecordLayout &L, int n_pairs, void *ws) {
@@ -646,7 +648,7 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
     CHECK_ALIGN(out_dev, "moe_layer_forward: out");
     if (xdt == RVQ_BF16)
         CHECK_ARG((const void *)out_dev != x_dev, "moe_layer_forward: bf16 x cannot alias out");
-    const FfnPlan P = plan_ffn(bank->d, bank->f, n * k, bank->n_experts);
+    const FfnPlan P = plan_ffn(bank->d, bank->f, n * k, bank->n_experts, n);
     cudaStream_t st = (cudaStream_t)stream;
     const bool pdl = events == nullptr;
     auto mark = [&](int i) -> rvq_status {
@@ -654,8 +656,14 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
         return RVQ_OK;
     };
     RVQ_TRY(mark(0));
-    RVQ_TRY(launch_router_logits(wr_dev, bias_dev, x_dev, (int)xdt, n, bank->n_experts, bank->d,
-                                 logits_dev, st));
+    if (xdt == RVQ_BF16 && router_tc_supported(n, bank->n_experts, bank->d))
+        // prefill-sized bf16 batch: the logits GEMM on the tensor cores
+        RVQ_TRY(launch_router_logits_tc(wr_dev, bias_dev, x_dev, n, bank->n_experts, bank->d,
+                                        logits_dev, (uint8_t *)ws_dev + P.off_wsplit,
+                                        (uint32_t *)ws_dev, st));
+    else
+        RVQ_TRY(launch_router_logits(wr_dev, bias_dev, x_dev, (int)xdt, n, bank->n_experts,
+                                     bank->d, logits_dev, st));
     RVQ_TRY(mark(1));
     RVQ_TRY(launch_route(logits_dev, n, bank->n_experts, k, topk_idx_dev, topk_w_dev, offsets_dev,
                          pairs_dev, (uint32_t *)ws_dev, st, pdl));

@@ -197,6 +197,15 @@ struct PfJob {
     int32_t selftest_stall;    // 1: the MMA role first waits for an arrival nothing makes
 };
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
+// cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000) or null
+void *tensor_map_encoder_entry();
+// tensor-core router logits (bf16 tokens, n >= 128, E % 128 == 0, d % 256 == 0):
+// splits Wr into three bf16 terms in wsplit (router_tc_split_bytes), then the GEMM
+bool router_tc_supported(int n, int E, int d);
+size_t router_tc_split_bytes(int E, int d);
+rvq_status launch_router_logits_tc(const float *wr, const float *bias, const void *x, int n,
+                                   int E, int d, float *logits, void *wsplit, uint32_t *status,
+                                   cudaStream_t stream);
 
 // FFN plan: how moe_expert_ffn splits its work (host side, deterministic).
 struct FfnPlan {
@@ -204,9 +213,11 @@ struct FfnPlan {
     int C_d, S_d;     // down
     int nslot_gu, nslot_d;
     size_t off_gpart, off_upart, off_h, off_dpart, off_desc_gu, off_desc_d;
-    size_t off_h16, off_ypair, total;  // tensor-core path: h bf16, y fp32 [pair][d]
+    size_t off_h16, off_ypair;  // tensor-core path: h bf16, y fp32 [pair][d]
+    size_t off_wsplit;          // tensor-core router: Wr as three bf16 terms (0 bytes if unused)
+    size_t total;
 };
-FfnPlan plan_ffn(int d, int f, int n_pairs, int E);
+FfnPlan plan_ffn(int d, int f, int n_pairs, int E, int n_tokens = 0);
 int num_sms();
 
 }  // namespace rvq

@@ -887,6 +887,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
+void *tensor_map_encoder_entry() { return reinterpret_cast<void *>(tensor_map_encoder()); }
+
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) {
     static int attr_done[64] = {0};
     int dev = 0;

@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(LG_NT) router_logits_kernel(
     for (int b = 0; b < TB; ++b) acc[b] = 0.f;
     const float4 *w4 = reinterpret_cast<const float4 *>(wr + (int64_t)e * d);
     const int d4 = d >> 2;
-#pragma unroll 4
+    // every load of a thread in flight at once (d = 7168: 7 per thread)
+#pragma unroll 8
     for (int c4 = threadIdx.x; c4 < d4; c4 += LG_NT) {
         const float4 wv = __ldg(w4 + c4);
 #pragma unroll

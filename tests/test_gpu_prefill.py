@@ -148,6 +148,32 @@ def test_prefill_chunk_full_size_zipf():
     sl.forget()
 
 
+@pytest.mark.parametrize("n", [2048, 300])
+def test_layer_router_on_tensor_cores_k3(n):
+    """The layer's router logits for a prefill-sized bf16 batch of the
+    K3-shaped layer (Zipf bias) come from the tensor-core GEMM (Wr as three
+    bf16 terms): within 1e-5 x RMS of the oracle's logits, routing and
+    grouping bit-exact given them.  n = 300 leaves a ragged 44-token tile."""
+    wl = W.WORKLOADS[4]
+    sl, L, bias = layer(2, wl.zipf_beta)
+    bits = sl.tokens_bf16(n)
+    x = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    b = L.forward(x, tc_min_tokens=1)
+    torch.cuda.synchronize()
+    assert L.status(n) == (0, 0)
+    x64 = bf16_bits_to_f64(bits)
+    logits = b["logits"].cpu().numpy()
+    assert_rms_close(logits, oracle.router_logits(sl.wr, x64, bias), 1e-5, "tensor-core logits")
+    idx, w = b["idx"].cpu().numpy(), b["w"].cpu().numpy()
+    ridx, rw, _ = oracle.route(logits, L.k)
+    assert np.array_equal(idx, ridx)
+    np.testing.assert_allclose(w, rw, rtol=2e-6, atol=1e-9)
+    roff, rpairs = oracle.group(ridx, L.E)
+    assert np.array_equal(b["offsets"].cpu().numpy(), roff)
+    assert np.array_equal(b["pairs"].cpu().numpy(), rpairs)
+    assert np.isfinite(b["out"].cpu().numpy()).all()
+
+
 def test_layer_forward_with_dispatch_d2048():
     """Whole layer through moe_layer_forward_ex for 100 tokens (tiled router
     logits, grid-wide selection, tensor-core experts, all-slot combine):
