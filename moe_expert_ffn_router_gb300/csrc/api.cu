@@ -484,6 +484,7 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
         RVQ_TRY(mark(1));
         RVQ_TRY(launch_swiglu_reduce(gpart, upart, np, P.nslot_gu, bank->f, h, st, pdl));
         RVQ_TRY(mark(2));
+        dn.early_start = 1;  // the plan is three launches back; only h is new
         RVQ_TRY(launch_lut_gemv_il(dn, pd, st, pdl));
         return mark(3);
     }

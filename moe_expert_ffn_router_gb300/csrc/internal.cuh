@@ -139,6 +139,11 @@ struct LutJob {
     // record header check
     int32_t check_header;
     int32_t layer, d, f;
+    // interleaved GEMV: 1 when only the inputs x come from the immediately
+    // preceding kernel (the pair plan was written two or more launches back),
+    // so the first table's codebook and code tiles are requested before the
+    // dependency wait
+    int32_t early_start;
 };
 
 __host__ __device__ inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }

@@ -796,21 +796,15 @@ __device__ __forceinline__ void il_build(uint8_t *lut, int h, const uint8_t *cb_
 }
 
 // One thread fetches a table's inputs onto the mbarrier: the pair's 256
-// input values of chunk group g and, unless `same_cb`, the codebook.
-__device__ __forceinline__ void il_fetch(const LutJob &job, const IlTab &t, bool same_cb,
-                                         uint8_t *cb_s, uint8_t *xs_s, uint32_t bar) {
+// input values of chunk group g and, unless `same_cb`, the codebook.  The
+// two halves can be issued apart (the codebook first, the inputs once the
+// kernel that writes them has completed): il_fetch_cb announces both.
+__device__ __forceinline__ void il_fetch_cb(const LutJob &job, const IlTab &t, bool same_cb,
+                                            uint8_t *cb_s, uint32_t bar) {
     const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
-    const uint32_t xbytes = 256u * esz;
-    const uint32_t bytes = xbytes + (same_cb ? 0u : (uint32_t)kCbBytes);
+    const uint32_t bytes = 256u * esz + (same_cb ? 0u : (uint32_t)kCbBytes);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
-    const uint8_t *xsrc = reinterpret_cast<const uint8_t *>(job.x) +
-                          ((int64_t)(t.d.y / job.x_div) * job.x_stride + (int64_t)t.g * 256) * esz;
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            (uint32_t)__cvta_generic_to_shared(xs_s)),
-        "l"(xsrc), "r"(xbytes), "r"(bar)
-        : "memory");
     if (!same_cb) {
         const uint8_t *cb = job.base + (uint64_t)t.d.x * job.record_bytes + job.cb_off[t.m];
         asm volatile(
@@ -819,6 +813,22 @@ __device__ __forceinline__ void il_fetch(const LutJob &job, const IlTab &t, bool
             "l"(cb), "r"((uint32_t)kCbBytes), "r"(bar)
             : "memory");
     }
+}
+__device__ __forceinline__ void il_fetch_x(const LutJob &job, const IlTab &t, uint8_t *xs_s,
+                                           uint32_t bar) {
+    const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
+    const uint8_t *xsrc = reinterpret_cast<const uint8_t *>(job.x) +
+                          ((int64_t)(t.d.y / job.x_div) * job.x_stride + (int64_t)t.g * 256) * esz;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            (uint32_t)__cvta_generic_to_shared(xs_s)),
+        "l"(xsrc), "r"((uint32_t)(256 * esz)), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void il_fetch(const LutJob &job, const IlTab &t, bool same_cb,
+                                         uint8_t *cb_s, uint8_t *xs_s, uint32_t bar) {
+    il_fetch_cb(job, t, same_cb, cb_s, bar);
+    il_fetch_x(job, t, xs_s, bar);
 }
 
 __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, const int4 *pd) {
@@ -839,8 +849,15 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, co
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
+    // The table walk reads the pair plan; with early_start it was written
+    // by a kernel that completed before the preceding one began, so the walk,
+    // the first code tiles and the first codebook need not wait for the
+    // preceding kernel (which writes only the inputs x).
+    const bool early = job.early_start != 0;
+    if (!early) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
 
     // table walk (identical in every thread) and this warp's tile walk
     IlWalk tw = il_start(job, S, w0), gw = tw;
@@ -885,17 +902,23 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, co
     uint32_t inph = 0;  // phase of the input barrier
     bool alive = true;  // false after a timed-out wait: no more reads, barriers still met
     int cb_m = -1, cb_e = -1;
+    if (has_cur && threadIdx.x == 0) {
+        // the first table's codebook and code tiles (bank data)
+        il_fetch_cb(job, cur, false, cb_s, inbar);
+        const uint8_t *t0 = job.base + (uint64_t)cur.d.x * job.record_bytes +
+                            job.codes_off[cur.m] +
+                            ((size_t)cur.g * RB + cur.r0 * (IL_ROWS / 32)) * kTileBytes;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(t0),
+                     "r"((uint32_t)(cur.nr * (IL_ROWS / 32) * kTileBytes))
+                     : "memory");
+    }
+    if (early) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
     if (has_cur) {
-        // the first table: fetched and built by all warps before streaming
-        if (threadIdx.x == 0) {
-            il_fetch(job, cur, false, cb_s, xs_s, inbar);
-            const uint8_t *t0 = job.base + (uint64_t)cur.d.x * job.record_bytes +
-                                job.codes_off[cur.m] +
-                                ((size_t)cur.g * RB + cur.r0 * (IL_ROWS / 32)) * kTileBytes;
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(t0),
-                         "r"((uint32_t)(cur.nr * (IL_ROWS / 32) * kTileBytes))
-                         : "memory");
-        }
+        // the first table: its inputs, then built by all warps before streaming
+        if (threadIdx.x == 0) il_fetch_x(job, cur, xs_s, inbar);
         cb_m = cur.m;
         cb_e = cur.d.x;
         alive = il_wait(inbar, inph, job.status);
