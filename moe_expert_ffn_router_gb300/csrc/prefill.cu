@@ -14,13 +14,16 @@
 // write their rows of A straight into tensor memory (tcgen05.st), so A costs
 // no shared-memory stores or operand reads, and every MMA reads B once.
 //
-// A work item is (expert, pass of <= 192 tokens, M tile of 128 A rows):
-//  * gate/up launch: the A rows are 64 weight rows of gate and the same 64
+// A work item is (expert, pass of <= 192 tokens, M tiles of 128 A rows):
+//  * gate/up launch: an M tile holds 64 weight rows of gate and the same 64
 //    rows of up, interleaved in fours (A row r holds weight row
 //    64 m + 4 (r / 8) + r % 4, of gate if r % 8 < 4, of up otherwise), so a
 //    row's gate and up accumulators sit four TMEM lanes apart and the epilogue
 //    pairs them with one shuffle: h = silu(g) * u -> bf16, row = the token's
 //    position in the expert-grouped order, so each pass's rows are contiguous.
+//    An item takes two M tiles (2 m, 2 m + 1) that share every K step's
+//    gathered token rows: 8 MMAs per B slot, half the L2 -> SM row traffic
+//    (the rows were the bound: ~7.7 cycles per gathered row per K step).
 //  * down launch: the A rows are down rows [128 m, 128 m + 128); B is the
 //    pass's contiguous h rows, loaded by TMA; the epilogue writes fp32 y
 //    [pair][d].
@@ -29,7 +32,8 @@
 // the expert and its codebooks.
 //
 // Warp roles (512 threads):
-//  warp 0      TMEM owner; lane 0 issues the MMAs (4 per K step) and commits
+//  warp 0      TMEM owner; lane 0 issues the MMAs (4 per M tile and K step)
+//              and commits
 //  warps 1-2   gate/up B producers: cp.async gathers of token rows into the
 //              B slot (fp32 inputs: converted to bf16 and stored)
 //  warp 3      gate/up B relay (lane 0): once a slot's rows have landed,
@@ -39,20 +43,25 @@
 //              proxy, completion counted on the K step's full barrier)
 //  warps 4-7   epilogue: TMEM -> registers -> global (lane quarter = warp % 4)
 //  warps 8-15  A producers: decode code bytes into TMEM (lane quarter =
-//              warp % 4); warps 8-11 take the even K steps, 12-15 the odd ones
-// K step t of the CTA's sequence uses A stage t % 4 (TMEM columns
-// 384 + 32 s), B slot t % 5 (shared memory; five slots keep up to 120 KiB of
-// token rows in flight against the L2 latency of the row gathers) and the
-// full/empty mbarrier pair t % 8.  full[t % 8] completes once the four decode
-// warps of the K step and the B side (the relay, or the TMA producer's
-// expect_tx arrival and its bytes) have arrived, so the MMA thread waits once
-// and commits once per K step.  At the group sizes of a prefill chunk the MMA
-// thread is the limit: an M=128 MMA occupies the tensor pipe for at least ~80
-// cycles whatever N <= 160, plus the thread's wait and commit.  A decode
-// warp reuses a stage after empty[(t - 4) % 8], a B producer a slot after
-// empty[(t - 5) % 8].  Two accumulators (TMEM columns 0 and 192, guarded by
-// acc_full / acc_empty) let the epilogue of one item overlap the main loop of
-// the next.
+//              warp % 4); down: warps 8-11 take the even K steps, 12-15 the
+//              odd ones; gate/up: warps 8-11 the item's first M tile, 12-15
+//              its second, every K step
+// K step t of the CTA's sequence uses an A stage (down: t % 4, TMEM columns
+// 384 + 32 s; gate/up: t % 2, columns 384 + 64 s + 32 u for M tile u), B slot
+// t % 5 (shared memory; five slots keep up to 120 KiB of token rows in flight
+// against the L2 latency of the row gathers) and the full/empty mbarrier pair
+// t % 8.  full[t % 8] completes once the decode warps of the K step and the B
+// side (the relay, or the TMA producer's expect_tx arrival and its bytes)
+// have arrived, so the MMA thread waits once and commits once per K step.
+// A decode warp reuses a stage after empty[t - stages], a B producer a slot
+// after empty[(t - 5) % 8].  Down: two accumulators (TMEM columns 0 and 192,
+// guarded by acc_full / acc_empty) let the epilogue of one item overlap the
+// main loop of the next.  Gate/up: the item's M tiles use both, each released
+// by the epilogue as soon as it is drained (the next item's first M tile
+// starts while the second still drains).
+// Measured limits: a single M=128 MMA occupies the tensor pipe for at least
+// ~80 cycles whatever N <= 160; with paired M tiles the gate/up K step is
+// bound by the decode warps (~1,100-1,300 cycles for 32 rows x 64 K each).
 //
 // Decoding is bound by shared-memory gathers of codewords, so the codebooks
 // sit in shared memory as fp16 (summed in fp16, then rounded once to bf16) in
@@ -110,6 +119,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemD = 0;                   // accumulator b: columns [PF_NMAX b, + PF_NMAX)
 constexpr uint32_t kTmemA = 2 * PF_NMAX;         // A stage s: columns [kTmemA + 32 s, + 32)
 static_assert(kTmemA + PF_NST * (PF_KC / 2) <= kTmemCols, "TMEM columns");
+// gate/up items pair two M tiles on one B slot: accumulator of M tile u at
+// columns [PF_NMAX u, + PF_NMAX), A stage s of M tile u at kTmemA + 64 s + 32 u
+constexpr int PF_NST_PAIR = 2;
+static_assert(kTmemA + PF_NST_PAIR * PF_KC <= kTmemCols, "TMEM columns (paired M tiles)");
 static_assert(PF_NBAR >= PF_NSLOT + 1 && PF_NBAR >= PF_NST + 1, "a barrier pair outlives its stage");
 static_assert(kSlotB % 1024 == 0 && OFF_ST % 1024 == 0, "swizzled slots start on 1 KiB");
 
@@ -117,9 +130,11 @@ constexpr int kLoaders = 64;                     // gate/up B producer threads (
 constexpr int kTmaRows = 32;                     // token rows per down B TMA box
 constexpr int kLoaderRows = 3;                   // token rows per producer thread (192 / 64)
 constexpr int kDecodeWarps = 8;                  // A producer warps (8-15)
-// full[] arrivals: one half's decode warps + the B side (the relay, or the
-// TMA producer's expect_tx arrival)
+// full[] arrivals: the decode warps of the K step (down: one half of them;
+// gate/up: all eight, four per M tile) + the B side (the relay, or the TMA
+// producer's expect_tx arrival)
 constexpr uint32_t kFullCount = kDecodeWarps / 2 + 1;
+constexpr uint32_t kFullCountPair = kDecodeWarps + 1;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: a bounded wait, never a hang
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -331,18 +346,17 @@ struct PfItem {
     bool valid;
 };
 
-// Cost of one item per K step, in units of ~7.7 cycles (one gathered token
-// row), fitted to timestamp traces of the 2048-token chunk:
-//  * gate/up (token rows gathered by cp.async): max(decode floor ~770
-//    cycles, ~240 + 7.7 per row);
+// Cost of one item per K step, in units of ~7.7 cycles, fitted to timestamp
+// traces of the 2048-token chunk:
+//  * gate/up (two M tiles, token rows gathered by cp.async): ~1,600 cycles
+//    of decoding plus ~3.9 per row, the epilogue between items included;
 //  * down (rows by TMA): ~800 cycles + ~1 per row, plus a start of ~3,000
 //    cycles spread over its 32 K steps.
 // CTAs get contiguous item ranges of equal total cost: item costs differ by
 // 2x or more across a Zipf-skewed chunk, and equal item counts left the
 // slowest CTA 1.5x behind the median.
 __device__ __forceinline__ int64_t pf_cost(const PfJob &job, int npad) {
-    return job.mode == PF_MODE_SWIGLU ? max((int64_t)112, (int64_t)32 + npad)
-                                      : (int64_t)116 + npad / 8;
+    return job.mode == PF_MODE_SWIGLU ? (int64_t)210 + npad / 2 : (int64_t)116 + npad / 8;
 }
 
 // Passes of expert e (0 when its group is below min_tokens) and their cost.
@@ -403,6 +417,8 @@ __device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, in
     return I;
 }
 
+// kPair: gate/up launch (two M tiles per item, SwiGLU epilogue); otherwise down.
+template <bool kPair>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_gemm_kernel(const PfJob job, const __grid_constant__ CUtensorMap tmap_b) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -416,9 +432,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     int32_t *Q = reinterpret_cast<int32_t *>(smem + OFF_Q);
     int64_t *W = reinterpret_cast<int64_t *>(smem + OFF_W);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool swiglu = job.mode == PF_MODE_SWIGLU;
-    const int MT = job.rows / job.tile_rows;
-    const int KS = job.cols / PF_KC;             // a multiple of 4: K step t uses stage t % 4
+    // gate/up: an item is a pair of M tiles sharing each K step's B slot
+    constexpr bool pair = kPair;
+    constexpr bool swiglu = kPair;
+    const int MT = job.rows / job.tile_rows / (pair ? 2 : 1);  // items per pass
+    constexpr int NST = pair ? PF_NST_PAIR : PF_NST;           // A stages: K step t uses t % NST
+    const int KS = job.cols / PF_KC;             // a multiple of 4
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -476,7 +495,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
         if (lane == 0) {
             for (int s = 0; s < PF_NBAR; ++s) {
-                mbar_init(bar(BAR_FULL + s), kFullCount);
+                mbar_init(bar(BAR_FULL + s), pair ? kFullCountPair : kFullCount);
                 mbar_init(bar(BAR_EMPTY + s), 1);
                 mbar_init(bar(BAR_LANDED + s), kLoaders);
             }
@@ -513,12 +532,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
                 const PfItem I = pf_item(job, Q, MT, it);
                 if (!I.valid) continue;
-                const uint32_t ab = nacc & 1u, use = nacc >> 1;
+                // down: two accumulators alternate over items; gate/up: an item
+                // uses both (one per M tile), each released by the epilogue on
+                // its own, so the next item starts on M tile 0 while the
+                // epilogue still drains M tile 1
+                const uint32_t ab = pair ? 0u : (nacc & 1u), use = pair ? nacc : (nacc >> 1);
                 if (!mbar_wait(bar(BAR_ACC_EMPTY + ab), (use & 1u) ^ 1u, abort_flag, job.status))
                     break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t idesc = idesc_bf16(PF_MROWS, I.npad);
-                const uint32_t td = tmem + kTmemD + ab * PF_NMAX;
                 bool ok = true;
                 for (int ks = 0; ks < KS; ++ks, ++kg) {
                     if (!mbar_wait_spin(bar(BAR_FULL + (kg & (PF_NBAR - 1))),
@@ -528,13 +550,34 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     }
                     // (the B producers fenced their slot writes into the async proxy)
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t ta = tmem + kTmemA + (kg & (PF_NST - 1)) * (PF_KC / 2);
                     // start-address field: +1 per 16 bytes (32 bytes per 16 K)
                     const uint64_t bd = bdesc0 + slot * (uint32_t)(kSlotB >> 4);
+                    if (pair) {
+                        const uint32_t ta = tmem + kTmemA + (kg & (PF_NST_PAIR - 1)) * PF_KC;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ts(td, ta + kk * 8, bd + 2 * kk, idesc,
-                                    (ks > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ts(tmem + kTmemD, ta + kk * 8, bd + 2 * kk, idesc,
+                                        (ks > 0 || kk > 0) ? 1u : 0u);
+                        if (ks == 0) {
+                            if (!mbar_wait_spin(bar(BAR_ACC_EMPTY + 1), (use & 1u) ^ 1u,
+                                                abort_flag, job.status)) {
+                                ok = false;
+                                break;
+                            }
+                            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ts(tmem + kTmemD + PF_NMAX, ta + 32 + kk * 8, bd + 2 * kk,
+                                        idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                    } else {
+                        const uint32_t ta = tmem + kTmemA + (kg & (PF_NST - 1)) * (PF_KC / 2);
+                        const uint32_t td = tmem + kTmemD + ab * PF_NMAX;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ts(td, ta + kk * 8, bd + 2 * kk, idesc,
+                                        (ks > 0 || kk > 0) ? 1u : 0u);
+                    }
                     mma_commit(bar(BAR_EMPTY + (kg & (PF_NBAR - 1))));
                     slot = slot == PF_NSLOT - 1 ? 0 : slot + 1;
                 }
@@ -698,15 +741,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 int p = j < I.n ? job.pairs[I.o + I.j0 + j] : -1;
                 pl[c] = (p >= 0 && p < job.n_pairs) ? p : -1;
             }
-            const uint32_t ab = nacc & 1u, use = nacc >> 1;
+            const uint32_t ab = pair ? 0u : (nacc & 1u), use = pair ? nacc : (nacc >> 1);
             if (!mbar_wait(bar(BAR_ACC_FULL + ab), use & 1u, abort_flag, job.status)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int R = I.mt * job.tile_rows + rin;
+            // gate/up: the item's two M tiles, accumulators 0 and 1, each
+            // released as soon as it is drained
+#pragma unroll 1
+            for (int mu = 0; mu < (pair ? 2 : 1); ++mu) {
+            const uint32_t acc = pair ? (uint32_t)mu : ab;
+            const int R = ((pair ? 2 * I.mt + mu : I.mt)) * job.tile_rows + rin;
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
                 if (32 * c >= I.n) break;
                 float a[32];
-                tmem_ld32(tl + ab * PF_NMAX + 32 * c, a);
+                tmem_ld32(tl + acc * PF_NMAX + 32 * c, a);
                 if (swiglu) {
                     // row of token t: its position in the grouped order
                     uint16_t *hrow = reinterpret_cast<uint16_t *>(job.out) +
@@ -730,14 +778,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + ab));
+            if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + acc));
+            }
             ++nacc;
         }
     } else {
         // ================= A producers (decode into TMEM) =================
         const int dt = tid - 256;
         const int quarter = warp & 3;            // TMEM lanes 32 quarter .. + 31
-        const int half = (warp - 8) >> 2;        // K steps t with t % 2 == half
+        // down: warps 8-11 take the even K steps, 12-15 the odd ones; gate/up:
+        // warps 8-11 decode the item's first M tile, 12-15 its second, every K step
+        const int half = pair ? 0 : (warp - 8) >> 2;
+        const int u = pair ? (warp - 8) >> 2 : 0;
+        constexpr int nj = pair ? 4 : 2;         // K steps of a 4-step group decoded here
         const int ar = quarter * 32 + lane;      // A row
         const int q = lane & 7;
         const int mat = swiglu ? (q >> 2) : 0;   // gate / up (down: both slots hold down)
@@ -781,12 +834,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 ++ncb;
                 cur_e = I.e;
             }
-            const int R = I.mt * job.tile_rows + rin;
+            const int R = (pair ? 2 * I.mt + u : I.mt) * job.tile_rows + rin;
             const int l = R & 31;
             // Chunk j of this row sits at byte (j - l) mod 32 of each stage
             // plane; rotating by l - 8 half puts chunks 8 half .. 8 half + 7 (K
             // step 4 g + half) in bytes 0..7 and chunks 8 half + 16 .. + 23 (K
-            // step 4 g + half + 2) in bytes 16..23.
+            // step 4 g + half + 2) in bytes 16..23 (gate/up: half 0, every
+            // chunk j at byte j).
             const int rot = (l - 8 * half) & 31;
             // this row's code planes of 32-chunk group g: 6 x 16 bytes (stage s, half h)
             const uint8_t *cp = rec + job.codes_off[mat] + (size_t)(R >> 5) * kTileBytes + l * 16;
@@ -817,12 +871,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         nxt[v] = *reinterpret_cast<const uint4 *>(cpn + v * 512);
                 }
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t kt = kg + 4 * g + 2 * j + half;  // this K step
-                    const uint32_t st = kt & (PF_NST - 1);
-                    // the stage's previous K step (4 back) has been consumed
-                    if (kt >= (uint32_t)PF_NST) {
-                        const uint32_t kp = kt - PF_NST;
+                for (int j = 0; j < nj; ++j) {
+                    // this K step, its A stage and its first code word
+                    const uint32_t kt = pair ? kg + 4 * g + j : kg + 4 * g + 2 * j + half;
+                    const uint32_t st = kt & (uint32_t)(NST - 1);
+                    const int w0 = pair ? 2 * j : 4 * j;
+                    const uint32_t tst = pair ? st * PF_KC + 32 * u : st * (PF_KC / 2);
+                    // the stage's previous K step (NST back) has been consumed
+                    if (kt >= (uint32_t)NST) {
+                        const uint32_t kp = kt - NST;
                         if (!mbar_wait(bar(BAR_EMPTY + (kp & (PF_NBAR - 1))),
                                        (kp / PF_NBAR) & 1u, abort_flag, job.status)) {
                             ok = false;
@@ -835,8 +892,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         uint32_t o[8];
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
-                            // chunk 2 hq + c of the K step: word 4 j + hq / 2, byte 2 (hq % 2) + c
-                            const int w = 4 * j + (hq >> 1), b = 8 * (2 * (hq & 1) + c);
+                            // chunk 2 hq + c of the K step: word w0 + hq / 2, byte 2 (hq % 2) + c
+                            const int w = w0 + (hq >> 1), b = 8 * (2 * (hq & 1) + c);
                             const uint32_t k0 = (U[0][w] >> b) & 0xFFu;
                             const uint32_t k1 = (U[1][w] >> b) & 0xFFu;
                             const uint32_t k2 = (U[2][w] >> b) & 0xFFu;
@@ -848,7 +905,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                             o[4 * c + 2] = sum3_bf16x2(w0.z, w1.z, w2.z);
                             o[4 * c + 3] = sum3_bf16x2(w0.w, w1.w, w2.w);
                         }
-                        tmem_st8(ta + st * (PF_KC / 2) + 8 * hq, o);
+                        tmem_st8(ta + tst + 8 * hq, o);
                     }
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -894,14 +951,18 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {
-        RVQ_CUDA(cudaFuncSetAttribute(prefill_gemm_kernel,
+        RVQ_CUDA(cudaFuncSetAttribute(prefill_gemm_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem));
+        RVQ_CUDA(cudaFuncSetAttribute(prefill_gemm_kernel<false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem));
         attr_done[dev] = 1;
     }
     // gate/up items cover 64 weight rows of each matrix, down items 128 rows
     const int want_rows = job.mode == PF_MODE_SWIGLU ? PF_MROWS / 2 : PF_MROWS;
+    // gate/up items take two M tiles
+    const int tile_mult = job.mode == PF_MODE_SWIGLU ? 2 * job.tile_rows : job.tile_rows;
     if ((job.mode != PF_MODE_SWIGLU && job.mode != PF_MODE_PLAIN) || job.tile_rows != want_rows ||
-        job.rows % job.tile_rows || job.cols % (4 * PF_KC) || job.E < 1 || job.E > kMaxE ||
+        job.rows % tile_mult || job.cols % (4 * PF_KC) || job.E < 1 || job.E > kMaxE ||
         job.min_tokens < 1) {
         set_error("prefill: rows %d / cols %d / tile %d / E %d not supported", job.rows, job.cols,
                   job.tile_rows, job.E);
@@ -948,7 +1009,10 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    RVQ_CUDA(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel, job, tmap));
+    if (job.mode == PF_MODE_SWIGLU)
+        RVQ_CUDA(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<true>, job, tmap));
+    else
+        RVQ_CUDA(cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<false>, job, tmap));
     return RVQ_OK;
 }
 
