@@ -56,6 +56,7 @@ def _load():
                 "oracle_rms_norm": (None, [vp, i32, i32, ctypes.c_double, vp]),
                 "oracle_moe_layer": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp, vp]),
+                "oracle_crc32": (ctypes.c_uint32, [vp, ctypes.c_size_t]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -220,3 +221,11 @@ def moe_layer(experts, wr, x, k, d, f, bias=None, route_logits=None):
     del keep
     return dict(logits=lg, logits_used=logits_used, idx=topk_idx, w=topk_w,
                 y_pair=y_pair, out=out, rc=int(rc))
+
+
+def crc32(data) -> int:
+    """CRC-32 (ISO-HDLC: reflected 0xEDB88320, preset and final complement)
+    of a byte buffer, one bit per step."""
+    b = np.ascontiguousarray(np.frombuffer(bytes(data), np.uint8) if isinstance(data, (bytes, bytearray))
+                             else np.asarray(data, dtype=np.uint8).reshape(-1))
+    return int(_load().oracle_crc32(b.ctypes.data if b.size else None, b.size))

@@ -291,3 +291,19 @@ int32_t oracle_moe_layer(const uint8_t *const *codes, const float *const *cbs,
     oracle_combine(y_pair, topk_w, n, k, d, x, out);
     return rc;
 }
+
+/* CRC-32 of n bytes: the checksum the pages offer as an opt-in check of each
+ * expert record's payload [GN, "Disk streaming structure"].  The pages do not
+ * name the variant; this is the common CRC-32 (ISO-HDLC / IEEE 802.3):
+ * reflected polynomial 0xEDB88320, register preset to all ones, bytes taken
+ * least significant bit first, result complemented.  One bit per step. */
+uint32_t oracle_crc32(const uint8_t *p, size_t n)
+{
+    uint32_t crc = 0xFFFFFFFFu;
+    for (size_t i = 0; i < n; ++i) {
+        crc ^= p[i];
+        for (int b = 0; b < 8; ++b)
+            crc = (crc & 1u) ? (crc >> 1) ^ 0xEDB88320u : crc >> 1;
+    }
+    return ~crc;
+}

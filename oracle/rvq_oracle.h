@@ -5,6 +5,7 @@
  */
 #ifndef RVQ_ORACLE_H
 #define RVQ_ORACLE_H
+#include <stddef.h>
 #include <stdint.h>
 
 void oracle_rvq_dequant_row(const uint8_t *codes, const float *cb, int32_t cols,
@@ -36,4 +37,5 @@ int32_t oracle_moe_layer(const uint8_t *const *codes, const float *const *cbs,
                          const double *x, const float *route_logits,
                          float *logits_used, int32_t *topk_idx, float *topk_w,
                          double *y_pair, double *out);
+uint32_t oracle_crc32(const uint8_t *p, size_t n);
 #endif

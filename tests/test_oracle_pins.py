@@ -379,3 +379,30 @@ def test_rms_norm_invariants():
     assert np.allclose(oracle.rms_norm(3.7 * x, eps=0.0), y, rtol=1e-13)
     assert np.allclose(oracle.rms_norm(-x, eps=0.0), -y, rtol=0, atol=0)
     assert np.allclose(oracle.rms_norm(x[2:3], eps=0.0), y[2:3], rtol=0, atol=0)
+
+
+# ------------------------------------------------------------ record checksum
+
+def test_crc32_check_value():
+    """The catalogued check value of CRC-32/ISO-HDLC: the nine ASCII bytes
+    "123456789" give 0xCBF43926."""
+    assert oracle.crc32(b"123456789") == 0xCBF43926
+    assert oracle.crc32(b"") == 0
+
+
+@pytest.mark.parametrize("n", [1, 7, 128, 4096, 100003])
+def test_crc32_matches_zlib(n):
+    """Library special case: zlib's crc32 is the same code."""
+    import zlib
+    data = np.random.default_rng(n).integers(0, 256, size=n, dtype=np.uint8)
+    assert oracle.crc32(data) == zlib.crc32(data.tobytes())
+
+
+def test_crc32_sees_every_single_bit_flip():
+    data = np.random.default_rng(5).integers(0, 256, size=3000, dtype=np.uint8)
+    ref = oracle.crc32(data)
+    for pos in (0, 1, 1499, 2998, 2999):
+        for bit in (0, 3, 7):
+            d = data.copy()
+            d[pos] ^= np.uint8(1 << bit)
+            assert oracle.crc32(d) != ref
