@@ -170,6 +170,7 @@ rvq_status rvq_gemv_noalloc(const uint8_t *packed_codes_dev, const float *packed
  * of one expert are adjacent, as in the pages' one-read expert record.
  * ------------------------------------------------------------------------ */
 #define RVQ_BANK_MAGIC 0x31515652u /* "RVQ1" little-endian */
+#define RVQ_HDR_FLAG_CRC32 0x1u    /* header crc32 holds the payload checksum  */
 
 typedef struct rvq_expert_header {
     uint32_t magic;        /* RVQ_BANK_MAGIC                                  */
@@ -177,8 +178,8 @@ typedef struct rvq_expert_header {
     int32_t layer;         /* layer id given to moe_bank_init                 */
     int32_t expert;        /* expert id == record index                       */
     int32_t d, f;          /* hidden and intermediate size                    */
-    uint32_t flags;        /* 0                                               */
-    uint32_t crc32;        /* 0 (payload checksum not computed)               */
+    uint32_t flags;        /* RVQ_HDR_FLAG_CRC32 once sealed, else 0          */
+    uint32_t crc32;        /* payload checksum once sealed (moe_bank_seal)    */
     uint64_t cb_off;       /* byte offsets from the record start             */
     uint64_t gate_off, up_off, down_off;
     uint64_t record_bytes;
@@ -211,6 +212,25 @@ rvq_status moe_bank_write_expert(const rvq_moe_bank *bank, int32_t expert,
  * version, layer, expert id, shape and offset ranges.  ECORRUPT on mismatch
  * (message names the first bad record). */
 rvq_status moe_bank_validate(const rvq_moe_bank *bank, rvq_stream_t stream);
+
+/* Payload checksums: the pages' opt-in CRC check of each expert record
+ * (GeekNews topic 32035, "Disk streaming structure").  CRC-32 (ISO-HDLC:
+ * reflected polynomial 0xEDB88320, register preset to all ones, result
+ * complemented) over each record's bytes [128, record_bytes), computed on the
+ * device, one block per record.  Both calls are asynchronous on `stream`.
+ *  - moe_bank_seal writes the value to every header (crc32) and sets
+ *    RVQ_HDR_FLAG_CRC32.  Seal after the last moe_bank_write_expert (a write
+ *    replaces the header and so clears the seal of that record).
+ *  - moe_bank_verify recomputes it.  crc_dev (uint32 [n_experts], dev, or
+ *    NULL) receives the computed values; a sealed record whose value differs
+ *    sets RVQ_DEV_ERR_CORRUPT in the status word of ws_dev (ws_bytes >=
+ *    RVQ_WS_STATUS_BYTES; read it with rvq_ws_status; the call does not clear
+ *    it).  Unsealed records are only reported in crc_dev.
+ * One pass reads the whole bank (4.2 GB for 256 K3-shaped experts), so the
+ * check is an explicit pass, not part of the layer call. */
+rvq_status moe_bank_seal(const rvq_moe_bank *bank, rvq_stream_t stream);
+rvq_status moe_bank_verify(const rvq_moe_bank *bank, uint32_t *crc_dev, void *ws_dev,
+                           size_t ws_bytes, rvq_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * Router.  logits[t][e] = sum_c Wr[e][c] * x[t][c] (+ bias[e]), fp32

@@ -21,6 +21,7 @@ RVQ_F32, RVQ_BF16 = 0, 1
 RVQ_WS_STATUS_BYTES = 256
 RVQ_CODEBOOK_BYTES = 24576
 RVQ_BANK_MAGIC = 0x31515652
+RVQ_HDR_FLAG_CRC32 = 0x1
 MOE_LAYER_EVENTS = 8
 DEV_ERR_INDEX, DEV_ERR_NONFINITE, DEV_ERR_CORRUPT, DEV_ERR_TIMEOUT = 1, 2, 4, 8
 STATUS = {0: "RVQ_OK", 1: "RVQ_EINVAL", 2: "RVQ_EALIGN", 3: "RVQ_ENOMEM", 4: "RVQ_ECORRUPT",
@@ -64,6 +65,8 @@ _SIGS = {
     "moe_bank_init": (_i32, [_BANKP, _vp, _u64, _i32, _i32, _i32, _i32]),
     "moe_bank_write_expert": (_i32, [_BANKP, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_bank_validate": (_i32, [_BANKP, _vp]),
+    "moe_bank_seal": (_i32, [_BANKP, _vp]),
+    "moe_bank_verify": (_i32, [_BANKP, _vp, _vp, _sz, _vp]),
     "moe_router_logits": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "moe_route_max_tokens": (_i32, [_i32]),
     "moe_route": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -211,6 +214,15 @@ def moe_bank_write_expert(bank, expert, gate_codes, up_codes, down_codes, codebo
 
 def moe_bank_validate(bank, stream=None):
     _check("moe_bank_validate", _lib.moe_bank_validate(ctypes.byref(bank), _stream(stream)))
+
+
+def moe_bank_seal(bank, stream=None):
+    _check("moe_bank_seal", _lib.moe_bank_seal(ctypes.byref(bank), _stream(stream)))
+
+
+def moe_bank_verify(bank, crc, ws, stream=None):
+    _check("moe_bank_verify", _lib.moe_bank_verify(ctypes.byref(bank), _p(crc), _p(ws),
+                                                   _nbytes(ws), _stream(stream)))
 
 
 # ------------------------------------------------------------------ MoE calls

@@ -357,6 +357,24 @@ rvq_status moe_bank_validate(const rvq_moe_bank *bank, rvq_stream_t stream) {
     return RVQ_OK;
 }
 
+rvq_status moe_bank_seal(const rvq_moe_bank *bank, rvq_stream_t stream) {
+    RVQ_TRY(check_bank(bank, "moe_bank_seal"));
+    return launch_record_crc(bank->base, bank->record_bytes, bank->n_experts, 1, nullptr, nullptr,
+                             (cudaStream_t)stream);
+}
+
+rvq_status moe_bank_verify(const rvq_moe_bank *bank, uint32_t *crc_dev, void *ws_dev,
+                           size_t ws_bytes, rvq_stream_t stream) {
+    RVQ_TRY(check_bank(bank, "moe_bank_verify"));
+    CHECK_ARG(ws_dev, "moe_bank_verify: null workspace");
+    if (ws_bytes < RVQ_WS_STATUS_BYTES) {
+        set_error("moe_bank_verify: workspace %zu < %u", ws_bytes, RVQ_WS_STATUS_BYTES);
+        return RVQ_ENOMEM;
+    }
+    return launch_record_crc(bank->base, bank->record_bytes, bank->n_experts, 0, crc_dev,
+                             (uint32_t *)ws_dev, (cudaStream_t)stream);
+}
+
 rvq_status moe_router_logits(const float *wr_dev, const float *bias_dev, const void *x_dev,
                              rvq_dtype xdt, int32_t n, int32_t E, int32_t d, float *logits_dev,
                              rvq_stream_t stream) {

@@ -202,6 +202,9 @@ struct PfJob {
     int32_t selftest_stall;    // 1: the MMA role first waits for an arrival nothing makes
 };
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
+// CRC-32 of each record's payload: mode 1 seals the headers, mode 0 verifies
+rvq_status launch_record_crc(uint8_t *base, uint64_t record_bytes, int n_records, int mode,
+                             uint32_t *crc_out, uint32_t *status, cudaStream_t stream);
 // cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000) or null
 void *tensor_map_encoder_entry();
 // tensor-core router logits (bf16 tokens, n >= 128, E % 128 == 0, d % 256 == 0):
