@@ -55,6 +55,7 @@ WORKLOADS = {
     "k3_stack8_b1": (3, 1),
     "k3_stack8_b32": (3, 32),
     "k3_prefill512_e64": (4, 512, 64),  # profiling case: ~128 tokens per expert, 1.06 GB bank
+    "k3_stack8_prefill2048": (5, 2048),
 }
 KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
            "lut_gemv_down", "combine"]
@@ -183,7 +184,7 @@ def workload_shape(name):
 
 def router_bias(config, src):
     wl = W.WORKLOADS[config]
-    if wl.kind != "prefill":
+    if not wl.is_prefill:
         return None
     return W.zipf_bias(src.lseed, src.shape.E, wl.zipf_beta)
 
@@ -226,12 +227,12 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     config, batch, s = workload_shape(args.workload)
-    prefill = W.WORKLOADS[config].kind == "prefill"
+    prefill = W.WORKLOADS[config].is_prefill
     tc_min = 1 if prefill else 0
     if args.tc_min_tokens is not None:
         tc_min = args.tc_min_tokens
     kernels = KERNELS_TC if tc_min > 0 else KERNELS
-    n_layers = W.WORKLOADS[config].layers if W.WORKLOADS[config].kind == "stack" else 1
+    n_layers = W.WORKLOADS[config].n_layers
     built = [build_layer(config, dev, shape=s, layer=i) for i in range(n_layers)]
     L, src = built[0]
     from moe_expert_ffn_router_gb300.layer import MoeStack
@@ -442,7 +443,7 @@ def reference_arm(args, rank):
     x64 = synth.bf16_to_f32(src.tokens_bf16(ntok)).astype(np.float64)
     idx, _, _ = oracle.route(oracle.router_logits(wr, x64, bias).astype(np.float32), s.k)
     work = [(t, int(e)) for t in range(ntok) for e in idx[t]]
-    layers = W.WORKLOADS[config].layers if W.WORKLOADS[config].kind == "stack" else 1
+    layers = W.WORKLOADS[config].n_layers
     # distinct experts per batch: exact for one token; for a stack the first
     # layer's count stands for every layer (independent seeds, same shape)
     uniq = layers * (s.k if batch == 1 else oracle_unique_experts(config, batch, src, s))

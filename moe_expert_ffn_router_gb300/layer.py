@@ -128,6 +128,12 @@ class MoeStack:
     def buffers(self, n: int) -> list[dict]:
         b = self._bufs.get(n)
         if b is None:
+            # the layers run one after another on one stream, so they share
+            # one workspace (24 GB per K3-shaped layer at 2048 tokens)
+            ws = self.layers[0].workspace(n)
+            for L in self.layers[1:]:
+                if moe_workspace_bytes(L.bank, n, L.k) <= ws.numel():
+                    L._ws[n] = ws
             b = [L.buffers(n) for L in self.layers]
             for L, bl in zip(self.layers, b):
                 bl["xn"] = torch.empty((n, L.d), dtype=torch.bfloat16, device=L.device)

@@ -91,7 +91,7 @@ class LayerShape:
 class Workload:
     config: int
     name: str
-    kind: str                       # "gemv" | "layer" | "stack" | "prefill"
+    kind: str                       # "gemv" | "layer" | "stack" | "prefill" | "stack_prefill"
     shape: LayerShape | None = None
     rows: int = 0                   # gemv only
     cols: int = 0                   # gemv only
@@ -99,6 +99,15 @@ class Workload:
     layers: int = 1
     zipf_beta: float = 0.0          # prefill only
     notes: str = field(default="", compare=False)
+
+    @property
+    def is_prefill(self) -> bool:
+        """A prefill chunk: Zipf-biased router, tensor-core experts."""
+        return self.kind in ("prefill", "stack_prefill")
+
+    @property
+    def n_layers(self) -> int:
+        return self.layers if self.kind in ("stack", "stack_prefill") else 1
 
 
 # Bias strength for the prefill chunk: chosen once so that the 2048 seeded
@@ -117,6 +126,11 @@ WORKLOADS = {
                 LayerShape(7168, 2048, 256, 16), batches=(1, 32), layers=8),
     4: Workload(4, "k3_prefill2048_d7168_f2048_e256_k16_zipf1.1", "prefill",
                 LayerShape(7168, 2048, 256, 16), batches=(2048,),
+                zipf_beta=PREFILL_ZIPF_BETA),
+    # the chunked prefill of the pages (chunks of tokens through the layers)
+    # on the 8-layer stack: config 4's chunk, each layer its own seeds and bias
+    5: Workload(5, "k3_stack8_prefill2048_d7168_f2048_e256_k16_zipf1.1", "stack_prefill",
+                LayerShape(7168, 2048, 256, 16), batches=(2048,), layers=8,
                 zipf_beta=PREFILL_ZIPF_BETA),
 }
 

@@ -71,3 +71,51 @@ def test_k3_stack_two_layers(n, sample):
         sl.forget()
     del stack, bufs
     torch.cuda.empty_cache()
+
+
+def test_k3_prefill_chunk_through_two_layers():
+    """The chunked prefill of the stack (config 5: 2048-token chunks, each
+    layer its own seeds and Zipf router bias, every expert on the tensor
+    cores): per layer the norm within bf16 rounding, routing and grouping
+    bit-exact given the GPU's logits (tensor-core router), logits within
+    1e-5 x RMS, and sampled token outputs within 2e-2 x RMS of the oracle
+    layer fed the same normalised input.  Layers share one workspace."""
+    from moe_expert_ffn_router_gb300.layer import MoeStack
+    torch.cuda.empty_cache()
+    wl = W.WORKLOADS[5]
+    n, sample = 2048, [0, 1023, 2047]
+    sls = [SynthLayer(5, layer) for layer in range(2)]
+    biases = [W.zipf_bias(sl.src.lseed, sl.shape.E, wl.zipf_beta) for sl in sls]
+    stack = MoeStack([sl.to_gpu(bias=b) for sl, b in zip(sls, biases)])
+    s = sls[0].shape
+    bits = sls[0].tokens_bf16(n)
+    x = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    bufs = stack.forward(x, tc_min_tokens=1)
+    torch.cuda.synchronize()
+    assert bufs[0]["ws"].data_ptr() == bufs[1]["ws"].data_ptr()
+    for L in stack.layers:
+        assert L.status(n) == (0, 0)
+    h = bf16_bits_to_f64(bits)
+    for i, (sl, bias, b) in enumerate(zip(sls, biases, bufs)):
+        xn = b["xn"].float().cpu().numpy().astype(np.float64)
+        ref_xn = oracle.rms_norm(h, eps=stack.eps)
+        assert np.all(np.abs(xn - ref_xn) <= 2.0 ** -8 * np.abs(ref_xn) + 1e-6), f"layer {i} norm"
+        logits = b["logits"].cpu().numpy()
+        idx = b["idx"].cpu().numpy()
+        ridx, _, _ = oracle.route(logits, s.k)
+        assert np.array_equal(idx, ridx), f"layer {i} routing"
+        roff, rpairs = oracle.group(ridx, s.E)
+        assert np.array_equal(b["offsets"].cpu().numpy(), roff)
+        assert np.array_equal(b["pairs"].cpu().numpy(), rpairs)
+        assert_rms_close(logits, oracle.router_logits(sl.wr, xn, bias), 1e-5, f"layer {i} logits")
+        out = b["out"].cpu().numpy().astype(np.float64)
+        assert np.isfinite(out).all()
+        for t in sample:
+            r = oracle.moe_layer(sl.expert, sl.wr, xn[t:t + 1], s.k, s.d, s.f, bias=bias,
+                                 route_logits=logits[t:t + 1])
+            delta = r["out"][0] - xn[t]
+            assert_rms_close(out[t] - h[t], delta, 2e-2, f"layer {i} token {t}")
+        h = out
+        sl.forget()
+    del stack, bufs
+    torch.cuda.empty_cache()
