@@ -233,6 +233,66 @@ rvq_status moe_bank_verify(const rvq_moe_bank *bank, uint32_t *crc_dev, void *ws
                            size_t ws_bytes, rvq_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * Tiered expert store: the pages' streaming engine with host memory in place
+ * of NVMe ("Running a 2.78-Trillion-Parameter Model on a Laptop", "Technical
+ * Insight"; GeekNews topic 32035, "Read-ahead and router prediction").  A
+ * host-resident bank holds every layer's expert records; an HBM cache of
+ * record slots holds recently used ones, keyed by (layer, expert), least
+ * recently used replaced first.
+ *  - host_bank: pinned host memory (cudaHostAlloc or registered), records
+ *    [layer][expert], moe_bank_record_bytes(d, f) each, byte-identical to a
+ *    device bank written by moe_bank_write_expert (copy one over).
+ *  - slots_dev: device buffer (256-byte aligned) of slots_bytes; it holds
+ *    slots_bytes / record_bytes slots.
+ *  - slot_map_dev: int32 [n_layers][n_experts] (dev), kept by the cache: the
+ *    slot of each resident record, -1 otherwise.  The kernels address records
+ *    through it and still check every header (expert id, layer), so a record
+ *    that is not resident is reported (RVQ_DEV_ERR_CORRUPT), never used.
+ * The cache owns host-side state; calls on one cache must not overlap.
+ * ------------------------------------------------------------------------ */
+typedef struct rvq_expert_cache rvq_expert_cache;
+typedef struct rvq_cache_stats {
+    uint64_t hits;          /* routed experts found resident                  */
+    uint64_t misses;        /* routed experts copied in on demand             */
+    uint64_t prefetched;    /* records copied in by router lookahead          */
+    uint64_t prefetch_used; /* of those, later routed while still resident    */
+    uint64_t bytes_copied;  /* host -> HBM record bytes                       */
+    int32_t slots;
+    int32_t pad;
+} rvq_cache_stats;
+rvq_status moe_cache_create(rvq_expert_cache **cache, const uint8_t *host_bank, int32_t n_layers,
+                            int32_t n_experts, int32_t d, int32_t f, uint8_t *slots_dev,
+                            uint64_t slots_bytes, int32_t *slot_map_dev);
+rvq_status moe_cache_destroy(rvq_expert_cache *cache);
+rvq_status moe_cache_stats(const rvq_expert_cache *cache, rvq_cache_stats *stats);
+/* The bank view of layer `layer` (base = the slots), e.g. for
+ * moe_workspace_bytes. */
+rvq_status moe_cache_bank(const rvq_expert_cache *cache, int32_t layer, rvq_moe_bank *bank);
+/* One MoE layer on cached records.  Synchronous on the host: after routing it
+ * reads the expert counts back to decide the copies.  Router logits -> top-k
+ * and grouping -> the routed experts made resident (misses copied
+ * host -> HBM on copy_stream; `stream` waits for the slots it needs) ->
+ * expert FFN on the cached records (lookup tables; tensor cores for groups of
+ * >= tc_min_tokens when > 0) -> combine + residual.  Other arguments as in
+ * moe_layer_forward_ex, with ws_bytes >= moe_workspace_bytes of the cache's
+ * bank view.  Router lookahead: with next_wr_dev non-NULL and lookahead > 0,
+ * the next layer's router (next_wr_dev, next_bias_dev) runs on this layer's
+ * input (next_logits_dev: fp32 [n][n_experts] scratch, dev), and each
+ * token's `lookahead` highest-scoring experts of the next layer are copied in
+ * while this layer's FFN runs (never replacing this layer's records; skipped
+ * when no slot is free).  ENOMEM when this layer's experts do not fit. */
+rvq_status moe_layer_forward_streamed(rvq_expert_cache *cache, int32_t layer,
+                                      const float *wr_dev, const float *bias_dev,
+                                      const void *x_dev, rvq_dtype xdt, int32_t n, int32_t k,
+                                      float *logits_dev, int32_t *topk_idx_dev, float *topk_w_dev,
+                                      int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
+                                      void *ws_dev, size_t ws_bytes, const void *residual_dev,
+                                      rvq_dtype rdt, int32_t tc_min_tokens,
+                                      const float *next_wr_dev, const float *next_bias_dev,
+                                      int32_t lookahead, float *next_logits_dev,
+                                      rvq_stream_t stream, rvq_stream_t copy_stream);
+
+/* --------------------------------------------------------------------------
  * Router.  logits[t][e] = sum_c Wr[e][c] * x[t][c] (+ bias[e]), fp32
  * accumulate.  Wr fp32 [E][d] (dev); bias fp32 [E] (dev) or NULL; x [n][d]
  * of xdt (dev); logits fp32 [n][E] (dev).  1 <= E <= 256, d % 8 == 0.

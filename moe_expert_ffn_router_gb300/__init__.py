@@ -41,6 +41,13 @@ class RvqMoeBank(ctypes.Structure):
                 ("f", ctypes.c_int32), ("layer", ctypes.c_int32)]
 
 
+class RvqCacheStats(ctypes.Structure):
+    _fields_ = [("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
+                ("prefetched", ctypes.c_uint64), ("prefetch_used", ctypes.c_uint64),
+                ("bytes_copied", ctypes.c_uint64), ("slots", ctypes.c_int32),
+                ("pad", ctypes.c_int32)]
+
+
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; "
                       "g.build()'` (nvcc, sm_103a)")
@@ -66,6 +73,14 @@ _SIGS = {
     "moe_bank_write_expert": (_i32, [_BANKP, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_bank_validate": (_i32, [_BANKP, _vp]),
     "moe_bank_seal": (_i32, [_BANKP, _vp]),
+    "moe_cache_create": (_i32, [ctypes.POINTER(_vp), _vp, _i32, _i32, _i32, _i32, _vp, _u64,
+                                _vp]),
+    "moe_cache_destroy": (_i32, [_vp]),
+    "moe_cache_stats": (_i32, [_vp, ctypes.POINTER(RvqCacheStats)]),
+    "moe_cache_bank": (_i32, [_vp, _i32, _BANKP]),
+    "moe_layer_forward_streamed": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
+                                          _vp, _vp, _vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp,
+                                          _vp, _i32, _vp, _vp, _vp]),
     "moe_bank_verify": (_i32, [_BANKP, _vp, _vp, _sz, _vp]),
     "moe_router_logits": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "moe_route_max_tokens": (_i32, [_i32]),
@@ -218,6 +233,47 @@ def moe_bank_validate(bank, stream=None):
 
 def moe_bank_seal(bank, stream=None):
     _check("moe_bank_seal", _lib.moe_bank_seal(ctypes.byref(bank), _stream(stream)))
+
+
+def moe_cache_create(host_bank, n_layers, n_experts, d, f, slots, slot_map) -> int:
+    """host_bank: pinned uint8 tensor of n_layers x n_experts records; slots:
+    device uint8 tensor; slot_map: device int32 [n_layers][n_experts].
+    Returns the cache handle (an address)."""
+    h = _vp()
+    _check("moe_cache_create",
+           _lib.moe_cache_create(ctypes.byref(h), _p(host_bank), n_layers, n_experts, d, f,
+                                 _p(slots), _nbytes(slots), _p(slot_map)))
+    return h.value
+
+
+def moe_cache_destroy(cache):
+    _check("moe_cache_destroy", _lib.moe_cache_destroy(cache))
+
+
+def moe_cache_stats(cache) -> dict:
+    st = RvqCacheStats()
+    _check("moe_cache_stats", _lib.moe_cache_stats(cache, ctypes.byref(st)))
+    return {k: int(getattr(st, k)) for k, _ in RvqCacheStats._fields_ if k != "pad"}
+
+
+def moe_cache_bank(cache, layer) -> RvqMoeBank:
+    bank = RvqMoeBank()
+    _check("moe_cache_bank", _lib.moe_cache_bank(cache, layer, ctypes.byref(bank)))
+    return bank
+
+
+def moe_layer_forward_streamed(cache, layer, wr, bias, x, n, k, logits, topk_idx, topk_w,
+                               offsets, pairs, out, ws, residual=None, tc_min_tokens=0,
+                               next_wr=None, next_bias=None, lookahead=0, next_logits=None,
+                               stream=None, copy_stream=None):
+    rdt = _dt(residual) if residual is not None else _dt(x)
+    cs = copy_stream.cuda_stream if copy_stream is not None else _stream(stream)
+    _check("moe_layer_forward_streamed",
+           _lib.moe_layer_forward_streamed(
+               cache, layer, _p(wr), _p(bias), _p(x), _dt(x), n, k, _p(logits), _p(topk_idx),
+               _p(topk_w), _p(offsets), _p(pairs), _p(out), _p(ws), _nbytes(ws), _p(residual),
+               rdt, tc_min_tokens, _p(next_wr), _p(next_bias), lookahead, _p(next_logits),
+               _stream(stream), cs))
 
 
 def moe_bank_verify(bank, crc, ws, stream=None):

@@ -418,8 +418,11 @@ size_t moe_workspace_bytes(const rvq_moe_bank *bank, int32_t n, int32_t k) {
     return plan_ffn(bank->d, bank->f, n * k, bank->n_experts, n).total;
 }
 
-static LutJob ffn_job(const rvq_moe_bank *bank, const RecordLayout &L, int n_pairs, void *ws) {
+static LutJob ffn_job(const rvq_moe_bank *bank, const RecordLayout &L, int n_pairs, void *ws,
+                      const int32_t *slot_of, int32_t n_records) {
     LutJob j = {};
+    j.slot_of = slot_of;
+    j.n_records = n_records;
     j.base = bank->base;
     j.record_bytes = bank->record_bytes;
     j.E = bank->n_experts;
@@ -433,12 +436,14 @@ static LutJob ffn_job(const rvq_moe_bank *bank, const RecordLayout &L, int n_pai
     return j;
 }
 
+}  // extern "C"
+
 // item plan -> gate/up LUT-GEMV -> SwiGLU reduction -> down LUT-GEMV; `marks`
 // (4 events or NULL) are recorded after each kernel.
-static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
-                          int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
-                          void *ws_dev, const FfnPlan &P, cudaStream_t st, void **marks,
-                          bool pdl, int32_t tc_min_tokens = 0) {
+rvq_status rvq::run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
+                   int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev, void *ws_dev,
+                   const FfnPlan &P, cudaStream_t st, void **marks, bool pdl,
+                   int32_t tc_min_tokens, const int32_t *slot_of, int32_t n_records) {
     auto mark = [&](int i) -> rvq_status {
         if (marks) RVQ_CUDA(cudaEventRecord((cudaEvent_t)marks[i], st));
         return RVQ_OK;
@@ -451,7 +456,7 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     float *h = (float *)(ws + P.off_h);
     float *dpart = (float *)(ws + P.off_dpart);
 
-    LutJob gu = ffn_job(bank, L, np, ws_dev);
+    LutJob gu = ffn_job(bank, L, np, ws_dev, slot_of, n_records);
     gu.codes_off[0] = L.gate_off;
     gu.codes_off[1] = L.up_off;
     gu.cb_off[0] = L.cb_off;
@@ -472,7 +477,7 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
     gu.pairs = pairs_dev;
     gu.desc = (ItemDesc *)(ws + P.off_desc_gu);
 
-    LutJob dn = ffn_job(bank, L, np, ws_dev);
+    LutJob dn = ffn_job(bank, L, np, ws_dev, slot_of, n_records);
     dn.codes_off[0] = L.down_off;
     dn.cb_off[0] = L.cb_off + 2 * RVQ_CODEBOOK_BYTES;
     dn.part[0] = dpart;
@@ -519,14 +524,17 @@ static rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
 // Tensor-core (prefill) path for experts with at least tc_min_tokens tokens:
 // gate/up GEMMs with the SwiGLU epilogue into h (bf16), then the down GEMM
 // writing y fp32 [pair][d] for those experts' pairs.
-static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
-                             int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
-                             void *ws_dev, const FfnPlan &P, float *y_pair, int32_t tc_min_tokens,
-                             cudaStream_t st, bool pdl, void *mid_event = nullptr) {
+rvq_status rvq::run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
+                      int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
+                      void *ws_dev, const FfnPlan &P, float *y_pair, int32_t tc_min_tokens,
+                      cudaStream_t st, bool pdl, void *mid_event, const int32_t *slot_of,
+                      int32_t n_records) {
     const RecordLayout L = record_layout(bank->d, bank->f);
     uint8_t *ws = (uint8_t *)ws_dev;
     PfJob g = {};
     g.base = bank->base;
+    g.slot_of = slot_of;
+    g.n_records = n_records;
     g.record_bytes = bank->record_bytes;
     g.codes_off[0] = L.gate_off;
     g.codes_off[1] = L.up_off;
@@ -566,6 +574,8 @@ static rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dt
     dn.out = y_pair;
     return launch_prefill_gemm(dn, st, pdl);
 }
+
+extern "C" {
 
 static rvq_status check_ffn_args(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
                                  int32_t n, int32_t k, void *ws_dev, size_t ws_bytes,

@@ -144,6 +144,10 @@ struct LutJob {
     // so the first table's codebook and code tiles are requested before the
     // dependency wait
     int32_t early_start;
+    // expert cache: record index of expert e = slot_of[e] (< n_records), or
+    // -1 when not resident; NULL: record e
+    const int32_t *slot_of;
+    int32_t n_records;
 };
 
 __host__ __device__ inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
@@ -200,7 +204,18 @@ struct PfJob {
     uint32_t *status;
     int32_t layer, d, f;       // record header check
     int32_t selftest_stall;    // 1: the MMA role first waits for an arrival nothing makes
+    const int32_t *slot_of;    // expert cache (as in LutJob); NULL: record e
+    int32_t n_records;
 };
+
+// Record index of expert e in the job's bank: its cache slot, or e itself;
+// -1 when a cached expert has no valid slot (the caller flags the record).
+template <class J>
+__device__ __forceinline__ int record_of(const J &job, int e) {
+    if (!job.slot_of) return e;
+    const int s = job.slot_of[e];
+    return (s >= 0 && s < job.n_records) ? s : -1;
+}
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
 // CRC-32 of each record's payload: mode 1 seals the headers, mode 0 verifies
 rvq_status launch_record_crc(uint8_t *base, uint64_t record_bytes, int n_records, int mode,
@@ -226,6 +241,19 @@ struct FfnPlan {
     size_t total;
 };
 FfnPlan plan_ffn(int d, int f, int n_pairs, int E, int n_tokens = 0);
+// The FFN launches of one layer (api.cu): lookup tables (run_ffn) and tensor
+// cores (run_ffn_tc).  slot_of / n_records: an expert cache's slot map and
+// slot count (NULL: the bank holds record e at index e).
+rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
+                   int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev, void *ws_dev,
+                   const FfnPlan &P, cudaStream_t st, void **marks, bool pdl,
+                   int32_t tc_min_tokens = 0, const int32_t *slot_of = nullptr,
+                   int32_t n_records = 0);
+rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
+                      int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
+                      void *ws_dev, const FfnPlan &P, float *y_pair, int32_t tc_min_tokens,
+                      cudaStream_t st, bool pdl, void *mid_event = nullptr,
+                      const int32_t *slot_of = nullptr, int32_t n_records = 0);
 int num_sms();
 
 }  // namespace rvq

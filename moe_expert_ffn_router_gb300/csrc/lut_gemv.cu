@@ -142,17 +142,23 @@ __device__ ItemDesc plan_one(const LutJob &job, const int32_t *soff, int i) {
         set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
         return d;
     }
+    // the walkers address the record by this index (an expert cache's slot)
+    const int rec = job.base ? record_of(job, e) : e;
+    if (rec < 0) {
+        set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
+        return d;
+    }
     if (job.check_header && job.base) {
         // the pages check magic, expert id and offset range on every read
-        const rvq_expert_header *h =
-            reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)e * job.record_bytes);
+        const rvq_expert_header *h = reinterpret_cast<const rvq_expert_header *>(
+            job.base + (uint64_t)rec * job.record_bytes);
         if (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
             h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes) {
             set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
             return d;
         }
     }
-    d.expert = e;
+    d.expert = rec;
     d.entryA = eA;
     d.entryB = eB;
     return d;
@@ -628,14 +634,18 @@ __global__ void __launch_bounds__(256) plan_pairs_kernel(const LutJob job, int4 
     } else if (job.tc_min_tokens > 0 && ne >= job.tc_min_tokens) {
         // the tensor-core path takes this expert
     } else {
-        const rvq_expert_header *h =
-            reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)e * job.record_bytes);
-        if (job.check_header &&
-            (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
-             h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes))
+        // {record index (an expert cache's slot), entry}: the walkers address
+        // the record by it
+        const int rec = record_of(job, e);
+        const rvq_expert_header *h = rec < 0 ? nullptr :
+            reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)rec * job.record_bytes);
+        if (rec < 0 ||
+            (job.check_header &&
+             (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
+              h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes)))
             set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
         else
-            d = make_int4(e, entry, 0, 0);
+            d = make_int4(rec, entry, 0, 0);
     }
     pd[p] = d;
 }

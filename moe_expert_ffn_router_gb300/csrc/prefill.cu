@@ -343,6 +343,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 
 struct PfItem {
     int e, o, j0, n, npad, mt;
+    int rec;  // record index of expert e (its cache slot, or e)
     bool valid;
 };
 
@@ -410,10 +411,12 @@ __device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, in
     I.j0 = (pi - Q[lo]) * PF_NMAX;
     I.n = min(PF_NMAX, ne - I.j0);
     I.npad = (I.n + 15) & ~15;
-    const rvq_expert_header *h =
-        reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)lo * job.record_bytes);
-    I.valid = I.n > 0 && h->magic == RVQ_BANK_MAGIC && h->expert == lo && h->layer == job.layer &&
-              h->d == job.d && h->f == job.f && h->record_bytes == job.record_bytes;
+    I.rec = record_of(job, lo);
+    const rvq_expert_header *h = I.rec < 0 ? nullptr :
+        reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)I.rec * job.record_bytes);
+    I.valid = I.n > 0 && h && h->magic == RVQ_BANK_MAGIC && h->expert == lo &&
+              h->layer == job.layer && h->d == job.d && h->f == job.f &&
+              h->record_bytes == job.record_bytes;
     return I;
 }
 
@@ -531,7 +534,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             if (job.selftest_stall) mbar_wait(bar(BAR_NEVER), 0, abort_flag, job.status);
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
                 const PfItem I = pf_item(job, Q, MT, it);
-                if (!I.valid) continue;
+                if (!I.valid) {
+                    // a bad or missing record (header mismatch, no cache slot):
+                    // every role skips the item; the MMA thread reports it
+                    if (I.n > 0) set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
+                    continue;
+                }
                 // down: two accumulators alternate over items; gate/up: an item
                 // uses both (one per M tile), each released by the epilogue on
                 // its own, so the next item starts on M tile 0 while the
@@ -804,7 +812,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         for (int it = it0; it < it1 && !*abort_flag; ++it) {
             const PfItem I = pf_item(job, Q, MT, it);
             if (!I.valid) continue;
-            const uint8_t *rec = job.base + (uint64_t)I.e * job.record_bytes;
+            const uint8_t *rec = job.base + (uint64_t)I.rec * job.record_bytes;
             if (I.e != cur_e) {
                 // every A producer is done with the previous codebooks
                 if (cur_e >= 0) {

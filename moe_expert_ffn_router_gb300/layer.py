@@ -6,9 +6,10 @@ import numpy as np
 import torch
 
 from . import (RVQ_WS_STATUS_BYTES, moe_bank_init, moe_bank_record_bytes, moe_bank_validate,
-               moe_bank_write_expert, moe_combine, moe_expert_ffn, moe_layer_forward,
-               moe_rms_norm, moe_route, moe_router_logits, moe_workspace_bytes, rvq_ws_clear,
-               rvq_ws_status)
+               moe_bank_write_expert, moe_cache_bank, moe_cache_create, moe_cache_destroy,
+               moe_cache_stats, moe_combine, moe_expert_ffn, moe_layer_forward,
+               moe_layer_forward_streamed, moe_rms_norm, moe_route, moe_router_logits,
+               moe_workspace_bytes, rvq_ws_clear, rvq_ws_status)
 
 
 def _dev(a, device, dtype=None):
@@ -154,4 +155,93 @@ class MoeStack:
         return bufs
 
 
-__all__ = ["MoeLayer", "MoeStack", "RVQ_WS_STATUS_BYTES"]
+class MoeStreamedStack:
+    """The same stack with its expert records in pinned host memory and an HBM
+    cache of `slots` records (moe_layer_forward_streamed per layer): the
+    pages' streaming engine with host memory in place of NVMe.  The layers'
+    device banks are copied into one host bank and released.  With
+    lookahead > 0 each layer prefetches the next layer's predicted experts."""
+
+    def __init__(self, layers: list[MoeLayer], slots: int, lookahead: int = 0,
+                 eps: float = 1e-6):
+        assert layers and all(L.d == layers[0].d and L.f == layers[0].f and L.E == layers[0].E
+                              for L in layers)
+        L0 = layers[0]
+        self.n_layers, self.E, self.d, self.f, self.k = len(layers), L0.E, L0.d, L0.f, L0.k
+        self.device = L0.device
+        self.eps, self.lookahead = eps, lookahead
+        rb = L0.record_bytes
+        self.host = torch.empty(self.n_layers * self.E * rb, dtype=torch.uint8, pin_memory=True)
+        for i, L in enumerate(layers):
+            self.host[i * self.E * rb:(i + 1) * self.E * rb].copy_(L.buf)
+            L.buf = None  # the device bank is no longer needed
+        torch.cuda.synchronize()
+        self.wr = [L.wr for L in layers]
+        self.bias = [L.bias for L in layers]
+        self.slots = torch.empty(slots * rb, dtype=torch.uint8, device=self.device)
+        self.slot_map = torch.full((self.n_layers, self.E), -1, dtype=torch.int32,
+                                   device=self.device)
+        self.cache = moe_cache_create(self.host, self.n_layers, self.E, self.d, self.f,
+                                      self.slots, self.slot_map)
+        self.copy_stream = torch.cuda.Stream(device=self.device)
+        self._bufs = {}
+
+    def buffers(self, n: int) -> list[dict]:
+        b = self._bufs.get(n)
+        if b is None:
+            dev, E, k = self.device, self.E, self.k
+            ws = torch.empty(moe_workspace_bytes(moe_cache_bank(self.cache, 0), n, k),
+                             dtype=torch.uint8, device=dev)
+            rvq_ws_clear(ws)
+            b = [dict(logits=torch.empty((n, E), dtype=torch.float32, device=dev),
+                      idx=torch.empty((n, k), dtype=torch.int32, device=dev),
+                      w=torch.empty((n, k), dtype=torch.float32, device=dev),
+                      offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                      pairs=torch.empty(n * k, dtype=torch.int32, device=dev),
+                      out=torch.empty((n, self.d), dtype=torch.float32, device=dev),
+                      xn=torch.empty((n, self.d), dtype=torch.bfloat16, device=dev),
+                      next_logits=torch.empty((n, E), dtype=torch.float32, device=dev),
+                      ws=ws) for _ in range(self.n_layers)]
+            self._bufs[n] = b
+        return b
+
+    def forward(self, x: torch.Tensor, tc_min_tokens: int = 0) -> list[dict]:
+        n = x.shape[0]
+        bufs = self.buffers(n)
+        h = x
+        for i in range(self.n_layers):
+            bi = bufs[i]
+            moe_rms_norm(h, n, self.d, bi["xn"], eps=self.eps)
+            nxt = i + 1 < self.n_layers and self.lookahead > 0
+            moe_layer_forward_streamed(
+                self.cache, i, self.wr[i], self.bias[i], bi["xn"], n, self.k, bi["logits"],
+                bi["idx"], bi["w"], bi["offsets"], bi["pairs"], bi["out"], bi["ws"],
+                residual=h, tc_min_tokens=tc_min_tokens,
+                next_wr=self.wr[i + 1] if nxt else None,
+                next_bias=self.bias[i + 1] if nxt else None,
+                lookahead=self.lookahead if nxt else 0,
+                next_logits=bi["next_logits"] if nxt else None,
+                copy_stream=self.copy_stream)
+            h = bi["out"]
+        return bufs
+
+    def stats(self) -> dict:
+        return moe_cache_stats(self.cache)
+
+    def status(self, n: int) -> tuple[int, int]:
+        return rvq_ws_status(self.buffers(n)[0]["ws"])
+
+    def close(self):
+        if self.cache:
+            torch.cuda.synchronize()
+            moe_cache_destroy(self.cache)
+            self.cache = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+__all__ = ["MoeLayer", "MoeStack", "MoeStreamedStack", "RVQ_WS_STATUS_BYTES"]
