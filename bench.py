@@ -57,6 +57,13 @@ WORKLOADS = {
     "k3_prefill512_e64": (4, 512, 64),  # profiling case: ~128 tokens per expert, 1.06 GB bank
     "k3_stack8_prefill2048": (5, 2048),
 }
+# tiered expert store: (config, batch, HBM cache slots, router lookahead per token):
+# the 8 K3-shaped layers' records in pinned host memory (34 GB), 256 slots of
+# HBM cache (4.25 GB), streamed per layer (moe_layer_forward_streamed)
+STREAM_WORKLOADS = {
+    "k3_stream8_b1": (3, 1, 256, 0),
+    "k3_stream8_b1_lookahead6": (3, 1, 256, 6),
+}
 KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
            "lut_gemv_down", "combine"]
 DOMINANT = "lut_gemv_gate_up"
@@ -479,6 +486,101 @@ def reference_arm(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_stream(args, rank, world, local_rank):
+    """The tiered expert store: every layer's records in pinned host memory, an
+    HBM cache of record slots, misses copied per layer after routing (and the
+    next layer's predicted experts prefetched with lookahead).  A step is one
+    batch through the whole stack, host reads of the routing included."""
+    import torch
+    import moe_expert_ffn_router_gb300 as rvq
+    from moe_expert_ffn_router_gb300.layer import MoeStreamedStack
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    config, batch, slots, lookahead = STREAM_WORKLOADS[args.workload]
+    wl = W.WORKLOADS[config]
+    s = wl.shape
+    layers = [build_layer(config, dev, shape=s, layer=i)[0] for i in range(wl.n_layers)]
+    src = W.ExpertSource(config, 0, s)
+    st = MoeStreamedStack(layers, slots=slots, lookahead=lookahead)
+    del layers
+    torch.cuda.empty_cache()
+    pool = max(64, 4 * batch)
+    bits = src.tokens_bf16(pool * batch)
+    host_x = torch.from_numpy(bits.view(np.int16)).reshape(pool, batch, s.d).pin_memory()
+    xbuf = torch.empty((batch, s.d), dtype=torch.bfloat16, device=dev)
+    out_host = torch.empty((batch, s.d), dtype=torch.float32).pin_memory()
+    uniq = []
+
+    def step(i, count=False):
+        xbuf.view(torch.int16).copy_(host_x[i % pool], non_blocking=True)
+        bufs = st.forward(xbuf)
+        out_host.copy_(bufs[-1]["out"], non_blocking=True)
+        if count:
+            uniq.append(sum(int((torch.diff(b["offsets"]) > 0).sum()) for b in bufs))
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    s0 = st.stats()
+    t0w = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record()
+    torch.cuda.synchronize()
+    t1w = time.perf_counter()
+    sampler.stop()
+    ms = replica_max_ms(e0.elapsed_time(e1), world, dev)
+    s1 = st.stats()
+    for i in range(args.steps):  # the routed experts of the same steps (not timed)
+        step(args.warmup + i, count=True)
+    torch.cuda.synchronize()
+    rc, bits_st = st.status(batch)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits_st:#x}")
+    d = {k: s1[k] - s0[k] for k in ("hits", "misses", "prefetched", "prefetch_used",
+                                     "bytes_copied")}
+    experts_total = sum(uniq)
+    weights = experts_total * 3 * s.d * s.f
+    value = job_rate(weights, world, ms) / 1e9
+    rb = st.host.numel() // (wl.n_layers * s.E)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload + ":" + wl.name, "batch": batch,
+                   "layers": wl.n_layers, "d": s.d, "f": s.f, "experts": s.E, "top_k": s.k,
+                   "host_bank_gb": round(st.host.numel() / 1e9, 2),
+                   "hbm_cache_slots": slots, "hbm_cache_gb": round(slots * rb / 1e9, 2),
+                   "lookahead": lookahead,
+                   "l2": "records stream from host memory every step (4.25 GB cache, 34 GB bank)",
+                   "parallelism": f"replicas{world}", "path": "fp32 lookup tables, streamed"},
+        "tok_s": round(job_rate(batch * args.steps, world, ms), 2),
+        "stream": {"hit_rate": round(d["hits"] / max(1, d["hits"] + d["misses"]), 4),
+                   "misses_per_step": round(d["misses"] / args.steps, 2),
+                   "prefetched_per_step": round(d["prefetched"] / args.steps, 2),
+                   "prefetch_used": d["prefetch_used"],
+                   "h2d_gbs": round(d["bytes_copied"] / (ms / 1e3) / 1e9, 1)},
+        "roofline": None,
+        "roofline_note": "bound by the host -> HBM record copies (h2d_gbs), not a kernel",
+        "cpu_baseline": None,
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step":
+                batch * s.d * 2 + d["bytes_copied"] // args.steps,
+                "d2h_bytes_per_step": batch * s.d * 4},
+        "clocks": sampler.summary(t0w, t1w),
+        # per layer: norm, router, top-k, pair plan, 2 GEMVs, SwiGLU, combine (+ the
+        # lookahead router of the next layer)
+        "gpu_launches": args.steps * (wl.n_layers * 8 + (wl.n_layers - 1 if lookahead else 0)),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    st.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,7 +588,8 @@ def main():
                     help="timed steps (default 200; 10 for --impl reference, whose steps "
                          "take about a second of CPU time each)")
     ap.add_argument("--warmup", type=int, default=None, help="untimed steps (default 10; 3)")
-    ap.add_argument("--workload", default="k3_decode_b1", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="k3_decode_b1",
+                    choices=sorted(WORKLOADS) + sorted(STREAM_WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--oracle-tokens", type=int, default=4)
     ap.add_argument("--tc-min-tokens", type=int, default=None,
@@ -507,6 +610,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         reference_arm(args, rank)
+        return
+    if args.workload in STREAM_WORKLOADS:
+        run_stream(args, rank, world, local_rank)
         return
     if world > 1:
         import torch

@@ -271,7 +271,9 @@ rvq_status moe_cache_bank(const rvq_expert_cache *cache, int32_t layer, rvq_moe_
 /* One MoE layer on cached records.  Synchronous on the host: after routing it
  * reads the expert counts back to decide the copies.  Router logits -> top-k
  * and grouping -> the routed experts made resident (misses copied
- * host -> HBM on copy_stream; `stream` waits for the slots it needs) ->
+ * host -> HBM on the cache's own copy streams (four, one per slot residue,
+ * so several copy engines run at once); `stream` waits for the slots it
+ * needs) ->
  * expert FFN on the cached records (lookup tables; tensor cores for groups of
  * >= tc_min_tokens when > 0) -> combine + residual.  Other arguments as in
  * moe_layer_forward_ex, with ws_bytes >= moe_workspace_bytes of the cache's
@@ -290,7 +292,7 @@ rvq_status moe_layer_forward_streamed(rvq_expert_cache *cache, int32_t layer,
                                       rvq_dtype rdt, int32_t tc_min_tokens,
                                       const float *next_wr_dev, const float *next_bias_dev,
                                       int32_t lookahead, float *next_logits_dev,
-                                      rvq_stream_t stream, rvq_stream_t copy_stream);
+                                      rvq_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * Router.  logits[t][e] = sum_c Wr[e][c] * x[t][c] (+ bias[e]), fp32

@@ -80,7 +80,7 @@ _SIGS = {
     "moe_cache_bank": (_i32, [_vp, _i32, _BANKP]),
     "moe_layer_forward_streamed": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
                                           _vp, _vp, _vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp,
-                                          _vp, _i32, _vp, _vp, _vp]),
+                                          _vp, _i32, _vp, _vp]),
     "moe_bank_verify": (_i32, [_BANKP, _vp, _vp, _sz, _vp]),
     "moe_router_logits": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "moe_route_max_tokens": (_i32, [_i32]),
@@ -265,15 +265,14 @@ def moe_cache_bank(cache, layer) -> RvqMoeBank:
 def moe_layer_forward_streamed(cache, layer, wr, bias, x, n, k, logits, topk_idx, topk_w,
                                offsets, pairs, out, ws, residual=None, tc_min_tokens=0,
                                next_wr=None, next_bias=None, lookahead=0, next_logits=None,
-                               stream=None, copy_stream=None):
+                               stream=None):
     rdt = _dt(residual) if residual is not None else _dt(x)
-    cs = copy_stream.cuda_stream if copy_stream is not None else _stream(stream)
     _check("moe_layer_forward_streamed",
            _lib.moe_layer_forward_streamed(
                cache, layer, _p(wr), _p(bias), _p(x), _dt(x), n, k, _p(logits), _p(topk_idx),
                _p(topk_w), _p(offsets), _p(pairs), _p(out), _p(ws), _nbytes(ws), _p(residual),
                rdt, tc_min_tokens, _p(next_wr), _p(next_bias), lookahead, _p(next_logits),
-               _stream(stream), cs))
+               _stream(stream)))
 
 
 def moe_bank_verify(bank, crc, ws, stream=None):

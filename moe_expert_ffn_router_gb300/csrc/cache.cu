@@ -10,9 +10,11 @@
 // fetch ahead ["Running a 2.78-Trillion-Parameter Model on a Laptop",
 // section "Technical Insight"; GeekNews topic 32035, section "Read-ahead and
 // router prediction"].  GB300 form:
-//  * host records are pinned; a miss is one cudaMemcpyAsync of the record on
-//    a copy stream (NVLink-C2C from Grace memory), and the compute stream
-//    waits on the slot's event only when it needs the slot;
+//  * host records are pinned; a miss is one cudaMemcpyAsync of the record,
+//    the misses spread round-robin over the cache's own copy streams (one
+//    stream moved ~176 GB/s of 16.6 MB records over NVLink-C2C; several keep
+//    more copy engines busy), and the compute stream waits on the slot's
+//    event only when it needs the slot;
 //  * the kernels address records through a device slot map
 //    (expert -> slot, -1 when absent), and still check each record's header
 //    (expert id, layer), so a stale or missing slot is reported as a corrupt
@@ -42,18 +44,23 @@ struct rvq_expert_cache {
     float *h_next = nullptr;         // pinned next-layer logits
     size_t h_next_cap = 0;
     uint64_t tick = 0;
+    std::vector<cudaStream_t> copy;  // the cache's copy streams
+    int next_copy = 0;
     rvq_cache_stats st = {};
 };
 
 namespace rvq {
 namespace {
 
+constexpr int kCopyStreams = 4;
+
 // Makes the listed experts of `layer` resident.  pinned: slots that must not
 // be replaced (this call's and, for a prefetch, the current layer's); a slot
-// this call uses is added.  Misses are copied on `cp`.  ENOMEM when no slot is
+// this call uses is added.  Misses are copied on the copy stream of their
+// slot.  ENOMEM when no slot is
 // free to replace (the caller's working set exceeds the cache).
 rvq_status cache_acquire(rvq_expert_cache *c, int layer, const std::vector<int> &experts,
-                         std::vector<uint8_t> &pinned, cudaStream_t cp, bool prefetch,
+                         std::vector<uint8_t> &pinned, bool prefetch,
                          std::vector<int> *slots_out) {
     for (int e : experts) {
         const int64_t k = (int64_t)layer * c->experts + e;
@@ -85,6 +92,9 @@ rvq_status cache_acquire(rvq_expert_cache *c, int layer, const std::vector<int> 
                 return RVQ_ENOMEM;
             }
             if (c->key[(size_t)victim] >= 0) c->map[(size_t)c->key[(size_t)victim]] = -1;
+            // a slot's copies stay on one stream, so a refill is ordered after
+            // the slot's previous copy
+            const cudaStream_t cp = c->copy[(size_t)victim % c->copy.size()];
             RVQ_CUDA(cudaMemcpyAsync(c->slots + (uint64_t)victim * c->rb,
                                      c->host + (uint64_t)k * c->rb, c->rb,
                                      cudaMemcpyHostToDevice, cp));
@@ -149,6 +159,9 @@ rvq_status moe_cache_create(rvq_expert_cache **out, const uint8_t *host_bank, in
     cudaError_t err = cudaSuccess;
     for (size_t s = 0; s < ns && err == cudaSuccess; ++s)
         err = cudaEventCreateWithFlags(&c->ready[s], cudaEventDisableTiming);
+    c->copy.assign(kCopyStreams, nullptr);
+    for (int i = 0; i < kCopyStreams && err == cudaSuccess; ++i)
+        err = cudaStreamCreateWithFlags(&c->copy[(size_t)i], cudaStreamNonBlocking);
     if (err == cudaSuccess)
         err = cudaHostAlloc(&c->stage, sizeof(int32_t) * (size_t)n_layers * n_experts,
                             cudaHostAllocDefault);
@@ -171,8 +184,12 @@ rvq_status moe_cache_create(rvq_expert_cache **out, const uint8_t *host_bank, in
 
 rvq_status moe_cache_destroy(rvq_expert_cache *c) {
     if (!c) return RVQ_OK;
+    for (cudaStream_t q : c->copy)
+        if (q) cudaStreamSynchronize(q);
     for (cudaEvent_t e : c->ready)
         if (e) cudaEventDestroy(e);
+    for (cudaStream_t q : c->copy)
+        if (q) cudaStreamDestroy(q);
     if (c->stage) cudaFreeHost(c->stage);
     if (c->h_off) cudaFreeHost(c->h_off);
     if (c->h_next) cudaFreeHost(c->h_next);
@@ -212,7 +229,7 @@ rvq_status moe_layer_forward_streamed(rvq_expert_cache *c, int32_t layer, const 
                                       rvq_dtype rdt, int32_t tc_min_tokens,
                                       const float *next_wr_dev, const float *next_bias_dev,
                                       int32_t lookahead, float *next_logits_dev,
-                                      rvq_stream_t stream, rvq_stream_t copy_stream) {
+                                      rvq_stream_t stream) {
     if (!c || layer < 0 || layer >= c->layers || !wr_dev || !x_dev || !logits_dev ||
         !topk_idx_dev || !topk_w_dev || !offsets_dev || !pairs_dev || !out_dev || !ws_dev) {
         set_error("moe_layer_forward_streamed: bad arguments (layer %d)", layer);
@@ -237,7 +254,7 @@ rvq_status moe_layer_forward_streamed(rvq_expert_cache *c, int32_t layer, const 
                   P.total);
         return RVQ_ENOMEM;
     }
-    cudaStream_t st = (cudaStream_t)stream, cp = (cudaStream_t)copy_stream;
+    cudaStream_t st = (cudaStream_t)stream;
     uint32_t *status = (uint32_t *)ws_dev;
     // routing
     if (xdt == RVQ_BF16 && router_tc_supported(n, E, B.d))
@@ -271,7 +288,7 @@ rvq_status moe_layer_forward_streamed(rvq_expert_cache *c, int32_t layer, const 
     for (int e = 0; e < E; ++e)
         if (c->h_off[e + 1] > c->h_off[e]) ex.push_back(e);
     std::vector<uint8_t> pinned((size_t)c->n_slots, 0);
-    RVQ_TRY(cache_acquire(c, layer, ex, pinned, cp, false, &slots));
+    RVQ_TRY(cache_acquire(c, layer, ex, pinned, false, &slots));
     for (int s : slots) RVQ_CUDA(cudaStreamWaitEvent(st, c->ready[(size_t)s], 0));
     int32_t *row = c->stage + (size_t)layer * E;
     for (int e = 0; e < E; ++e) row[e] = c->map[(size_t)layer * E + e];
@@ -313,7 +330,7 @@ rvq_status moe_layer_forward_streamed(rvq_expert_cache *c, int32_t layer, const 
         }
         for (int e = 0; e < E; ++e)
             if (want[(size_t)e]) pred.push_back(e);
-        RVQ_TRY(cache_acquire(c, layer + 1, pred, pinned, cp, true, nullptr));
+        RVQ_TRY(cache_acquire(c, layer + 1, pred, pinned, true, nullptr));
     }
     return RVQ_OK;
 }

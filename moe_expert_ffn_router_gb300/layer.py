@@ -183,7 +183,6 @@ class MoeStreamedStack:
                                    device=self.device)
         self.cache = moe_cache_create(self.host, self.n_layers, self.E, self.d, self.f,
                                       self.slots, self.slot_map)
-        self.copy_stream = torch.cuda.Stream(device=self.device)
         self._bufs = {}
 
     def buffers(self, n: int) -> list[dict]:
@@ -220,8 +219,7 @@ class MoeStreamedStack:
                 next_wr=self.wr[i + 1] if nxt else None,
                 next_bias=self.bias[i + 1] if nxt else None,
                 lookahead=self.lookahead if nxt else 0,
-                next_logits=bi["next_logits"] if nxt else None,
-                copy_stream=self.copy_stream)
+                next_logits=bi["next_logits"] if nxt else None)
             h = bi["out"]
         return bufs
 
