@@ -57,6 +57,7 @@ def _load():
                 "oracle_moe_layer": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp, vp]),
                 "oracle_crc32": (ctypes.c_uint32, [vp, ctypes.c_size_t]),
+                "oracle_rvq_encode": (None, [vp, i32, i32, i32, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -229,3 +230,16 @@ def crc32(data) -> int:
     b = np.ascontiguousarray(np.frombuffer(bytes(data), np.uint8) if isinstance(data, (bytes, bytearray))
                              else np.asarray(data, dtype=np.uint8).reshape(-1))
     return int(_load().oracle_crc32(b.ctypes.data if b.size else None, b.size))
+
+
+def rvq_encode(w, iters):
+    """Residual k-means encoder (3 stages x 256 codewords of 8 dimensions).
+    w: fp32 [rows][cols]; returns (codes uint8 [rows][cols/8][3], codebooks
+    fp32 [3][256][8])."""
+    w = _c(w, np.float32)
+    rows, cols = w.shape
+    assert cols % 8 == 0 and rows * cols // 8 >= 256
+    codes = np.empty((rows, cols // 8, 3), np.uint8)
+    cb = np.empty((3, 256, 8), np.float32)
+    _load().oracle_rvq_encode(_p(w), rows, cols, int(iters), _p(codes), _p(cb))
+    return codes, cb

@@ -307,3 +307,75 @@ uint32_t oracle_crc32(const uint8_t *p, size_t n)
     }
     return ~crc;
 }
+
+/* Offline RVQ encoder: residual k-means, one stage at a time, the pages'
+ * conversion step (their converter encodes every expert matrix once, offline
+ * [GN, "Conversion"]) for matrices given as fp32 weights.  The pages give no
+ * algorithm; this is the plainest residual quantiser:
+ *  - sub-vector i = W[r][8j .. 8j+7], i = r * (cols / 8) + j; R = W;
+ *  - per stage s: codebook C[k] = R[floor(k * N / 256)] for k < 256, then
+ *    `iters` rounds of (assign every sub-vector to its nearest codeword,
+ *    ties to the lower index; replace each codeword that has members by
+ *    their mean); a last assignment gives the stage's codes; R -= C[code].
+ * Distances are taken in fp32 as d = fma(t, t, d) over the 8 dimensions in
+ * order, t = r - c (the decision that sets an integer code is made in the
+ * precision the device uses).  A mean is the members' sum in int64 fixed
+ * point (each value times 2^32, rounded to nearest even), times 2^-32,
+ * divided by the member count in double and rounded to fp32: the sum does
+ * not depend on the order of the additions.  |W| < 1024 keeps every sum in
+ * range.  codes: [rows][cols/8][3]; codebooks: [3][256][8]. */
+static int32_t oracle_nearest(const float *r, const float *cb)
+{
+    int32_t best = 0;
+    float bd = 0.f;
+    for (int32_t k = 0; k < 256; ++k) {
+        float d = 0.f;
+        for (int i = 0; i < 8; ++i) {
+            float t = r[i] - cb[k * 8 + i];
+            d = fmaf(t, t, d);
+        }
+        if (k == 0 || d < bd) {
+            bd = d;
+            best = k;
+        }
+    }
+    return best;
+}
+
+void oracle_rvq_encode(const float *w, int32_t rows, int32_t cols, int32_t iters,
+                       uint8_t *codes, float *codebooks)
+{
+    const size_t N = (size_t)rows * (cols / 8);
+    float *R = (float *)malloc(sizeof(float) * N * 8);
+    int32_t *a = (int32_t *)malloc(sizeof(int32_t) * N);
+    memcpy(R, w, sizeof(float) * N * 8);
+    for (int s = 0; s < 3; ++s) {
+        float *C = codebooks + (size_t)s * 256 * 8;
+        for (int32_t k = 0; k < 256; ++k)
+            memcpy(C + k * 8, R + ((size_t)k * N / 256) * 8, sizeof(float) * 8);
+        for (int32_t it = 0; it <= iters; ++it) {
+            for (size_t i = 0; i < N; ++i) a[i] = oracle_nearest(R + i * 8, C);
+            if (it == iters) break;
+            long long sum[256][8];
+            long long cnt[256];
+            memset(sum, 0, sizeof(sum));
+            memset(cnt, 0, sizeof(cnt));
+            for (size_t i = 0; i < N; ++i) {
+                ++cnt[a[i]];
+                for (int d = 0; d < 8; ++d)
+                    sum[a[i]][d] += llrint((double)R[i * 8 + d] * 4294967296.0);
+            }
+            for (int32_t k = 0; k < 256; ++k)
+                if (cnt[k] > 0)
+                    for (int d = 0; d < 8; ++d)
+                        C[k * 8 + d] = (float)(((double)sum[k][d] * (1.0 / 4294967296.0)) /
+                                               (double)cnt[k]);
+        }
+        for (size_t i = 0; i < N; ++i) {
+            codes[i * 3 + s] = (uint8_t)a[i];
+            for (int d = 0; d < 8; ++d) R[i * 8 + d] -= C[a[i] * 8 + d];
+        }
+    }
+    free(R);
+    free(a);
+}

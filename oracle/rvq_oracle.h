@@ -38,4 +38,6 @@ int32_t oracle_moe_layer(const uint8_t *const *codes, const float *const *cbs,
                          float *logits_used, int32_t *topk_idx, float *topk_w,
                          double *y_pair, double *out);
 uint32_t oracle_crc32(const uint8_t *p, size_t n);
+void oracle_rvq_encode(const float *w, int32_t rows, int32_t cols, int32_t iters,
+                       uint8_t *codes, float *codebooks);
 #endif

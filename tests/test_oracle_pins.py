@@ -406,3 +406,62 @@ def test_crc32_sees_every_single_bit_flip():
             d = data.copy()
             d[pos] ^= np.uint8(1 << bit)
             assert oracle.crc32(d) != ref
+
+
+# ------------------------------------------------------------ offline encoder
+
+def _prototype_matrix():
+    """96 x 64 weights whose 768 sub-vectors cycle through 256 distinct
+    prototypes P[p] = (p + 1) * (1..8) / 1024 (exact in fp32 and in the
+    encoder's 2^-32 fixed point)."""
+    P = ((np.arange(256)[:, None] + 1) * (np.arange(8)[None, :] + 1) / 1024.0).astype(np.float32)
+    sub = P[np.arange(768) % 256]
+    return sub.reshape(96, 64), P
+
+
+def test_encode_recovers_prototypes_exactly():
+    """Closed form: the initial codebook takes sub-vectors 3k (N = 768), i.e.
+    P[3k mod 256], all distinct since 3 is odd; every sub-vector matches one
+    codeword exactly (code 171 p mod 256, 171 = 3^-1 mod 256), the means of
+    identical members are exact, the residual is zero, and the later stages
+    get zero codebooks and code 0 (ties to the lower index)."""
+    w, P = _prototype_matrix()
+    codes, cb = oracle.rvq_encode(w, 3)
+    i = np.arange(768).reshape(96, 8)
+    assert np.array_equal(codes[..., 0], (171 * (i % 256)) % 256)
+    assert np.array_equal(codes[..., 1:], np.zeros((96, 8, 2), np.uint8))
+    assert np.array_equal(cb[0], P[(3 * np.arange(256)) % 256])
+    assert not cb[1:].any()
+    deq = (cb[0][codes[..., 0]] + cb[1][codes[..., 1]] + cb[2][codes[..., 2]]).reshape(96, 64)
+    assert np.array_equal(deq, w)
+
+
+def _stage_distortion(w, codes, cb, stages):
+    r = w.reshape(-1, 8).astype(np.float64)
+    c = codes.reshape(-1, 3)
+    for s in range(stages):
+        r = r - cb[s][c[:, s]].astype(np.float64)
+    return float((r ** 2).sum())
+
+
+def test_encode_lloyd_rounds_never_increase_distortion():
+    w = np.random.default_rng(11).normal(0, 0.02, size=(64, 512)).astype(np.float32)
+    d = [_stage_distortion(w, *oracle.rvq_encode(w, it), 1) for it in (0, 1, 2, 4)]
+    assert all(b <= a * (1 + 1e-6) for a, b in zip(d, d[1:])), d
+    assert d[-1] < d[0]
+    full = _stage_distortion(w, *oracle.rvq_encode(w, 2), 3)
+    assert full < _stage_distortion(w, *oracle.rvq_encode(w, 2), 1)
+
+
+def test_encode_codes_are_nearest_codewords():
+    """Every stage's code is a nearest codeword of that stage's residual
+    (checked in double: its distance is within fp32 rounding of the least)."""
+    w = np.random.default_rng(12).normal(0, 0.02, size=(32, 256)).astype(np.float32)
+    codes, cb = oracle.rvq_encode(w, 2)
+    r = w.reshape(-1, 8).astype(np.float32)
+    c = codes.reshape(-1, 3)
+    for s in range(3):
+        dist = ((r[:, None, :].astype(np.float64) - cb[s][None].astype(np.float64)) ** 2).sum(-1)
+        got = dist[np.arange(len(r)), c[:, s]]
+        assert np.all(got <= dist.min(1) * (1 + 1e-5) + 1e-12)
+        r = r - cb[s][c[:, s]]
