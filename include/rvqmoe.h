@@ -163,6 +163,29 @@ rvq_status rvq_gemv_noalloc(const uint8_t *packed_codes_dev, const float *packed
                             int32_t n, float *y_dev, rvq_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * Offline RVQ encoder: the pages' conversion step (GeekNews topic 32035,
+ * "Quantization and accuracy", "Conversion": every expert matrix is encoded
+ * once, offline, into 3 x 256 codewords of 8 dimensions).  Residual k-means,
+ * one stage at a time: codebook = the residual sub-vectors at indices
+ * floor(k N / 256) (N = rows * cols / 8, sub-vector i = W[i / (cols/8)]
+ * [8 (i % (cols/8)) ..]), then `iters` rounds of nearest codeword (fp32
+ * distance, fused multiply-adds in dimension order, ties to the lower index)
+ * and mean of each codeword's members (int64 fixed point x 2^32 summed, then
+ * divided by the count in double, rounded to fp32), a last assignment for the
+ * stage's codes, and the residual minus the chosen codewords.  Reproducible:
+ * bit-identical from run to run and to the same steps on the CPU.
+ * w fp32 [rows][cols] (dev), |w| < 128, cols % 8 == 0, 256 <= N <= 2^21
+ * (N = rows * cols / 8 sub-vectors; the bounds keep the fixed-point member
+ * sums inside int64, and a 7168 x 2048 expert matrix is N = 1,835,008);
+ * codes uint8 [rows][cols/8][3] and codebooks fp32 [3][256][8] (dev) in the
+ * canonical layout rvq_pack / moe_bank_write_expert take; ws of
+ * rvq_encode_workspace_bytes(rows, cols) bytes, 256-byte aligned. */
+size_t rvq_encode_workspace_bytes(int32_t rows, int32_t cols);
+rvq_status rvq_encode(const float *w_dev, int32_t rows, int32_t cols, int32_t iters,
+                      uint8_t *codes_dev, float *codebooks_dev, void *ws_dev, size_t ws_bytes,
+                      rvq_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * Expert bank: n_experts records of record_bytes each, contiguous in HBM.
  * Record = [rvq_expert_header, 128 B][packed codebooks gate, up, down]
  *          [packed codes gate f x d][up f x d][down d x f]; every part starts

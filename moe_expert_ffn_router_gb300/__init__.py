@@ -73,6 +73,8 @@ _SIGS = {
     "moe_bank_write_expert": (_i32, [_BANKP, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_bank_validate": (_i32, [_BANKP, _vp]),
     "moe_bank_seal": (_i32, [_BANKP, _vp]),
+    "rvq_encode_workspace_bytes": (_sz, [_i32, _i32]),
+    "rvq_encode": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "moe_cache_create": (_i32, [ctypes.POINTER(_vp), _vp, _i32, _i32, _i32, _i32, _vp, _u64,
                                 _vp]),
     "moe_cache_destroy": (_i32, [_vp]),
@@ -233,6 +235,15 @@ def moe_bank_validate(bank, stream=None):
 
 def moe_bank_seal(bank, stream=None):
     _check("moe_bank_seal", _lib.moe_bank_seal(ctypes.byref(bank), _stream(stream)))
+
+
+def rvq_encode_workspace_bytes(rows, cols) -> int:
+    return int(_lib.rvq_encode_workspace_bytes(rows, cols))
+
+
+def rvq_encode(w, rows, cols, iters, codes, codebooks, ws, stream=None):
+    _check("rvq_encode", _lib.rvq_encode(_p(w), rows, cols, iters, _p(codes), _p(codebooks),
+                                         _p(ws), _nbytes(ws), _stream(stream)))
 
 
 def moe_cache_create(host_bank, n_layers, n_experts, d, f, slots, slot_map) -> int:

@@ -357,6 +357,31 @@ rvq_status moe_bank_validate(const rvq_moe_bank *bank, rvq_stream_t stream) {
     return RVQ_OK;
 }
 
+size_t rvq_encode_workspace_bytes(int32_t rows, int32_t cols) {
+    if (rows < 1 || cols < 8 || cols % 8 || (int64_t)rows * (cols / 8) < 256 ||
+        (int64_t)rows * (cols / 8) > (int64_t(1) << 21))
+        return 0;
+    return encode_workspace_bytes(rows, cols);
+}
+
+rvq_status rvq_encode(const float *w_dev, int32_t rows, int32_t cols, int32_t iters,
+                      uint8_t *codes_dev, float *codebooks_dev, void *ws_dev, size_t ws_bytes,
+                      rvq_stream_t stream) {
+    CHECK_ARG(w_dev && codes_dev && codebooks_dev && ws_dev, "rvq_encode: null pointer");
+    CHECK_ARG(rows >= 1 && cols >= 8 && cols % 8 == 0 && (int64_t)rows * (cols / 8) >= 256 &&
+                  (int64_t)rows * (cols / 8) <= (int64_t(1) << 21) && iters >= 0 && iters <= 1000,
+              "rvq_encode: rows %d, cols %d, iters %d", rows, cols, iters);
+    CHECK_ALIGN(w_dev, "rvq_encode: w");
+    CHECK_ALIGN(codebooks_dev, "rvq_encode: codebooks");
+    CHECK_ARG(((uintptr_t)ws_dev & 255u) == 0, "rvq_encode: workspace is not 256-byte aligned");
+    if (ws_bytes < encode_workspace_bytes(rows, cols)) {
+        set_error("rvq_encode: workspace %zu < %zu", ws_bytes, encode_workspace_bytes(rows, cols));
+        return RVQ_ENOMEM;
+    }
+    return launch_rvq_encode(w_dev, rows, cols, iters, codes_dev, codebooks_dev, ws_dev,
+                             (cudaStream_t)stream);
+}
+
 rvq_status moe_bank_seal(const rvq_moe_bank *bank, rvq_stream_t stream) {
     RVQ_TRY(check_bank(bank, "moe_bank_seal"));
     return launch_record_crc(bank->base, bank->record_bytes, bank->n_experts, 1, nullptr, nullptr,

@@ -217,6 +217,10 @@ __device__ __forceinline__ int record_of(const J &job, int e) {
     return (s >= 0 && s < job.n_records) ? s : -1;
 }
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
+// offline residual k-means encoder (encode.cu)
+size_t encode_workspace_bytes(int rows, int cols);
+rvq_status launch_rvq_encode(const float *w, int rows, int cols, int iters, uint8_t *codes,
+                             float *codebooks, void *ws, cudaStream_t stream);
 // CRC-32 of each record's payload: mode 1 seals the headers, mode 0 verifies
 rvq_status launch_record_crc(uint8_t *base, uint64_t record_bytes, int n_records, int mode,
                              uint32_t *crc_out, uint32_t *status, cudaStream_t stream);

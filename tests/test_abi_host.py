@@ -70,6 +70,16 @@ def test_argument_checks_return_before_any_launch():
     assert lib.moe_route(A16, 4, 64, 8, A16, A16, A16, A16, A256, 8, s) == ENOMEM
     assert lib.moe_combine(A16, A16, 2, 2, 6, A16, 0, A16, s) == EINVAL
     assert lib.moe_combine(A16, A16, 2, 2, 8, A16, 1, A16, s) == EINVAL  # bf16 alias
+    # offline encoder: too few or too many sub-vectors, ragged cols, bad iters,
+    # unaligned workspace, short workspace
+    ok = rvq.rvq_encode_workspace_bytes(256, 512)
+    assert lib.rvq_encode(A16, 1, 2040, 2, A16, A16, A256, ok, s) == EINVAL      # N = 255
+    assert lib.rvq_encode(A16, 2049, 8192, 2, A16, A16, A256, 1 << 40, s) == EINVAL  # N > 2^21
+    assert lib.rvq_encode(A16, 256, 516, 2, A16, A16, A256, ok, s) == EINVAL
+    assert lib.rvq_encode(A16, 256, 512, -1, A16, A16, A256, ok, s) == EINVAL
+    assert lib.rvq_encode(A16, 256, 512, 2, A16, A16, A16 + 16, ok, s) == EINVAL
+    assert lib.rvq_encode(A16, 256, 512, 2, A16, A16, A256, ok - 1, s) == ENOMEM
+    assert lib.rvq_encode(None, 256, 512, 2, A16, A16, A256, ok, s) == EINVAL
 
 
 def test_bank_init_checks():
@@ -115,3 +125,15 @@ def test_fuzz_argument_validation():
         n, E, k = rng.randint(-2, 5000), rng.randint(-2, 300), rng.randint(-2, 40)
         rc = lib.moe_route(A16, n, E, k, A16, A16, A16, A16, A256, 0, None)
         assert rc != 0
+
+
+def test_encode_workspace_bytes():
+    """Residual [N][8] fp32, assignment [N] int32, 256 x 8 int64 sums and 256
+    int64 counts, each padded to 256 bytes; 0 for a shape the encoder refuses."""
+    pad = lambda x: (x + 255) // 256 * 256
+    for rows, cols in ((256, 512), (37, 72), (2048, 7168)):
+        N = rows * cols // 8
+        assert rvq.rvq_encode_workspace_bytes(rows, cols) == pad(32 * N) + pad(4 * N) + 16384 + 2048
+    assert rvq.rvq_encode_workspace_bytes(1, 2040) == 0
+    assert rvq.rvq_encode_workspace_bytes(2049, 8192) == 0
+    assert rvq.rvq_encode_workspace_bytes(4, 500) == 0
