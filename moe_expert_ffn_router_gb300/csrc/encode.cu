@@ -18,7 +18,7 @@
 //    |w| < 128 every residual stays below 1024 = 2^10, so at most 2^21
 //    sub-vectors keep a sum below 2^63.
 // Per stage and round: one assignment pass (codebook in shared memory, one
-// thread per sub-vector, per-block fixed-point partial sums in shared memory,
+// thread per two sub-vectors, per-block fixed-point partial sums in shared memory,
 // one global atomic per block and entry) and one update of the 2048 entries.
 #include "internal.cuh"
 
@@ -28,6 +28,7 @@ namespace rvq {
 namespace {
 
 constexpr int ENC_NT = 256;
+constexpr int ENC_SV = 2;  // sub-vectors per thread in the search
 
 struct EncWs {
     float *R;             // [N][8] residual
@@ -44,12 +45,17 @@ __global__ void __launch_bounds__(ENC_NT) enc_init_codebook(const float *__restr
     C[t] = R[((int64_t)k * N / 256) * 8 + d];
 }
 
+// One thread per ENC_SV sub-vectors (i, i + ENC_NT, ... of the block's
+// ENC_SV x ENC_NT): the nearest codeword of each, and (do_sums) their
+// fixed-point sums and counts.  The sub-vectors' distances are independent
+// chains that share each codeword load; each chain still accumulates its 8
+// squared differences in dimension order.
 __global__ void __launch_bounds__(ENC_NT) enc_assign(const float *__restrict__ R, int64_t N,
                                                      const float *__restrict__ C,
                                                      int32_t *__restrict__ a, int do_sums,
                                                      unsigned long long *__restrict__ gsum,
                                                      unsigned long long *__restrict__ gcnt) {
-    __shared__ float cb[256 * 8];
+    __shared__ __align__(16) float cb[256 * 8];
     __shared__ unsigned long long ssum[256 * 8];
     __shared__ unsigned long long scnt[256];
     for (int i = threadIdx.x; i < 256 * 8; i += ENC_NT) {
@@ -58,34 +64,58 @@ __global__ void __launch_bounds__(ENC_NT) enc_assign(const float *__restrict__ R
     }
     for (int i = threadIdx.x; i < 256; i += ENC_NT) scnt[i] = 0ull;
     __syncthreads();
-    for (int64_t i = (int64_t)blockIdx.x * ENC_NT + threadIdx.x; i < N;
-         i += (int64_t)gridDim.x * ENC_NT) {
-        float r[8];
-        const float4 r0 = *reinterpret_cast<const float4 *>(R + i * 8);
-        const float4 r1 = *reinterpret_cast<const float4 *>(R + i * 8 + 4);
-        r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
-        r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
-        int best = 0;
-        float bd = 0.f;
-        for (int k = 0; k < 256; ++k) {
-            float dist = 0.f;
+    for (int64_t i0 = (int64_t)blockIdx.x * ENC_SV * ENC_NT + threadIdx.x; i0 < N;
+         i0 += (int64_t)gridDim.x * ENC_SV * ENC_NT) {
+        float r[ENC_SV][8];
 #pragma unroll
-            for (int d = 0; d < 8; ++d) {
-                const float t = __fsub_rn(r[d], cb[k * 8 + d]);
-                dist = __fmaf_rn(t, t, dist);
-            }
-            if (k == 0 || dist < bd) {
-                bd = dist;
-                best = k;
-            }
+        for (int v = 0; v < ENC_SV; ++v) {
+            const int64_t i = i0 + v * ENC_NT;
+            const float4 *p = reinterpret_cast<const float4 *>(R + (i < N ? i : i0) * 8);
+            const float4 x0 = p[0], x1 = p[1];
+            r[v][0] = x0.x; r[v][1] = x0.y; r[v][2] = x0.z; r[v][3] = x0.w;
+            r[v][4] = x1.x; r[v][5] = x1.y; r[v][6] = x1.z; r[v][7] = x1.w;
         }
-        a[i] = best;
-        if (do_sums) {
-            atomicAdd(&scnt[best], 1ull);
+        float bd[ENC_SV], dk[ENC_SV];
+        int best[ENC_SV];
+        auto dist = [&](int k, float (&dd)[ENC_SV]) {
+            const float4 c0 = *reinterpret_cast<const float4 *>(cb + k * 8);
+            const float4 c1 = *reinterpret_cast<const float4 *>(cb + k * 8 + 4);
+            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int v = 0; v < ENC_SV; ++v) dd[v] = 0.f;
 #pragma unroll
             for (int d = 0; d < 8; ++d)
-                atomicAdd(&ssum[best * 8 + d],
-                          (unsigned long long)__double2ll_rn((double)r[d] * 4294967296.0));
+#pragma unroll
+                for (int v = 0; v < ENC_SV; ++v) {
+                    const float t = __fsub_rn(r[v][d], c[d]);
+                    dd[v] = __fmaf_rn(t, t, dd[v]);
+                }
+        };
+        dist(0, bd);
+#pragma unroll
+        for (int v = 0; v < ENC_SV; ++v) best[v] = 0;
+#pragma unroll 3
+        for (int k = 1; k < 256; ++k) {
+            dist(k, dk);
+#pragma unroll
+            for (int v = 0; v < ENC_SV; ++v)
+                if (dk[v] < bd[v]) {
+                    bd[v] = dk[v];
+                    best[v] = k;
+                }
+        }
+#pragma unroll
+        for (int v = 0; v < ENC_SV; ++v) {
+            const int64_t i = i0 + v * ENC_NT;
+            if (i >= N) continue;
+            a[i] = best[v];
+            if (do_sums) {
+                atomicAdd(&scnt[best[v]], 1ull);
+#pragma unroll
+                for (int d = 0; d < 8; ++d)
+                    atomicAdd(&ssum[best[v] * 8 + d],
+                              (unsigned long long)__double2ll_rn((double)r[v][d] * 4294967296.0));
+            }
         }
     }
     if (!do_sums) return;
@@ -151,7 +181,11 @@ rvq_status launch_rvq_encode(const float *w, int rows, int cols, int iters, uint
     RVQ_CUDA(cudaMemcpyAsync(W.R, w, (size_t)N * 32, cudaMemcpyDeviceToDevice, stream));
     RVQ_CUDA(cudaMemsetAsync(W.sum, 0, 256 * 8 * 8, stream));
     RVQ_CUDA(cudaMemsetAsync(W.cnt, 0, 256 * 8, stream));
-    const int grid = (int)std::min<int64_t>((N + ENC_NT - 1) / ENC_NT, 4 * num_sms());
+    // one wave of resident blocks (a persistent grid-stride loop)
+    int per_sm = 0;
+    RVQ_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, enc_assign, ENC_NT, 0));
+    const int grid = (int)std::min<int64_t>((N + ENC_SV * ENC_NT - 1) / (ENC_SV * ENC_NT),
+                                            (int64_t)std::max(1, per_sm) * num_sms());
     for (int s = 0; s < 3; ++s) {
         float *C = codebooks + (size_t)s * 256 * 8;
         enc_init_codebook<<<8, ENC_NT, 0, stream>>>(W.R, N, C);
