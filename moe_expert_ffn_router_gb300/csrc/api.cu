@@ -38,13 +38,13 @@ RecordLayout record_layout(int32_t d, int32_t f) {
 }
 
 int num_sms() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // per device
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
     if (dev < 64 && cached[dev]) return cached[dev];
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-        v = 148;
+        v = 152;
     if (dev < 64) cached[dev] = v;
     return v;
 }

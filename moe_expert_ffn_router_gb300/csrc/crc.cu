@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(CRC_NT) record_crc_kernel(uint8_t *base, uint6
 
 rvq_status launch_record_crc(uint8_t *base, uint64_t record_bytes, int n_records, int mode,
                              uint32_t *crc_out, uint32_t *status, cudaStream_t stream) {
-    static int table_done[64] = {0};
+    static std::atomic<int> table_done[64];  // per device; copying twice is harmless
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev >= 64 || !table_done[dev]) {

@@ -1106,7 +1106,7 @@ rvq_status launch_lut_plan(const LutJob &ja, const LutJob *jb, cudaStream_t stre
 }
 
 rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl) {
-    static int attr_done[64] = {0};
+    static std::atomic<int> attr_done[64];  // per device; setting twice is harmless
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {
@@ -1140,7 +1140,7 @@ rvq_status launch_lut_plan_pairs(const LutJob &job, int4 *pd, cudaStream_t strea
 }
 
 rvq_status launch_lut_gemv_il(const LutJob &job, const int4 *pd, cudaStream_t stream, bool pdl) {
-    static int attr_done[64] = {0};
+    static std::atomic<int> attr_done[64];  // per device; setting twice is harmless
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {

@@ -955,7 +955,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 void *tensor_map_encoder_entry() { return reinterpret_cast<void *>(tensor_map_encoder()); }
 
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) {
-    static int attr_done[64] = {0};
+    static std::atomic<int> attr_done[64];  // per device; setting twice is harmless
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {

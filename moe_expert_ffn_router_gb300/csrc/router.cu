@@ -457,7 +457,7 @@ template <int NT, bool SELECT>
 rvq_status launch_route_nt(const float *logits, int n, int E, int k, int32_t *idx, float *w,
                            int32_t *offsets, int32_t *pairs, uint32_t *status,
                            cudaStream_t stream, bool pdl) {
-    static int attr_done[64] = {0};
+    static std::atomic<int> attr_done[64];  // per device; setting twice is harmless
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {

@@ -305,7 +305,7 @@ rvq_status launch_router_logits_tc(const float *wr, const float *bias, const voi
         set_error("router (tensor cores): n %d / E %d / d %d or alignment not supported", n, E, d);
         return RVQ_EINVAL;
     }
-    static int attr_done[64] = {0};
+    static std::atomic<int> attr_done[64];  // per device; setting twice is harmless
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {
