@@ -26,7 +26,11 @@
  *
  * Conventions for every call:
  *  - Pointers marked (dev) are device memory, (host) host memory.  The caller
- *    owns every buffer; the library allocates nothing and frees nothing.
+ *    owns every buffer; the library allocates no device or host buffers (the
+ *    tiered expert store's handle and its copy streams, created by
+ *    moe_cache_create and released by moe_cache_destroy, are the exception).
+ *  - Batch sizes (n tokens) are at least 1: an empty batch is an argument
+ *    error (RVQ_EINVAL), so a caller with no tokens skips the call.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream), except where "synchronous" is stated.
  *  - Arguments are checked on the host before anything is launched; a bad

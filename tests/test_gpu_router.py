@@ -47,6 +47,17 @@ def test_route_random(n, E, k):
     check_route(rng.normal(size=(n, E)).astype(np.float32), k)
 
 
+@pytest.mark.parametrize("E,k", [(256, 16), (64, 8), (16, 16)])
+def test_route_at_the_single_launch_token_limit(E, k):
+    """The largest batch one routing call takes (its grouping runs in one
+    block's shared memory): selection, weights and grouping still bit-exact,
+    and the next size up is refused before any launch."""
+    n = rvq.moe_route_max_tokens(E)
+    check_route(rng.normal(size=(n, E)).astype(np.float32), k)
+    with pytest.raises(RuntimeError):
+        run_route(np.zeros((n + 1, E), np.float32), k)
+
+
 def test_route_ties_and_degenerate():
     E, k = 256, 16
     lg = np.round(rng.normal(size=(50, E)) * 2).astype(np.float32)   # many exact ties
