@@ -27,6 +27,18 @@ __global__ void __launch_bounds__(LG_NT) router_logits_kernel(
     const int e = blockIdx.x;
     const int t0 = blockIdx.y * TB;
     const int nt = min(TB, n - t0);
+    // Launched early behind the preceding kernel: the block's router row is
+    // requested into L2 before the dependency wait (a hint only: every load
+    // below comes after the wait, so a row written by that kernel is still
+    // read as it left it), hiding its DRAM time behind the preceding kernel.
+    if (threadIdx.x == 0 && blockIdx.y == 0) {
+        const float *row = wr + (int64_t)e * d;
+        if (((uintptr_t)row & 15u) == 0 && (d & 3) == 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row), "r"((uint32_t)d * 4u)
+                         : "memory");
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     float acc[TB];
 #pragma unroll
     for (int b = 0; b < TB; ++b) acc[b] = 0.f;
@@ -426,8 +438,20 @@ int route_max_tokens(int E) {
 
 rvq_status launch_router_logits(const float *wr, const float *bias, const void *x, int xdt, int n,
                                 int E, int d, float *logits, cudaStream_t stream) {
+    // the small-batch kernels may start behind the preceding kernel
+    // (programmatic dependent launch; they wait before reading anything)
+    cudaLaunchConfig_t pcfg = {};
+    cudaLaunchAttribute pattr[1];
+    pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pattr[0].val.programmaticStreamSerializationAllowed = 1;
+    pcfg.attrs = pattr;
+    pcfg.numAttrs = 1;
+    pcfg.blockDim = dim3(LG_NT);
+    pcfg.stream = stream;
     if (n == 1) {
-        router_logits_kernel<1><<<dim3(E, 1), LG_NT, 0, stream>>>(wr, bias, x, xdt, n, E, d, logits);
+        pcfg.gridDim = dim3((unsigned)E, 1);
+        RVQ_CUDA(cudaLaunchKernelEx(&pcfg, router_logits_kernel<1>, wr, bias, x, xdt, n, E, d,
+                                    logits));
     } else if (n > 64 && d % LT_K == 0) {
         // a cluster of LT_S blocks per output tile when K splits evenly
         const int S = d % (LT_S * LT_K) == 0 ? LT_S : 1;
@@ -446,8 +470,9 @@ rvq_status launch_router_logits(const float *wr, const float *bias, const void *
         RVQ_CUDA(cudaLaunchKernelEx(&cfg, router_logits_tiled_kernel, wr, bias, x, xdt, n, E, d,
                                     logits));
     } else {
-        router_logits_kernel<8><<<dim3(E, (n + 7) / 8), LG_NT, 0, stream>>>(wr, bias, x, xdt, n, E, d,
-                                                                            logits);
+        pcfg.gridDim = dim3((unsigned)E, (unsigned)((n + 7) / 8));
+        RVQ_CUDA(cudaLaunchKernelEx(&pcfg, router_logits_kernel<8>, wr, bias, x, xdt, n, E, d,
+                                    logits));
     }
     RVQ_LAUNCHED("router_logits");
     return RVQ_OK;
