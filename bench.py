@@ -56,6 +56,9 @@ WORKLOADS = {
     "k3_stack8_b32": (3, 32),
     "k3_prefill512_e64": (4, 512, 64),  # profiling case: ~128 tokens per expert, 1.06 GB bank
     "k3_stack8_prefill2048": (5, 2048),
+    # the decode layer on a bank whose codes come from the offline encoder
+    # (N(0, 0.02^2) weights, 2 Lloyd rounds per stage) instead of uniform codes
+    "k3_decode_b1_encoded": (2, 1, None, "encoded"),
 }
 # tiered expert store: (config, batch, HBM cache slots, router lookahead per token):
 # the 8 K3-shaped layers' records in pinned host memory (34 GB), 256 slots of
@@ -191,9 +194,14 @@ def workload_shape(name):
     spec = WORKLOADS[name]
     config, batch = spec[0], spec[1]
     s = W.WORKLOADS[config].shape
-    if len(spec) > 2:
+    if len(spec) > 2 and spec[2] is not None:
         s = W.LayerShape(s.d, s.f, spec[2], s.k)
     return config, batch, s
+
+
+def encoded_bank(name):
+    spec = WORKLOADS.get(name, ())
+    return len(spec) > 3 and spec[3] == "encoded"
 
 
 def router_bias(config, src):
@@ -203,17 +211,42 @@ def router_bias(config, src):
     return W.zipf_bias(src.lseed, src.shape.E, wl.zipf_beta)
 
 
-def build_layer(config, device, k=None, shape=None, layer=0):
+def build_layer(config, device, k=None, shape=None, layer=0, encoded=False):
     from moe_expert_ffn_router_gb300.layer import MoeLayer
     s = shape or W.WORKLOADS[config].shape
     src = W.ExpertSource(config, layer, s)
     L = MoeLayer(s.E, s.d, s.f, k or s.k, layer=layer, device=device)
-    for e in range(s.E):
+    if encoded:
+        encode_experts(L, s, device, seed=1000 * layer + config)
+    for e in range(s.E if encoded else 0, s.E):
         mats = [(src.codes(e, m), src.codebooks(e, m)) for m in range(3)]
         L.load_expert(e, mats[0][0], mats[1][0], mats[2][0], np.stack([c for _, c in mats]))
     L.set_router(src.router_weight(), router_bias(config, src))
     L.validate()
     return L, src
+
+
+def encode_experts(L, s, device, seed, iters=2, sigma=0.02):
+    """Every expert's gate, up and down matrix drawn N(0, sigma^2) on the
+    device (a seeded generator per matrix) and encoded by rvq_encode."""
+    import torch
+    import moe_expert_ffn_router_gb300 as rvq
+    shapes = [(s.f, s.d), (s.f, s.d), (s.d, s.f)]
+    ws = torch.empty(max(rvq.rvq_encode_workspace_bytes(r, c) for r, c in shapes),
+                     dtype=torch.uint8, device=device)
+    gen = torch.Generator(device=device)
+    for e in range(s.E):
+        codes, cbs = [], []
+        for m, (r, c) in enumerate(shapes):
+            gen.manual_seed(seed * 1_000_003 + e * 3 + m)
+            w = torch.randn((r, c), generator=gen, device=device) * sigma
+            cd = torch.empty((r, c // 8, 3), dtype=torch.uint8, device=device)
+            cb = torch.empty((3, 256, 8), dtype=torch.float32, device=device)
+            rvq.rvq_encode(w, r, c, iters, cd, cb, ws)
+            codes.append(cd)
+            cbs.append(cb)
+        L.load_expert(e, codes[0], codes[1], codes[2], torch.stack(cbs))
+    torch.cuda.synchronize(device)
 
 
 def replica_max_ms(ms, world, device):
@@ -247,7 +280,8 @@ def run_gpu(args, rank, world, local_rank):
         tc_min = args.tc_min_tokens
     kernels = KERNELS_TC if tc_min > 0 else KERNELS
     n_layers = W.WORKLOADS[config].n_layers
-    built = [build_layer(config, dev, shape=s, layer=i) for i in range(n_layers)]
+    encoded = encoded_bank(args.workload)
+    built = [build_layer(config, dev, shape=s, layer=i, encoded=encoded) for i in range(n_layers)]
     L, src = built[0]
     from moe_expert_ffn_router_gb300.layer import MoeStack
     stack = MoeStack([b[0] for b in built])
@@ -778,7 +812,10 @@ def main():
                        "parallelism": f"replicas{world}",
                        "path": ("tensor cores for every expert group (bf16 operands, "
                                 "fp32 accumulate)") if r["prefill"] else
-                               "fp32 lookup tables"},
+                               "fp32 lookup tables",
+                       "codes": ("encoded from N(0, 0.02^2) weights by rvq_encode, 2 Lloyd "
+                                 "rounds per stage") if encoded_bank(args.workload) else
+                                "uniform random (seeded)"},
             "code_byte_gbs": round(r["code_gbs"], 1),
             "layer_tok_s": round(r["tok_s"], 1),
             "unique_experts_per_step": round(r["uniq_mean"], 2),
