@@ -432,7 +432,8 @@ def run_gpu(args, rank, world, local_rank):
                launches=((TC_LAUNCHES_PER_STEP if tc_min == 1 else len(KERNELS) if tc_min == 0
                           else len(KERNELS) + TC_LAUNCHES_PER_STEP - 3)
                          + router_launches(batch, s.E, s.d) - 1
-                         + (1 if n_layers > 1 else 0)) * args.steps * n_layers,
+                         # a stack's pre-norm: inside the router launch for one token
+                         + (1 if n_layers > 1 and batch > 1 else 0)) * args.steps * n_layers,
                config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
     del L, stack, built
     return res

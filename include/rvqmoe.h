@@ -417,6 +417,27 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
                                 const void *residual_dev, rvq_dtype rdt, int32_t tc_min_tokens,
                                 void **events, rvq_stream_t stream);
 
+/* A pre-norm layer of a stack in one call: xn = bf16(h / sqrt(mean(h^2) +
+ * eps)) row by row (the values moe_rms_norm gives), then moe_layer_forward_ex
+ * with x = xn (bf16) and residual = h: out = h + sum_slot w * expert(xn).
+ * The stack's reading of the pages' per-layer input (they show no
+ * normalisation; the stream grows without bound otherwise).
+ *  - h_dev: dtype hdt (fp32 or bf16) [n][d], 16-byte aligned; out may alias an
+ *    fp32 h (each element is read before it is written), not a bf16 one.
+ *  - xn_dev: bf16 [n][d] (dev, 16-byte aligned), written; must not alias h or
+ *    out.
+ *  - eps > 0.  Other arguments as in moe_layer_forward_ex (no event marks).
+ * For one token the norm runs inside the router launch (every router block
+ * derives the same factor; block 0 writes xn), one launch less on the decode
+ * critical path; larger batches launch the norm first. */
+rvq_status moe_layer_forward_prenorm(const rvq_moe_bank *bank, const float *wr_dev,
+                                     const float *bias_dev, const void *h_dev, rvq_dtype hdt,
+                                     int32_t n, int32_t k, float eps, uint16_t *xn_dev,
+                                     float *logits_dev, int32_t *topk_idx_dev, float *topk_w_dev,
+                                     int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
+                                     void *ws_dev, size_t ws_bytes, int32_t tc_min_tokens,
+                                     rvq_stream_t stream);
+
 /* Row-wise RMS normalisation without a gain, the pre-norm of a layer stack:
  * out[t][c] = x[t][c] / sqrt(mean_c x[t][c]^2 + eps), sums in fp32.
  * The pages describe no normalisation: a stack of their layers (router,

@@ -96,6 +96,8 @@ _SIGS = {
                                  _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_layer_forward_ex": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp,
                                     _vp, _vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp]),
+    "moe_layer_forward_prenorm": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
+                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
     "moe_rms_norm": (_i32, [_vp, _i32, _i32, _i32, ctypes.c_float, _vp, _i32, _vp]),
     "rvq_selftest_prefill_timeout": (_i32, [_BANKP, _vp, _sz, _vp]),
     "rvq_ws_clear": (_i32, [_vp, _vp]),
@@ -343,6 +345,16 @@ def moe_layer_forward(bank, wr, bias, x, n, k, logits, topk_idx, topk_w, offsets
                                      _p(logits), _p(topk_idx), _p(topk_w), _p(offsets),
                                      _p(pairs), _p(out), _p(ws), _nbytes(ws), _p(residual), rdt,
                                      int(tc_min_tokens), ev, _stream(stream)))
+
+
+def moe_layer_forward_prenorm(bank, wr, bias, h, n, k, eps, xn, logits, topk_idx, topk_w, offsets,
+                              pairs, out, ws, tc_min_tokens=0, stream=None):
+    """out = h + MoE(bf16 rms_norm(h)); xn (bf16 [n][d]) receives the normalised rows."""
+    _check("moe_layer_forward_prenorm",
+           _lib.moe_layer_forward_prenorm(ctypes.byref(bank), _p(wr), _p(bias), _p(h), _dt(h), n, k,
+                                          float(eps), _p(xn), _p(logits), _p(topk_idx),
+                                          _p(topk_w), _p(offsets), _p(pairs), _p(out), _p(ws),
+                                          _nbytes(ws), int(tc_min_tokens), _stream(stream)))
 
 
 def rvq_selftest_prefill_timeout(bank, ws, stream=None):

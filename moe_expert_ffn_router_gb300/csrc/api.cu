@@ -678,6 +678,14 @@ rvq_status moe_rms_norm(const void *x_dev, rvq_dtype xdt, int32_t n, int32_t d, 
                            false);
 }
 
+static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
+                                     int32_t n, int32_t k, float *logits_dev,
+                                     int32_t *topk_idx_dev, float *topk_w_dev,
+                                     int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
+                                     void *ws_dev, const void *residual_dev, rvq_dtype rdt,
+                                     int32_t tc_min_tokens, void **events, cudaStream_t st,
+                                     const FfnPlan &P);
+
 rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
                                 const float *bias_dev, const void *x_dev, rvq_dtype xdt, int32_t n,
                                 int32_t k, float *logits_dev, int32_t *topk_idx_dev,
@@ -709,6 +717,7 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
         if (events) RVQ_CUDA(cudaEventRecord((cudaEvent_t)events[i], st));
         return RVQ_OK;
     };
+    (void)pdl;
     RVQ_TRY(mark(0));
     if (xdt == RVQ_BF16 && router_tc_supported(n, bank->n_experts, bank->d))
         // prefill-sized bf16 batch: the logits GEMM on the tensor cores
@@ -719,6 +728,24 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
         RVQ_TRY(launch_router_logits(wr_dev, bias_dev, x_dev, (int)xdt, n, bank->n_experts,
                                      bank->d, logits_dev, st));
     RVQ_TRY(mark(1));
+    return layer_after_router(bank, x_dev, xdt, n, k, logits_dev, topk_idx_dev, topk_w_dev,
+                              offsets_dev, pairs_dev, out_dev, ws_dev, residual_dev, rdt,
+                              tc_min_tokens, events, st, P);
+}
+
+// Routing, expert FFN and combine of a layer whose logits are computed.
+static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt,
+                                     int32_t n, int32_t k, float *logits_dev,
+                                     int32_t *topk_idx_dev, float *topk_w_dev,
+                                     int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
+                                     void *ws_dev, const void *residual_dev, rvq_dtype rdt,
+                                     int32_t tc_min_tokens, void **events, cudaStream_t st,
+                                     const FfnPlan &P) {
+    const bool pdl = events == nullptr;
+    auto mark = [&](int i) -> rvq_status {
+        if (events) RVQ_CUDA(cudaEventRecord((cudaEvent_t)events[i], st));
+        return RVQ_OK;
+    };
     RVQ_TRY(launch_route(logits_dev, n, bank->n_experts, k, topk_idx_dev, topk_w_dev, offsets_dev,
                          pairs_dev, (uint32_t *)ws_dev, st, pdl));
     RVQ_TRY(mark(2));
@@ -758,6 +785,50 @@ rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, cons
     return moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
                                 topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
                                 nullptr, xdt, 0, events, stream);
+}
+
+rvq_status moe_layer_forward_prenorm(const rvq_moe_bank *bank, const float *wr_dev,
+                                     const float *bias_dev, const void *h_dev, rvq_dtype hdt,
+                                     int32_t n, int32_t k, float eps, uint16_t *xn_dev,
+                                     float *logits_dev, int32_t *topk_idx_dev, float *topk_w_dev,
+                                     int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
+                                     void *ws_dev, size_t ws_bytes, int32_t tc_min_tokens,
+                                     rvq_stream_t stream) {
+    CHECK_ARG(h_dev && xn_dev && wr_dev && logits_dev && topk_idx_dev && topk_w_dev &&
+                  offsets_dev && pairs_dev && out_dev,
+              "moe_layer_forward_prenorm: null pointer");
+    CHECK_ARG(hdt == RVQ_F32 || hdt == RVQ_BF16, "moe_layer_forward_prenorm: h dtype %d", (int)hdt);
+    CHECK_ARG(eps > 0.f, "moe_layer_forward_prenorm: eps must be positive");
+    CHECK_ALIGN(h_dev, "moe_layer_forward_prenorm: h");
+    CHECK_ALIGN(xn_dev, "moe_layer_forward_prenorm: xn");
+    CHECK_ARG((const void *)xn_dev != h_dev && (void *)xn_dev != (void *)out_dev,
+              "moe_layer_forward_prenorm: xn aliases h or out");
+    if (hdt == RVQ_BF16)
+        CHECK_ARG((const void *)out_dev != h_dev, "moe_layer_forward_prenorm: bf16 h cannot alias out");
+    RVQ_TRY(check_ffn_args(bank, xn_dev, RVQ_BF16, n, k, ws_dev, ws_bytes,
+                           "moe_layer_forward_prenorm"));
+    CHECK_ALIGN(wr_dev, "moe_layer_forward_prenorm: Wr");
+    CHECK_ALIGN(out_dev, "moe_layer_forward_prenorm: out");
+    const int d = bank->d;
+    const FfnPlan P = plan_ffn(d, bank->f, n * k, bank->n_experts, n);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (n == 1) {
+        // one token: the norm inside the router launch
+        RVQ_TRY(launch_router_norm_logits(wr_dev, bias_dev, h_dev, (int)hdt, bank->n_experts, d,
+                                          eps, xn_dev, logits_dev, st));
+    } else {
+        RVQ_TRY(launch_rms_norm(h_dev, (int)hdt, n, d, eps, xn_dev, (int)RVQ_BF16, st, true));
+        if (router_tc_supported(n, bank->n_experts, d))
+            RVQ_TRY(launch_router_logits_tc(wr_dev, bias_dev, xn_dev, n, bank->n_experts, d,
+                                            logits_dev, (uint8_t *)ws_dev + P.off_wsplit,
+                                            (uint32_t *)ws_dev, st));
+        else
+            RVQ_TRY(launch_router_logits(wr_dev, bias_dev, xn_dev, (int)RVQ_BF16, n,
+                                         bank->n_experts, d, logits_dev, st));
+    }
+    return layer_after_router(bank, xn_dev, RVQ_BF16, n, k, logits_dev, topk_idx_dev, topk_w_dev,
+                              offsets_dev, pairs_dev, out_dev, ws_dev, h_dev, hdt, tc_min_tokens,
+                              nullptr, st, P);
 }
 
 rvq_status rvq_selftest_prefill_timeout(const rvq_moe_bank *bank, void *ws_dev, size_t ws_bytes,

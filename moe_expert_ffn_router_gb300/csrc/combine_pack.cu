@@ -112,28 +112,14 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(const void *__restrict__ 
     asm volatile("griddepcontrol.launch_dependents;");
     const int64_t row = (int64_t)blockIdx.x * d;
     const int d4 = d >> 2;
-    float ss = 0.f;
-    for (int c4 = threadIdx.x; c4 < d4; c4 += blockDim.x) {
-        const float4 v = load4(x, xdt, row + c4 * 4);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
-    const float inv = 1.0f / sqrtf(tot / (float)d + eps);
+    const float inv = block_rms_inv(x, xdt, row, d, eps, red);
     for (int c4 = threadIdx.x; c4 < d4; c4 += blockDim.x) {
         const float4 v = load4(x, xdt, row + c4 * 4);
         const float4 y = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
         if (odt == RVQ_BF16) {
             uint2 b;
-            b.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
-            b.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
+            b.x = bf16x2_bits(y.x, y.y);
+            b.y = bf16x2_bits(y.z, y.w);
             *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(out) + row + c4 * 4) = b;
         } else {
             *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + row + c4 * 4) = y;

@@ -92,6 +92,32 @@ __device__ __forceinline__ float4 load4(const void *base, int dtype, int64_t idx
     return *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + idx);
 }
 
+// 1 / sqrt(mean(x[row .. row + d)^2) + eps) for a block of 256 threads (red:
+// 8 floats of shared memory).  The RMS norm and the router that normalises
+// its own input both use it, so they derive the same factor bit for bit.
+__device__ __forceinline__ float block_rms_inv(const void *x, int xdt, int64_t row, int d, float eps,
+                                               float *red) {
+    const int d4 = d >> 2;
+    float ss = 0.f;
+    for (int c4 = threadIdx.x; c4 < d4; c4 += 256) {
+        const float4 v = load4(x, xdt, row + c4 * 4);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    return 1.0f / sqrtf(tot / (float)d + eps);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
 __device__ __forceinline__ float load1(const void *base, int dtype, int64_t idx) {
     if (dtype == RVQ_BF16)
         return __uint_as_float(
@@ -175,6 +201,11 @@ rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, 
                           const void *res, int rdt, float *out, cudaStream_t stream, bool pdl);
 rvq_status launch_router_logits(const float *wr, const float *bias, const void *x, int xdt,
                                 int n, int E, int d, float *logits, cudaStream_t stream);
+// One token: xn = bf16(h / rms(h)) (written by block 0) and its logits, in one
+// launch; the same values as launch_rms_norm followed by launch_router_logits.
+rvq_status launch_router_norm_logits(const float *wr, const float *bias, const void *h, int hdt,
+                                     int E, int d, float eps, uint16_t *xn, float *logits,
+                                     cudaStream_t stream);
 rvq_status launch_route(const float *logits, int n, int E, int k, int32_t *idx, float *w,
                         int32_t *offsets, int32_t *pairs, uint32_t *status,
                         cudaStream_t stream, bool pdl);

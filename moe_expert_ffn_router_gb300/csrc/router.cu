@@ -87,6 +87,57 @@ __global__ void __launch_bounds__(LG_NT) router_logits_kernel(
     }
 }
 
+// One token of a pre-norm layer: every block derives the RMS factor of h
+// itself (the 28 KB row is read from L2 by all of them), rounds h / rms to
+// bf16 exactly as the RMS norm kernel does and takes the dot product with its
+// router row in the order router_logits_kernel<1> uses; block 0 also writes
+// the normalised row for the expert FFN.  One launch instead of two on the
+// decode critical path.
+__global__ void __launch_bounds__(LG_NT) router_norm_logits_kernel(
+    const float *__restrict__ wr, const float *__restrict__ bias, const void *__restrict__ h,
+    int hdt, int E, int d, float eps, uint16_t *__restrict__ xn, float *__restrict__ logits) {
+    __shared__ float red[LG_NT / 32];
+    const int e = blockIdx.x;
+    if (threadIdx.x == 0) {
+        const float *row = wr + (int64_t)e * d;
+        if (((uintptr_t)row & 15u) == 0 && (d & 3) == 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row), "r"((uint32_t)d * 4u)
+                         : "memory");
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const float inv = block_rms_inv(h, hdt, 0, d, eps, red);
+    const float4 *w4 = reinterpret_cast<const float4 *>(wr + (int64_t)e * d);
+    const int d4 = d >> 2;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int c4 = threadIdx.x; c4 < d4; c4 += LG_NT) {
+        const float4 wv = __ldg(w4 + c4);
+        const float4 v = load4(h, hdt, (int64_t)c4 * 4);
+        uint2 q;
+        q.x = bf16x2_bits(v.x * inv, v.y * inv);
+        q.y = bf16x2_bits(v.z * inv, v.w * inv);
+        if (e == 0) *reinterpret_cast<uint2 *>(xn + (int64_t)c4 * 4) = q;
+        acc = fmaf(wv.x, __uint_as_float(q.x << 16), acc);
+        acc = fmaf(wv.y, __uint_as_float(q.x & 0xFFFF0000u), acc);
+        acc = fmaf(wv.z, __uint_as_float(q.y << 16), acc);
+        acc = fmaf(wv.w, __uint_as_float(q.y & 0xFFFF0000u), acc);
+    }
+    __syncthreads();  // every warp has read red[] (the RMS sum) before it is reused
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < LG_NT / 32; ++q) v += red[q];
+        if (bias) v += bias[e];
+        logits[e] = v;
+    }
+}
+
 // Prefill-sized batches: a tiled fp32 GEMM, logits[n][E] = x Wr^T.  Each
 // output tile of 64 tokens x 64 experts belongs to a cluster of LT_S blocks
 // that split the hidden dimension; in a block 256 threads hold 4 x 4 outputs
@@ -475,6 +526,24 @@ rvq_status launch_router_logits(const float *wr, const float *bias, const void *
                                     logits));
     }
     RVQ_LAUNCHED("router_logits");
+    return RVQ_OK;
+}
+
+rvq_status launch_router_norm_logits(const float *wr, const float *bias, const void *h, int hdt,
+                                     int E, int d, float eps, uint16_t *xn, float *logits,
+                                     cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)E);
+    cfg.blockDim = dim3(LG_NT);
+    cfg.stream = stream;
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, router_norm_logits_kernel, wr, bias, h, hdt, E, d, eps, xn,
+                                logits));
+    RVQ_LAUNCHED("router_norm_logits");
     return RVQ_OK;
 }
 

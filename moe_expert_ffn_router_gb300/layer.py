@@ -8,7 +8,8 @@ import torch
 from . import (RVQ_WS_STATUS_BYTES, moe_bank_init, moe_bank_record_bytes, moe_bank_validate,
                moe_bank_write_expert, moe_cache_bank, moe_cache_create, moe_cache_destroy,
                moe_cache_stats, moe_combine, moe_expert_ffn, moe_layer_forward,
-               moe_layer_forward_streamed, moe_rms_norm, moe_route, moe_router_logits,
+               moe_layer_forward_prenorm, moe_layer_forward_streamed, moe_rms_norm, moe_route,
+               moe_router_logits,
                moe_workspace_bytes, rvq_ws_clear, rvq_ws_status)
 
 
@@ -148,10 +149,16 @@ class MoeStack:
         bufs = self.buffers(n)
         h = x
         for i, L in enumerate(self.layers):
-            moe_rms_norm(h, n, L.d, bufs[i]["xn"], eps=self.eps)
-            L.forward(bufs[i]["xn"], bufs[i], events=events if i == 0 else None,
-                      tc_min_tokens=tc_min_tokens, residual=h)
-            h = bufs[i]["out"]
+            b = bufs[i]
+            if events is not None and i == 0:
+                # per-kernel timing marks: the norm and the layer as separate calls
+                moe_rms_norm(h, n, L.d, b["xn"], eps=self.eps)
+                L.forward(b["xn"], b, events=events, tc_min_tokens=tc_min_tokens, residual=h)
+            else:
+                moe_layer_forward_prenorm(L.bank, L.wr, L.bias, h, n, L.k, self.eps, b["xn"],
+                                          b["logits"], b["idx"], b["w"], b["offsets"], b["pairs"],
+                                          b["out"], b["ws"], tc_min_tokens=tc_min_tokens)
+            h = b["out"]
         return bufs
 
 

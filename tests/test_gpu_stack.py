@@ -119,3 +119,32 @@ def test_k3_prefill_chunk_through_two_layers():
         sl.forget()
     del stack, bufs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n,hdt", [(1, torch.float32), (1, torch.bfloat16), (5, torch.float32)])
+def test_prenorm_call_equals_norm_then_layer(n, hdt):
+    """moe_layer_forward_prenorm (one token: the norm inside the router
+    launch; more tokens: the norm kernel first) gives bit for bit what
+    moe_rms_norm followed by moe_layer_forward_ex gives: xn, logits,
+    routing and out (d = 2048 layer, fp32 and bf16 streams)."""
+    sl = SynthLayer(1, 0)
+    L = sl.to_gpu()
+    rng = np.random.default_rng(n)
+    h = torch.from_numpy((rng.normal(size=(n, L.d)) * 3).astype(np.float32)).to(DEV).to(hdt)
+    eps = 1e-6
+    ref = L.buffers(n)
+    ref["xn"] = torch.empty((n, L.d), dtype=torch.bfloat16, device=DEV)
+    rvq.moe_rms_norm(h, n, L.d, ref["xn"], eps=eps)
+    L.forward(ref["xn"], ref, residual=h)
+    got = L.buffers(n)
+    got["xn"] = torch.empty((n, L.d), dtype=torch.bfloat16, device=DEV)
+    rvq.moe_layer_forward_prenorm(L.bank, L.wr, L.bias, h, n, L.k, eps, got["xn"], got["logits"],
+                                  got["idx"], got["w"], got["offsets"], got["pairs"], got["out"],
+                                  got["ws"])
+    torch.cuda.synchronize()
+    assert L.status(n) == (0, 0)
+    for key in ("xn", "logits", "idx", "w", "offsets", "pairs", "out"):
+        a, b = got[key], ref[key]
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
+    sl.forget()
