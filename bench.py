@@ -433,7 +433,9 @@ def run_gpu(args, rank, world, local_rank):
                           else len(KERNELS) + TC_LAUNCHES_PER_STEP - 3)
                          + router_launches(batch, s.E, s.d) - 1
                          # a stack's pre-norm: inside the router launch for one token
-                         + (1 if n_layers > 1 and batch > 1 else 0)) * args.steps * n_layers,
+                         + (1 if n_layers > 1 and batch > 1 else 0)
+                         # decode batches on lookup tables: the pair plan inside the routing launch
+                         - (1 if tc_min == 0 and batch <= 16 else 0)) * args.steps * n_layers,
                config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
     del L, stack, built
     return res

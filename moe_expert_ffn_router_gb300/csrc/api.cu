@@ -468,7 +468,8 @@ static LutJob ffn_job(const rvq_moe_bank *bank, const RecordLayout &L, int n_pai
 rvq_status rvq::run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                    int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev, void *ws_dev,
                    const FfnPlan &P, cudaStream_t st, void **marks, bool pdl,
-                   int32_t tc_min_tokens, const int32_t *slot_of, int32_t n_records) {
+                   int32_t tc_min_tokens, const int32_t *slot_of, int32_t n_records,
+                   bool pairs_planned) {
     auto mark = [&](int i) -> rvq_status {
         if (marks) RVQ_CUDA(cudaEventRecord((cudaEvent_t)marks[i], st));
         return RVQ_OK;
@@ -520,19 +521,19 @@ rvq_status rvq::run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype x
     dn.pairs = pairs_dev;
     dn.desc = (ItemDesc *)(ws + P.off_desc_d);
     gu.tc_min_tokens = dn.tc_min_tokens = tc_min_tokens;
-    if (P.C_gu == 1 && P.C_d == 1 && n <= 16) {
+    if (decode_pair_plan(P, n)) {
         // decode batches up to 16 tokens: one-token units with the table build
         // interleaved into the streaming (measured faster than two-token items
         // up to 16 tokens, slower from 32); the pair plan reuses the gate/up
         // descriptor space (>= n_pairs x 16 bytes)
         int4 *pd = (int4 *)(ws + P.off_desc_gu);
-        RVQ_TRY(launch_lut_plan_pairs(gu, pd, st, pdl));
+        if (!pairs_planned) RVQ_TRY(launch_lut_plan_pairs(gu, pd, st, pdl));
         RVQ_TRY(mark(0));
         RVQ_TRY(launch_lut_gemv_il(gu, pd, st, pdl));
         RVQ_TRY(mark(1));
         RVQ_TRY(launch_swiglu_reduce(gpart, upart, np, P.nslot_gu, bank->f, h, st, pdl));
         RVQ_TRY(mark(2));
-        dn.early_start = 1;  // the plan is three launches back; only h is new
+        dn.early_start = 1;  // the plan is three launches back (or more); only h is new
         RVQ_TRY(launch_lut_gemv_il(dn, pd, st, pdl));
         return mark(3);
     }
@@ -746,13 +747,20 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
         if (events) RVQ_CUDA(cudaEventRecord((cudaEvent_t)events[i], st));
         return RVQ_OK;
     };
+    // decode batches on the lookup-table path: the routing block also writes
+    // the GEMV's pair plan (one launch less on the critical path)
+    const bool fuse_plan = tc_min_tokens <= 0 && n <= 64 && decode_pair_plan(P, n);
+    LutJob plan = {};
+    if (fuse_plan)
+        plan = ffn_job(bank, record_layout(bank->d, bank->f), n * k, ws_dev, nullptr, 0);
     RVQ_TRY(launch_route(logits_dev, n, bank->n_experts, k, topk_idx_dev, topk_w_dev, offsets_dev,
-                         pairs_dev, (uint32_t *)ws_dev, st, pdl));
+                         pairs_dev, (uint32_t *)ws_dev, st, pdl, fuse_plan ? &plan : nullptr,
+                         fuse_plan ? (int4 *)((uint8_t *)ws_dev + P.off_desc_gu) : nullptr));
     RVQ_TRY(mark(2));
     if (tc_min_tokens <= 0) {
         // lookup-table path only; the down partials are reduced inside the combine
         RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st,
-                        events ? events + 3 : nullptr, pdl));
+                        events ? events + 3 : nullptr, pdl, 0, nullptr, 0, fuse_plan));
         float *dpart = (float *)((uint8_t *)ws_dev + P.off_dpart);
         RVQ_TRY(launch_combine(dpart, P.nslot_d, topk_w_dev, n, k, bank->d, residual_dev,
                                (int)rdt, out_dev, st, pdl));

@@ -206,9 +206,13 @@ rvq_status launch_router_logits(const float *wr, const float *bias, const void *
 rvq_status launch_router_norm_logits(const float *wr, const float *bias, const void *h, int hdt,
                                      int E, int d, float eps, uint16_t *xn, float *logits,
                                      cudaStream_t stream);
+// With `plan` (n <= 64 only), the routing block also writes the decode
+// GEMV's pair descriptors pd[position] = pair_desc(plan, ...) (the plan's
+// tc_min_tokens must be <= 0), so no separate plan launch is needed.
 rvq_status launch_route(const float *logits, int n, int E, int k, int32_t *idx, float *w,
                         int32_t *offsets, int32_t *pairs, uint32_t *status,
-                        cudaStream_t stream, bool pdl);
+                        cudaStream_t stream, bool pdl, const LutJob *plan = nullptr,
+                        int4 *pd = nullptr);
 int route_max_tokens(int E);
 rvq_status launch_pack(const uint8_t *src, int rows, int cols, uint8_t *dst, bool unpack,
                        cudaStream_t stream);
@@ -249,6 +253,29 @@ __device__ __forceinline__ int record_of(const J &job, int e) {
     const int s = job.slot_of[e];
     return (s >= 0 && s < job.n_records) ? s : -1;
 }
+// The decode GEMV's descriptor of one sorted (expert e, group size ne) pair
+// entry: {record index, entry, 0, 0}, or {-1, ...} for a pair the tensor-core
+// path takes or one that cannot be used (a bad entry sets RVQ_DEV_ERR_INDEX; a
+// missing record or a header that does not match sets RVQ_DEV_ERR_CORRUPT).
+__device__ __forceinline__ int4 pair_desc(const LutJob &job, int e, int ne, int entry) {
+    int4 d = make_int4(-1, 0, 0, 0);
+    if (entry < 0 || entry >= job.n_pairs) {
+        set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
+        return d;
+    }
+    if (job.tc_min_tokens > 0 && ne >= job.tc_min_tokens) return d;
+    const int rec = record_of(job, e);
+    const rvq_expert_header *h = rec < 0 ? nullptr :
+        reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)rec * job.record_bytes);
+    if (rec < 0 ||
+        (job.check_header &&
+         (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer || h->d != job.d ||
+          h->f != job.f || h->record_bytes != job.record_bytes)))
+        set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
+    else
+        d = make_int4(rec, entry, 0, 0);
+    return d;
+}
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
 // offline residual k-means encoder (encode.cu)
 size_t encode_workspace_bytes(int rows, int cols);
@@ -285,7 +312,12 @@ rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, i
                    int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev, void *ws_dev,
                    const FfnPlan &P, cudaStream_t st, void **marks, bool pdl,
                    int32_t tc_min_tokens = 0, const int32_t *slot_of = nullptr,
-                   int32_t n_records = 0);
+                   int32_t n_records = 0, bool pairs_planned = false);
+// run_ffn takes the interleaved decode GEMV with a per-pair plan for these
+// shapes; pairs_planned = the routing launch already wrote that plan.
+inline bool decode_pair_plan(const FfnPlan &P, int n) {
+    return P.C_gu == 1 && P.C_d == 1 && n <= 16;
+}
 rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                       int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
                       void *ws_dev, const FfnPlan &P, float *y_pair, int32_t tc_min_tokens,

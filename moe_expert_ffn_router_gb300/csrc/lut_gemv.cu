@@ -629,24 +629,12 @@ __global__ void __launch_bounds__(256) plan_pairs_kernel(const LutJob job, int4 
     }
     const int e = lo, ne = soff[e + 1] - soff[e];
     const int entry = job.pairs[p];
-    if (!(soff[e] <= p && p < soff[e + 1]) || entry < 0 || entry >= job.n_pairs) {
+    // {record index (an expert cache's slot), entry}: the walkers address the
+    // record by it
+    if (!(soff[e] <= p && p < soff[e + 1]))
         set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
-    } else if (job.tc_min_tokens > 0 && ne >= job.tc_min_tokens) {
-        // the tensor-core path takes this expert
-    } else {
-        // {record index (an expert cache's slot), entry}: the walkers address
-        // the record by it
-        const int rec = record_of(job, e);
-        const rvq_expert_header *h = rec < 0 ? nullptr :
-            reinterpret_cast<const rvq_expert_header *>(job.base + (uint64_t)rec * job.record_bytes);
-        if (rec < 0 ||
-            (job.check_header &&
-             (h->magic != RVQ_BANK_MAGIC || h->expert != e || h->layer != job.layer ||
-              h->d != job.d || h->f != job.f || h->record_bytes != job.record_bytes)))
-            set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
-        else
-            d = make_int4(rec, entry, 0, 0);
-    }
+    else
+        d = pair_desc(job, e, ne, entry);
     pd[p] = d;
 }
 

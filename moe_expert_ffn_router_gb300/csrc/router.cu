@@ -371,7 +371,8 @@ __global__ void __launch_bounds__(NT, 1) route_kernel(const float *__restrict__ 
                                                       float *__restrict__ wout,
                                                       int32_t *__restrict__ offsets,
                                                       int32_t *__restrict__ pairs,
-                                                      uint32_t *status) {
+                                                      uint32_t *status, const LutJob plan,
+                                                      int4 *__restrict__ pd) {
     constexpr int NWARP = NT / 32;
     extern __shared__ __align__(16) uint32_t rsm[];
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -467,6 +468,9 @@ __global__ void __launch_bounds__(NT, 1) route_kernel(const float *__restrict__ 
             const size_t wi = (size_t)e * W + (t >> 5);
             const int pos = cnt[e] + pre[wi] + __popc(mask[wi] & ((1u << (t & 31)) - 1u));
             pairs[pos] = t * k + lane;
+            // the decode plan's descriptor of this position (group sizes are
+            // not needed: the plan's tc_min_tokens is <= 0)
+            if (pd) pd[pos] = pair_desc(plan, e, 0, t * k + lane);
         }
     }
 }
@@ -550,7 +554,7 @@ rvq_status launch_router_norm_logits(const float *wr, const float *bias, const v
 template <int NT, bool SELECT>
 rvq_status launch_route_nt(const float *logits, int n, int E, int k, int32_t *idx, float *w,
                            int32_t *offsets, int32_t *pairs, uint32_t *status,
-                           cudaStream_t stream, bool pdl) {
+                           cudaStream_t stream, bool pdl, const LutJob *plan, int4 *pd) {
     static std::atomic<int> attr_done[64];  // per device; setting twice is harmless
     int dev = 0;
     RVQ_CUDA(cudaGetDevice(&dev));
@@ -570,17 +574,22 @@ rvq_status launch_route_nt(const float *logits, int n, int E, int k, int32_t *id
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    const LutJob none = {};
     RVQ_CUDA(cudaLaunchKernelEx(&cfg, route_kernel<NT, SELECT>, logits, n, E, k, idx, w, offsets,
-                                pairs, status));
+                                pairs, status, plan ? *plan : none, plan ? pd : nullptr));
     return RVQ_OK;
 }
 
 rvq_status launch_route(const float *logits, int n, int E, int k, int32_t *idx, float *w,
                         int32_t *offsets, int32_t *pairs, uint32_t *status, cudaStream_t stream,
-                        bool pdl) {
+                        bool pdl, const LutJob *plan, int4 *pd) {
+    if (plan && (n > 64 || !pd || plan->tc_min_tokens > 0)) {
+        set_error("route: the fused pair plan needs n <= 64, pd and no tensor-core dispatch");
+        return RVQ_EINVAL;
+    }
     if (n <= 64)
         return launch_route_nt<256, true>(logits, n, E, k, idx, w, offsets, pairs, status, stream,
-                                          pdl);
+                                          pdl, plan, pd);
     // larger batches: the selection spreads over the grid, the grouping stays in one block
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((n + 7) / 8));
@@ -593,7 +602,7 @@ rvq_status launch_route(const float *logits, int n, int E, int k, int32_t *idx, 
     cfg.numAttrs = pdl ? 1 : 0;
     RVQ_CUDA(cudaLaunchKernelEx(&cfg, route_select_kernel, logits, n, E, k, idx, w, status));
     return launch_route_nt<1024, false>(logits, n, E, k, idx, w, offsets, pairs, status, stream,
-                                        pdl);
+                                        pdl, nullptr, nullptr);
 }
 
 }  // namespace rvq
