@@ -73,6 +73,11 @@ ENCODE_WORKLOADS = {
     "k3_encode_2048x7168_iters8": (2048, 7168, 8),
 }
 ENCODE_UNIT = "Mweights/s"
+# one RVQ matrix times one input vector: (rows, cols, n); the 73.7 KB of codes
+# and codebooks stay in L2, so the call is bound by launch latency, not HBM
+GEMV_WORKLOADS = {
+    "gemv_256x512": (256, 512, 1),
+}
 ENCODE_METRIC = "offline RVQ encoder: weights encoded per second (3 stages x 256 codewords)"
 KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
            "lut_gemv_down", "combine"]
@@ -442,25 +447,97 @@ def run_gpu(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_sample(config, tokens, src=None, shape=None):
-    """Time the oracle (as it stands, one thread) on `tokens` tokens through the
-    whole oracle layer.  Returns seconds per token."""
-    import oracle
-    import synth
-    s = shape or W.WORKLOADS[config].shape
-    src = src or W.ExpertSource(config, 0, s)
-    wr = src.router_weight()
-    bias = router_bias(config, src)
-    x64 = synth.bf16_to_f32(src.tokens_bf16(tokens)).astype(np.float64)
-    lg = oracle.router_logits(wr, x64, bias).astype(np.float32)
-    idx, _, _ = oracle.route(lg, s.k)
-    cache = {}
-    for e in sorted(set(idx.reshape(-1).tolist())):
-        cache[e] = tuple((src.codes(e, m), src.codebooks(e, m)) for m in range(3))
-    t0 = time.perf_counter()
-    for t in range(tokens):
-        oracle.moe_layer(lambda e: cache[e], wr, x64[t:t + 1], s.k, s.d, s.f, bias=bias)
-    return (time.perf_counter() - t0) / tokens
+def host_cores():
+    """Host cores this process may run on (its CPU affinity)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleBatch:
+    """One batch of the workload through the oracle as it stands: router
+    logits and top-k for the batch, every (token, expert) pair's expert FFN
+    (explicit dequantisation, fp64 matmuls), the weighted combine.  The pairs
+    run on a thread pool in this harness (the C oracle releases the GIL); the
+    oracle itself is single-threaded code."""
+
+    def __init__(self, config, shape, tokens_bf16):
+        import oracle
+        import synth
+        self.oracle = oracle
+        self.s = s = shape
+        self.src = src = W.ExpertSource(config, 0, s)
+        self.wr = src.router_weight()
+        self.bias = router_bias(config, src)
+        self.x64 = synth.bf16_to_f32(tokens_bf16).astype(np.float64)
+        lg = oracle.router_logits(self.wr, self.x64, self.bias).astype(np.float32)
+        self.idx, _, _ = oracle.route(lg, s.k)
+        self.mats = {}
+
+    def experts(self, rows):
+        """Generate (outside any timing) the experts the given tokens route to."""
+        for t in rows:
+            for e in self.idx[t]:
+                e = int(e)
+                if e not in self.mats:
+                    self.mats[e] = tuple((self.src.codes(e, m), self.src.codebooks(e, m))
+                                         for m in range(3))
+
+    def run(self, rows, pairs=None, threads=1):
+        """The oracle layer on tokens `rows` (all their pairs, or the first
+        `pairs` of them when given: a bounded sample).  Returns seconds."""
+        from concurrent.futures import ThreadPoolExecutor
+        o, s = self.oracle, self.s
+        self.experts(rows)
+        t0 = time.perf_counter()
+        x = self.x64[rows]
+        lg = o.router_logits(self.wr, x, self.bias).astype(np.float32)
+        idx, w, _ = o.route(lg, s.k)
+        work = [(i, int(e)) for i in range(len(rows)) for e in idx[i]]
+        if pairs is not None:
+            work = work[:pairs]
+
+        def ffn(item):
+            i, e = item
+            return o.expert_ffn(*self.mats[e], s.d, s.f, x[i])
+
+        if threads > 1:
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                ys = list(ex.map(ffn, work))
+        else:
+            ys = [ffn(it) for it in work]
+        if pairs is None:
+            o.combine(np.stack(ys), w, x)
+        return time.perf_counter() - t0
+
+
+def oracle_baseline(config, shape, batch, layers, uniq_mean, tokens_bf16):
+    """cpu_baseline of the GPU arm: the oracle on the host's cores (threads over
+    the (token, expert) pairs of one batch), and on one core (a sample of
+    pairs), scaled to the workload's batch, layers and distinct experts."""
+    s = shape
+    cores = host_cores()
+    pairs_batch = batch * s.k
+    ob = OracleBatch(config, s, tokens_bf16)
+    rows = list(range(min(batch, max(1, (4 * cores) // s.k))))
+    ob.experts(rows)
+    # all cores: whole tokens (every pair of each) while that stays bounded
+    t_all = ob.run(rows, threads=cores)
+    pairs_all = len(rows) * s.k
+    step_all = t_all / pairs_all * pairs_batch * layers
+    # one core: two pairs of the first token
+    t_one = ob.run([0], pairs=2, threads=1)
+    step_one = t_one / 2 * pairs_batch * layers
+    weights = uniq_mean * 3 * s.d * s.f
+    return {"value": round(weights / step_all / 1e9, 6), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "single_thread": {"value": round(weights / step_one / 1e9, 6), "cores": 1,
+                              "s_per_pair": round(t_one / 2, 3)},
+            "sample": f"{len(rows)} token(s), {pairs_all} (token, expert) pairs through the "
+                      f"oracle layer on {cores} threads ({t_all:.2f} s; one core: 2 pairs, "
+                      f"{t_one:.2f} s), scaled to the {batch}-token batch ({pairs_batch} pairs), "
+                      f"{layers} layer(s) and {uniq_mean:.1f} distinct experts per layer"}
 
 
 def oracle_unique_experts(config, batch, src, s):
@@ -474,60 +551,192 @@ def oracle_unique_experts(config, batch, src, s):
 
 
 def reference_arm(args, rank):
-    """The oracle as the reference implementation.  Each step evaluates m of
-    the (token, expert) pairs of one batch (all of them when the step budget
-    allows), so the whole --steps/--warmup run stays near a minute of CPU
-    time; a step's time is the measured time per pair times the batch's n k
-    pairs, and the value counts the distinct experts' weights of the batch,
-    as the GPU arm does."""
+    """The oracle as the reference implementation, on the host's cores (threads
+    over the (token, expert) pairs in this harness).  A step is one batch of
+    the workload through the oracle layer: every pair when the batch has at
+    most 4 pairs per core, otherwise a stated sample of 4 pairs per core
+    (value scaled to the whole batch).  steps / ms_per_step report what ran:
+    when the requested steps would take more than ~150 s, fewer run."""
     if rank != 0:
         return
-    import oracle
-    import synth
+    if args.workload in GEMV_WORKLOADS:
+        return reference_gemv(args)
     config, batch, s = workload_shape(args.workload)
     src = W.ExpertSource(config, 0, s)
-    per_pair_s = 1.4 * (s.d * s.f) / (7168 * 2048)  # measured on the GB300 host, one core
-    m = int(max(1, min(s.k * batch, 60.0 / ((args.steps + args.warmup) * per_pair_s))))
-    wr = src.router_weight()
-    bias = router_bias(config, src)
-    ntok = max(1, (args.steps + args.warmup) * m // s.k + 1)
-    x64 = synth.bf16_to_f32(src.tokens_bf16(ntok)).astype(np.float64)
-    idx, _, _ = oracle.route(oracle.router_logits(wr, x64, bias).astype(np.float32), s.k)
-    work = [(t, int(e)) for t in range(ntok) for e in idx[t]]
+    cores = host_cores()
     layers = W.WORKLOADS[config].n_layers
-    # distinct experts per batch: exact for one token; for a stack the first
-    # layer's count stands for every layer (independent seeds, same shape)
+    pool = max(8, args.steps + args.warmup)
+    bits = src.tokens_bf16(pool * batch).reshape(pool, batch, s.d)
+    full = batch * s.k <= 4 * cores
+    sample_pairs = None if full else 4 * cores
+    ob = OracleBatch(config, s, bits.reshape(-1, s.d))
     uniq = layers * (s.k if batch == 1 else oracle_unique_experts(config, batch, src, s))
-    times, npairs, pos = 0.0, 0, 0
-    for i in range(args.warmup + args.steps):
-        chunk = work[pos:pos + m]
-        pos += m
-        mats = {e: tuple((src.codes(e, q), src.codebooks(e, q)) for q in range(3))
-                for _, e in chunk}
-        t0 = time.perf_counter()
-        for t, e in chunk:
-            oracle.expert_ffn(*mats[e], s.d, s.f, x64[t])
-        dt = time.perf_counter() - t0
+    budget_s = 150.0
+    times, ran = [], 0
+    t_start = time.perf_counter()
+    total = args.warmup + args.steps
+    for i in range(total):
+        # the whole batch, or its first tokens up to 4 pairs per core
+        rows = list(range(i * batch, i * batch + (batch if full else
+                                                    max(1, sample_pairs // s.k))))
+        dt = ob.run(rows, pairs=sample_pairs, threads=cores)
         if i >= args.warmup:
-            times += dt
-            npairs += len(chunk)
-    step_s = times / npairs * batch * s.k * layers
+            times.append(dt)
+            ran += 1
+        elapsed = time.perf_counter() - t_start
+        if ran >= 1 and elapsed + dt > budget_s:  # the next step would pass the budget
+            break
+    per_step = float(np.mean(times))                    # seconds per step as run
+    npairs = batch * s.k if full else sample_pairs
+    step_s = per_step / npairs * batch * s.k * layers   # the whole batch, every layer
     value = uniq * 3 * s.d * s.f / step_s / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(step_s * 1e3, 2), "higher_is_better": True,
+            "n_gpus": args.gpus, "steps": ran, "warmup": args.warmup,
+            "steps_requested": args.steps, "ms_per_step": round(per_step * 1e3, 2),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload + ":" + W.WORKLOADS[config].name,
                        "batch": batch, "experts": s.E, "layers": layers},
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1,
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
                              "kind": "oracle",
-                             "sample": f"{m} (token, expert) pairs of the {batch * s.k} per "
-                                       "step timed (oracle expert FFN: explicit dequant + "
-                                       "fp64 matmuls), scaled to the whole batch; "
-                                       f"{uniq} distinct experts per batch"},
+                             "sample": (f"every step is one whole {batch}-token batch "
+                                        f"({batch * s.k} (token, expert) pairs) of layer 0"
+                                        if full else
+                                        f"every step is {sample_pairs} of the batch's "
+                                        f"{batch * s.k} (token, expert) pairs")
+                                       + f" on {cores} threads; value scaled to "
+                                       f"{layers} layer(s) and {uniq} distinct experts"
+                                       + ("" if full else " and the whole batch")},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def gemv_inputs(rows, cols, n):
+    """The single-matrix workload's seeded inputs: canonical codes, codebooks
+    and fp32 x (N(0, 1)), from the generator of the layer workloads."""
+    import synth
+    mseed = W.matrix_seed(W.layer_seed(0, 0), 0, 0)
+    codes = W.codes(mseed, rows, cols)
+    cb = W.codebooks(mseed)
+    x = W.tokens_f32(W.layer_seed(0, 0), n, cols)
+    return codes, cb, x
+
+
+def run_gemv(args, rank, world, local_rank):
+    """rvq_gemv on one 256 x 512 matrix (fp32 input, batch 1) per step: the
+    single-GEMV configuration.  L2-resident, so the figure is latency, not a
+    fraction of HBM bandwidth (reported as such)."""
+    import torch
+    import moe_expert_ffn_router_gb300 as rvq
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    rows, cols, n = GEMV_WORKLOADS[args.workload]
+    codes, cb, x = gemv_inputs(rows, cols, n)
+    packed = torch.empty(rvq.rvq_code_bytes(rows, cols), dtype=torch.uint8, device=dev)
+    rvq.rvq_pack(torch.from_numpy(codes).to(dev), rows, cols, packed)
+    cbp = torch.empty(6144, dtype=torch.float32, device=dev)
+    rvq.rvq_pack_codebooks(torch.from_numpy(cb).to(dev), cbp)
+    xd = torch.from_numpy(x).to(dev)
+    y = torch.empty((n, rows), dtype=torch.float32, device=dev)
+    ws = torch.empty(rvq.rvq_gemv_workspace_bytes(rows, cols, n), dtype=torch.uint8, device=dev)
+    rvq.rvq_ws_clear(ws)
+    for _ in range(args.warmup):
+        rvq.rvq_gemv(packed, cbp, rows, cols, xd, n, y, ws)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    t0w = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        rvq.rvq_gemv(packed, cbp, rows, cols, xd, n, y, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    t1w = time.perf_counter()
+    sampler.stop()
+    ms = replica_max_ms(e0.elapsed_time(e1), world, dev)
+    rc, bits = rvq.rvq_ws_status(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits:#x}")
+    # end to end: x from pinned host memory, y back, each step
+    xh = torch.from_numpy(x).pin_memory()
+    yh = torch.empty((n, rows), dtype=torch.float32).pin_memory()
+    e0.record()
+    for _ in range(args.steps):
+        xd.copy_(xh, non_blocking=True)
+        rvq.rvq_gemv(packed, cbp, rows, cols, xd, n, y, ws)
+        yh.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = replica_max_ms(e0.elapsed_time(e1), world, dev)
+    weights = rows * cols * n
+    us = ms / args.steps * 1e3
+    algo_bytes = 3 * rows * cols // 8 + rvq.RVQ_CODEBOOK_BYTES + n * cols * 4
+    peak, peak_kind = load_peaks()
+    ach = algo_bytes / (us / 1e6) / 1e9
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        reps = 20
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle.rvq_gemv(codes, cb, rows, cols, x.astype(np.float64))
+        dt = (time.perf_counter() - t0) / reps
+        cpu = {"value": round(weights / dt / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the oracle GEMV (explicit dequant, fp64) on the same matrix, "
+                         f"{reps} calls, {dt * 1e3:.2f} ms per call"}
+    line = {
+        "metric": METRIC, "value": round(job_rate(weights * args.steps, world, ms) / 1e9, 3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5), "us_per_call": round(us, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload + ":" + W.WORKLOADS[0].name, "rows": rows,
+                   "cols": cols, "batch": n,
+                   "l2": "L2-resident: 73.7 KB of codes and codebooks, reused every step",
+                   "parallelism": f"replicas{world}", "path": "fp32 lookup tables"},
+        "roofline": {"bound": "hbm", "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(ach / peak, 5), "peak_source": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "note": "L2-resident and launch-latency bound: the fraction is "
+                             "reported, not a target"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(job_rate(weights * args.steps, world, ms_e2e) / 1e9, 3),
+                "unit": UNIT, "h2d_bytes_per_step": n * cols * 4,
+                "d2h_bytes_per_step": n * rows * 4,
+                "note": "x copied from pinned host memory and y back around each call"},
+        "clocks": sampler.summary(t0w, t1w),
+        # plan, GEMV, slot reduction
+        "gpu_launches": 3 * args.steps * world,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def reference_gemv(args):
+    """The oracle GEMV (explicit dequantisation, fp64 dot products) per step."""
+    import oracle
+    rows, cols, n = GEMV_WORKLOADS[args.workload]
+    codes, cb, x = gemv_inputs(rows, cols, n)
+    x64 = x.astype(np.float64)
+    for _ in range(args.warmup):
+        oracle.rvq_gemv(codes, cb, rows, cols, x64)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.rvq_gemv(codes, cb, rows, cols, x64)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = rows * cols * n / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": rows, "cols": cols, "batch": n},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "the whole workload, every step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
 
 
 def run_stream(args, rank, world, local_rank):
@@ -740,7 +949,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=None, help="untimed steps (default 10; 3)")
     ap.add_argument("--workload", default="k3_decode_b1",
                     choices=sorted(WORKLOADS) + sorted(STREAM_WORKLOADS) +
-                    sorted(ENCODE_WORKLOADS))
+                    sorted(ENCODE_WORKLOADS) + sorted(GEMV_WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--oracle-tokens", type=int, default=4)
     ap.add_argument("--tc-min-tokens", type=int, default=None,
@@ -779,6 +988,9 @@ def main():
         return
     if args.workload in ENCODE_WORKLOADS:
         run_encode(args, rank, world, local_rank)
+        return
+    if args.workload in GEMV_WORKLOADS:
+        run_gemv(args, rank, world, local_rank)
         return
     if args.workload in STREAM_WORKLOADS:
         run_stream(args, rank, world, local_rank)

@@ -153,18 +153,28 @@ rvq_status rvq_gemv(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
  * workspace: the split-K scratch is a fixed RVQ_NOALLOC_SCRATCH_BYTES device
  * array inside the library, held by every GPU that loads the library until
  * the process exits.  Calls no cudaMalloc/cudaFree or allocating routine.
- *  - Returns RVQ_ENOMEM, launching nothing, when rows x cols x n would need
- *    more scratch than the fixed maximum (rvq_gemv_workspace_bytes > max).
- *  - The first call on a device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *  - Argument checks as rvq_gemv (EINVAL / EALIGN), then RVQ_ENOMEM when
+ *    rows x cols x n would need more scratch than the fixed maximum
+ *    (rvq_gemv_workspace_bytes > max).  A rejected call launches nothing.
+ *  - The first call on a device (and the first after the device's context
+ *    was replaced, e.g. by cudaDeviceReset) looks up the array's device
+ *    address with that device current; make that first call before any
+ *    stream capture.
  *  - Every call shares the one array: calls whose work overlaps on the GPU
  *    (other streams, other threads) race and give wrong results; serialise
- *    them.  Each call clears the status block it needs at the start.
+ *    them.  Each call clears the status block it needs at the start, so a
+ *    call's device status must be read before the next call.
+ * rvq_gemv_noalloc_status: synchronous; waits for `stream`, then reads the
+ * device status word of the array (what rvq_ws_status reads from a
+ * workspace) and returns RVQ_OK, RVQ_EDEVICE, RVQ_ECORRUPT or RVQ_ETIMEOUT,
+ * storing the raw bits in *bits_out if not NULL and clearing them.  The GEMV
+ * sets a bit only when one of its bounded waits expires (RVQ_ETIMEOUT).
  * ------------------------------------------------------------------------ */
 #define RVQ_NOALLOC_SCRATCH_BYTES 4194304u /* 4 MiB */
 rvq_status rvq_gemv_noalloc(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
                             int32_t rows, int32_t cols, const void *x_dev, rvq_dtype xdt,
                             int32_t n, float *y_dev, rvq_stream_t stream);
+rvq_status rvq_gemv_noalloc_status(uint32_t *bits_out, rvq_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * Offline RVQ encoder: the pages' conversion step (GeekNews topic 32035,
@@ -416,6 +426,24 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
                                 float *out_dev, void *ws_dev, size_t ws_bytes,
                                 const void *residual_dev, rvq_dtype rdt, int32_t tc_min_tokens,
                                 void **events, rvq_stream_t stream);
+
+/* One whole MoE layer with its input and output in host memory, for callers
+ * whose tokens arrive from and leave to the host: one cudaMemcpyAsync of
+ * x_host (n x d of xdt) into x_dev, the layer of moe_layer_forward_ex (x is
+ * also the residual; no event marks), and one cudaMemcpyAsync of out (fp32
+ * n x d) from out_dev back to out_host, all on `stream` and asynchronous:
+ * synchronise the stream before reading out_host.  Pinned host buffers let
+ * the copies run asynchronously; pageable ones work, with the driver's
+ * staging.  x_dev (dev, >= n x d x sizeof(xdt) bytes, 16-byte aligned) and
+ * the other device buffers are the caller's, as in moe_layer_forward_ex.
+ * Every argument is checked before the first copy (EINVAL / EALIGN / ENOMEM,
+ * nothing queued). */
+rvq_status moe_layer_forward_host(const rvq_moe_bank *bank, const float *wr_dev,
+                                  const float *bias_dev, const void *x_host, rvq_dtype xdt,
+                                  int32_t n, int32_t k, void *x_dev, float *logits_dev,
+                                  int32_t *topk_idx_dev, float *topk_w_dev, int32_t *offsets_dev,
+                                  int32_t *pairs_dev, float *out_dev, float *out_host, void *ws_dev,
+                                  size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream);
 
 /* A pre-norm layer of a stack in one call: xn = bf16(h / sqrt(mean(h^2) +
  * eps)) row by row (the values moe_rms_norm gives), then moe_layer_forward_ex

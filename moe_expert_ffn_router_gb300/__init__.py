@@ -68,6 +68,7 @@ _SIGS = {
     "rvq_gemv_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "rvq_gemv": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
     "rvq_gemv_noalloc": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp]),
+    "rvq_gemv_noalloc_status": (_i32, [ctypes.POINTER(_u32), _vp]),
     "moe_bank_record_bytes": (_u64, [_i32, _i32]),
     "moe_bank_init": (_i32, [_BANKP, _vp, _u64, _i32, _i32, _i32, _i32]),
     "moe_bank_write_expert": (_i32, [_BANKP, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -96,6 +97,8 @@ _SIGS = {
                                  _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_layer_forward_ex": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp,
                                     _vp, _vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp]),
+    "moe_layer_forward_host": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
     "moe_layer_forward_prenorm": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
     "moe_rms_norm": (_i32, [_vp, _i32, _i32, _i32, ctypes.c_float, _vp, _i32, _vp]),
@@ -210,6 +213,14 @@ def rvq_gemv_noalloc(packed_codes, packed_cb, rows, cols, x, n, y, stream=None):
     _check("rvq_gemv_noalloc",
            _lib.rvq_gemv_noalloc(_p(packed_codes), _p(packed_cb), rows, cols, _p(x), _dt(x), n,
                                  _p(y), _stream(stream)))
+
+
+def rvq_gemv_noalloc_status(stream=None) -> tuple[int, int]:
+    """Device status of the no-allocation GEMV's fixed array: (status code,
+    raw bits) after the stream's work; clears the bits."""
+    bits = _u32(0)
+    rc = _lib.rvq_gemv_noalloc_status(ctypes.byref(bits), _stream(stream))
+    return int(rc), int(bits.value)
 
 
 # ------------------------------------------------------------------ bank
@@ -345,6 +356,22 @@ def moe_layer_forward(bank, wr, bias, x, n, k, logits, topk_idx, topk_w, offsets
                                      _p(logits), _p(topk_idx), _p(topk_w), _p(offsets),
                                      _p(pairs), _p(out), _p(ws), _nbytes(ws), _p(residual), rdt,
                                      int(tc_min_tokens), ev, _stream(stream)))
+
+
+def moe_layer_forward_host(bank, wr, bias, x_host, n, k, x_dev, logits, topk_idx, topk_w,
+                           offsets, pairs, out, out_host, ws, tc_min_tokens=0, stream=None):
+    """The layer with x read from and out written to host tensors (pinned for
+    asynchronous copies); x_dev is the device copy of x.  Asynchronous."""
+    assert not x_host.is_cuda and not out_host.is_cuda and x_host.dtype == x_dev.dtype
+    assert x_host.is_contiguous() and out_host.is_contiguous()
+    assert out_host.dtype == torch.float32 and out_host.numel() >= n * out.shape[-1]
+    _check("moe_layer_forward_host",
+           _lib.moe_layer_forward_host(ctypes.byref(bank), _p(wr), _p(bias),
+                                       ctypes.c_void_p(x_host.data_ptr()), _dt(x_dev), n, k,
+                                       _p(x_dev), _p(logits), _p(topk_idx), _p(topk_w),
+                                       _p(offsets), _p(pairs), _p(out),
+                                       ctypes.c_void_p(out_host.data_ptr()), _p(ws), _nbytes(ws),
+                                       int(tc_min_tokens), _stream(stream)))
 
 
 def moe_layer_forward_prenorm(bank, wr, bias, h, n, k, eps, xn, logits, topk_idx, topk_w, offsets,

@@ -215,18 +215,54 @@ size_t rvq_gemv_workspace_bytes(int32_t rows, int32_t cols, int32_t n) {
            align256(items * sizeof(ItemDesc));
 }
 
+}  // extern "C"
+
+// Host-side argument checks of rvq_gemv (every one runs before any launch);
+// also used by rvq_gemv_noalloc, which has no workspace argument.
+rvq_status rvq::check_gemv_args(const char *who, const uint8_t *packed_codes_dev,
+                                const float *packed_cb_dev, int32_t rows, int32_t cols,
+                                const void *x_dev, rvq_dtype xdt, int32_t n, const float *y_dev) {
+    CHECK_ARG(packable(rows, cols), "%s: rows %d must be a multiple of 32 and cols %d of 512", who,
+              rows, cols);
+    CHECK_ARG(n >= 1, "%s: n %d", who, n);
+    CHECK_ARG(packed_codes_dev && packed_cb_dev && x_dev && y_dev, "%s: null pointer", who);
+    CHECK_ARG(xdt == RVQ_F32 || xdt == RVQ_BF16, "%s: dtype %d", who, (int)xdt);
+    const void *ptrs[3] = {packed_codes_dev, packed_cb_dev, x_dev};
+    const char *names[3] = {"codes", "codebooks", "x"};
+    for (int i = 0; i < 3; ++i)
+        if (!aligned16(ptrs[i])) {
+            set_error("%s: %s pointer %p is not 16-byte aligned", who, names[i], ptrs[i]);
+            return RVQ_EALIGN;
+        }
+    return RVQ_OK;
+}
+
+// Reads (and, when nonzero, clears) a device status word after the stream's
+// work: RVQ_OK, RVQ_ECORRUPT, RVQ_ETIMEOUT or RVQ_EDEVICE.
+rvq_status rvq::read_status_word(void *status_dev, uint32_t *bits_out, cudaStream_t st) {
+    uint32_t bits = 0;
+    RVQ_CUDA(cudaMemcpyAsync(&bits, status_dev, 4, cudaMemcpyDeviceToHost, st));
+    RVQ_CUDA(cudaStreamSynchronize(st));
+    if (bits_out) *bits_out = bits;
+    if (bits) {
+        RVQ_CUDA(cudaMemsetAsync(status_dev, 0, 4, st));
+        RVQ_CUDA(cudaStreamSynchronize(st));
+        set_error("device status bits 0x%x", bits);
+        if (bits & RVQ_DEV_ERR_CORRUPT) return RVQ_ECORRUPT;
+        if (bits & RVQ_DEV_ERR_TIMEOUT) return RVQ_ETIMEOUT;
+        return RVQ_EDEVICE;
+    }
+    return RVQ_OK;
+}
+
+extern "C" {
+
 rvq_status rvq_gemv(const uint8_t *packed_codes_dev, const float *packed_cb_dev, int32_t rows,
                     int32_t cols, const void *x_dev, rvq_dtype xdt, int32_t n, float *y_dev,
                     void *ws_dev, size_t ws_bytes, rvq_stream_t stream) {
-    CHECK_ARG(packable(rows, cols), "rvq_gemv: rows %d must be a multiple of 32 and cols %d of 512",
-              rows, cols);
-    CHECK_ARG(n >= 1, "rvq_gemv: n %d", n);
-    CHECK_ARG(packed_codes_dev && packed_cb_dev && x_dev && y_dev && ws_dev,
-              "rvq_gemv: null pointer");
-    CHECK_ARG(xdt == RVQ_F32 || xdt == RVQ_BF16, "rvq_gemv: dtype %d", (int)xdt);
-    CHECK_ALIGN(packed_codes_dev, "rvq_gemv: codes");
-    CHECK_ALIGN(packed_cb_dev, "rvq_gemv: codebooks");
-    CHECK_ALIGN(x_dev, "rvq_gemv: x");
+    RVQ_TRY(check_gemv_args("rvq_gemv", packed_codes_dev, packed_cb_dev, rows, cols, x_dev, xdt, n,
+                            y_dev));
+    CHECK_ARG(ws_dev, "rvq_gemv: null workspace");
     CHECK_ALIGN(ws_dev, "rvq_gemv: workspace");
     const size_t need = rvq_gemv_workspace_bytes(rows, cols, n);
     if (ws_bytes < need) {
@@ -594,7 +630,7 @@ rvq_status rvq::run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtyp
     dn.rows = bank->d;
     dn.cols = bank->f;
     dn.x = ws + P.off_h16;
-    dn.x_dtype = RVQ_BF16;
+    dn.x_dtype = PF_H_F16;
     dn.x_stride = bank->f;
     dn.x_div = 1;
     dn.out = y_pair;
@@ -749,7 +785,7 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
     };
     // decode batches on the lookup-table path: the routing block also writes
     // the GEMV's pair plan (one launch less on the critical path)
-    const bool fuse_plan = tc_min_tokens <= 0 && n <= 64 && decode_pair_plan(P, n);
+    const bool fuse_plan = tc_min_tokens <= 0 && decode_pair_plan(P, n);
     LutJob plan = {};
     if (fuse_plan)
         plan = ffn_job(bank, record_layout(bank->d, bank->f), n * k, ws_dev, nullptr, 0);
@@ -783,6 +819,32 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
     RVQ_TRY(launch_combine(ypair, 1, topk_w_dev, n, k, bank->d, residual_dev, (int)rdt, out_dev,
                            st, pdl));
     return mark(7);
+}
+
+rvq_status moe_layer_forward_host(const rvq_moe_bank *bank, const float *wr_dev,
+                                  const float *bias_dev, const void *x_host, rvq_dtype xdt,
+                                  int32_t n, int32_t k, void *x_dev, float *logits_dev,
+                                  int32_t *topk_idx_dev, float *topk_w_dev, int32_t *offsets_dev,
+                                  int32_t *pairs_dev, float *out_dev, float *out_host, void *ws_dev,
+                                  size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream) {
+    CHECK_ARG(bank && x_host && out_host && x_dev && out_dev, "moe_layer_forward_host: null pointer");
+    CHECK_ARG(n >= 1 && bank->d > 0, "moe_layer_forward_host: n %d", n);
+    CHECK_ARG(xdt == RVQ_F32 || xdt == RVQ_BF16, "moe_layer_forward_host: dtype %d", (int)xdt);
+    CHECK_ALIGN(x_dev, "moe_layer_forward_host: x_dev");
+    // every argument of the layer call is checked before the first copy
+    RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_layer_forward_host"));
+    CHECK_ARG(wr_dev && logits_dev && topk_idx_dev && topk_w_dev && offsets_dev && pairs_dev,
+              "moe_layer_forward_host: null pointer");
+    CHECK_ALIGN(out_dev, "moe_layer_forward_host: out_dev");
+    const size_t esz = xdt == RVQ_BF16 ? 2 : 4;
+    const size_t xbytes = (size_t)n * bank->d * esz, obytes = (size_t)n * bank->d * 4;
+    cudaStream_t st = (cudaStream_t)stream;
+    RVQ_CUDA(cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, st));
+    RVQ_TRY(moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
+                                 topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
+                                 nullptr, xdt, tc_min_tokens, nullptr, stream));
+    RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
+    return RVQ_OK;
 }
 
 rvq_status moe_layer_forward(const rvq_moe_bank *bank, const float *wr_dev, const float *bias_dev,
@@ -901,20 +963,7 @@ rvq_status rvq_ws_clear(void *ws_dev, rvq_stream_t stream) {
 
 rvq_status rvq_ws_status(void *ws_dev, uint32_t *bits_out, rvq_stream_t stream) {
     CHECK_ARG(ws_dev, "rvq_ws_status: null workspace");
-    uint32_t bits = 0;
-    cudaStream_t st = (cudaStream_t)stream;
-    RVQ_CUDA(cudaMemcpyAsync(&bits, ws_dev, 4, cudaMemcpyDeviceToHost, st));
-    RVQ_CUDA(cudaStreamSynchronize(st));
-    if (bits_out) *bits_out = bits;
-    if (bits) {
-        RVQ_CUDA(cudaMemsetAsync(ws_dev, 0, 4, st));
-        RVQ_CUDA(cudaStreamSynchronize(st));
-        set_error("device status bits 0x%x", bits);
-        if (bits & RVQ_DEV_ERR_CORRUPT) return RVQ_ECORRUPT;
-        if (bits & RVQ_DEV_ERR_TIMEOUT) return RVQ_ETIMEOUT;
-        return RVQ_EDEVICE;
-    }
-    return RVQ_OK;
+    return read_status_word(ws_dev, bits_out, (cudaStream_t)stream);
 }
 
 }  // extern "C"

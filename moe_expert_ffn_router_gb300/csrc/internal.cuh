@@ -26,6 +26,10 @@ rvq_status cuda_status(cudaError_t e, const char *what);
         if (_e != cudaSuccess) return ::rvq::cuda_status(_e, #expr); \
     } while (0)
 #define RVQ_LAUNCHED(what) RVQ_CUDA(cudaGetLastError())
+rvq_status check_gemv_args(const char *who, const uint8_t *packed_codes_dev,
+                           const float *packed_cb_dev, int32_t rows, int32_t cols,
+                           const void *x_dev, rvq_dtype xdt, int32_t n, const float *y_dev);
+rvq_status read_status_word(void *status_dev, uint32_t *bits_out, cudaStream_t st);
 
 // ------------------------------------------------------------------ layout
 constexpr int kTileRows = 32;          // rows per tile (one per lane)
@@ -176,6 +180,9 @@ struct LutJob {
     // -1 when not resident; NULL: record e
     const int32_t *slot_of;
     int32_t n_records;
+    // tensor-core table builds: 1 makes the builder first wait for an mbarrier
+    // arrival that nothing makes (self-test of the bounded-wait path)
+    int32_t selftest_stall;
 };
 
 __host__ __device__ inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
@@ -185,6 +192,10 @@ rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl);
 // one partial slot per chunk group).  pd: per sorted pair {expert | -1, entry}.
 rvq_status launch_lut_plan_pairs(const LutJob &job, int4 *pd, cudaStream_t stream, bool pdl);
 rvq_status launch_lut_gemv_il(const LutJob &job, const int4 *pd, cudaStream_t stream, bool pdl);
+// The decode GEMV with tensor-core table builds (lut_tc.cu): same work,
+// layouts and outputs as launch_lut_gemv_il.  pd may be NULL for a single
+// matrix (job.base NULL: codes_ptr / cb_ptr, pair p = entry p).
+rvq_status launch_lut_gemv_tc(const LutJob &job, const int4 *pd, cudaStream_t stream, bool pdl);
 // Descriptors for one or two LUT-GEMV jobs sharing the same grouping.
 rvq_status launch_lut_plan(const LutJob &ja, const LutJob *jb, cudaStream_t stream, bool pdl);
 rvq_status launch_lut_build(const float *cb, const void *x, int xdt, int n, int cols,
@@ -220,8 +231,9 @@ rvq_status launch_pack_codebooks(const float *src, float *dst, int count, cudaSt
 rvq_status launch_write_header(uint8_t *record, const rvq_expert_header &h, cudaStream_t stream);
 
 // ------------------------------------------------- tensor-core (prefill) job
-constexpr int PF_MODE_SWIGLU = 0;  // gate/up: A rows interleave gate and up; out = h bf16
+constexpr int PF_MODE_SWIGLU = 0;  // gate/up: A rows interleave gate and up; out = h fp16
 constexpr int PF_MODE_PLAIN = 1;   // down: out = y fp32
+constexpr int PF_H_F16 = 2;        // PfJob x_dtype of a down launch: fp16 h rows
 struct PfJob {
     const uint8_t *base;       // bank
     uint64_t record_bytes;
@@ -300,7 +312,7 @@ struct FfnPlan {
     int C_d, S_d;     // down
     int nslot_gu, nslot_d;
     size_t off_gpart, off_upart, off_h, off_dpart, off_desc_gu, off_desc_d;
-    size_t off_h16, off_ypair;  // tensor-core path: h bf16, y fp32 [pair][d]
+    size_t off_h16, off_ypair;  // tensor-core path: h fp16, y fp32 [pair][d]
     size_t off_wsplit;          // tensor-core router: Wr as three bf16 terms (0 bytes if unused)
     size_t total;
 };
@@ -313,10 +325,16 @@ rvq_status run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, i
                    const FfnPlan &P, cudaStream_t st, void **marks, bool pdl,
                    int32_t tc_min_tokens = 0, const int32_t *slot_of = nullptr,
                    int32_t n_records = 0, bool pairs_planned = false);
+// Tokens route_kernel takes in one block; only that path can also write the
+// decode GEMV's pair plan.
+constexpr int kRouteSingleBlockTokens = 64;
 // run_ffn takes the interleaved decode GEMV with a per-pair plan for these
 // shapes; pairs_planned = the routing launch already wrote that plan.
+constexpr int kDecodePairPlanMaxTokens = 16;
+static_assert(kDecodePairPlanMaxTokens <= kRouteSingleBlockTokens,
+              "every batch with a pair plan must fit the single-block routing launch");
 inline bool decode_pair_plan(const FfnPlan &P, int n) {
-    return P.C_gu == 1 && P.C_d == 1 && n <= 16;
+    return P.C_gu == 1 && P.C_d == 1 && n <= kDecodePairPlanMaxTokens;
 }
 rvq_status run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                       int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,

@@ -1,13 +1,21 @@
-// Prefill path of the expert FFN: RVQ code tiles dequantised to bf16 feed
-// tcgen05 tensor-core GEMMs (fp32 accumulators in TMEM).
+// Prefill path of the expert FFN: RVQ code tiles dequantised to 16-bit floats
+// feed tcgen05 tensor-core GEMMs (fp32 accumulators in TMEM).
 //
 // For prefill-sized groups (tens to hundreds of tokens per expert) the FFN is
 // a real dense contraction, so the weights are decoded once per tile --
 // W[r][8j+i] = C1[c(r,j,1)][i] + C2[c(r,j,2)][i] + C3[c(r,j,3)][i], the residual
 // decode of the pages ("WASTE Inference Engine", section "Residual Vector
-// Quantization (RVQ)") -- rounded to bf16 and multiplied on the tensor cores.
+// Quantization (RVQ)") -- and multiplied on the tensor cores.
 //
-// GEMM orientation (swap-AB): A = 128 weight rows x 64 K (bf16 in tensor
+// Precision: the codewords are staged as fp16 and summed in fp16.  Gate and
+// up take that sum rounded once to bf16, against the bf16 tokens.  Down takes
+// the fp16 sum as it is, against h = silu(g) u rounded to fp16: with both
+// down operands in bf16 (the weight sum rounded twice, h to 8 bits) one pair
+// in about two thousand exceeded 2e-2 x RMS of the fp64 oracle in the tail,
+// fp16 operands keep the worst pair near 1.5e-2.  |h| above the fp16 range
+// (65504) saturates and is reported as RVQ_DEV_ERR_NONFINITE.
+//
+// GEMM orientation (swap-AB): A = 128 weight rows x 64 K (16-bit, in tensor
 // memory: row = TMEM lane, two K values per 32-bit column), B = up to 192
 // tokens of one expert's group x 64 K (K-major, 128-byte swizzle, shared
 // memory), D = W x^T (128 rows x N tokens, fp32, TMEM).  The decode warps
@@ -19,7 +27,7 @@
 //    rows of up, interleaved in fours (A row r holds weight row
 //    64 m + 4 (r / 8) + r % 4, of gate if r % 8 < 4, of up otherwise), so a
 //    row's gate and up accumulators sit four TMEM lanes apart and the epilogue
-//    pairs them with one shuffle: h = silu(g) * u -> bf16, row = the token's
+//    pairs them with one shuffle: h = silu(g) * u -> fp16, row = the token's
 //    position in the expert-grouped order, so each pass's rows are contiguous.
 //    An item takes two M tiles (2 m, 2 m + 1) that share every K step's
 //    gathered token rows: 8 MMAs per B slot, half the L2 -> SM row traffic
@@ -74,6 +82,7 @@
 // Every wait is bounded (1 s); on expiry the CTA records RVQ_DEV_ERR_TIMEOUT,
 // every role leaves its loop, the MMAs in flight are drained and TMEM is freed.
 #include "internal.cuh"
+#include "tc_util.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -135,152 +144,30 @@ constexpr int kDecodeWarps = 8;                  // A producer warps (8-15)
 // producer's expect_tx arrival)
 constexpr uint32_t kFullCount = kDecodeWarps / 2 + 1;
 constexpr uint32_t kFullCountPair = kDecodeWarps + 1;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s: a bounded wait, never a hang
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (SBO), leading offset unused for swizzled K-major.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);        // start address
-    d |= (uint64_t)1u << 16;                         // LBO (16 B, unused)
-    d |= (uint64_t)(1024u >> 4) << 32;               // SBO = 1024 B
-    d |= (uint64_t)1u << 46;                         // descriptor version (sm_100 family)
-    d |= (uint64_t)2u << 61;                         // SWIZZLE_128B
-    return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-// D (TMEM) (+)= A (TMEM, 128 lanes x 16 K) x B (shared memory descriptor).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t mbar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     mbar)
-                 : "memory");
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-    asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(mbar)
-                 : "memory");
-}
-
-// try_wait with a suspend hint: a waiting warp sleeps (up to 20 us) instead
-// of spinning, leaving issue slots to the decoding warps; it wakes when the
-// phase completes.
-__device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        "selp.b32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(parity), "r"(20000u)
-        : "memory");
-    return done != 0;
-}
-
-// Bounded wait on an mbarrier phase.  Returns false once another role has
-// aborted, or after kWaitLimitNs (then this thread raises the abort flag and
-// records the timeout).
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag,
-                                          uint32_t *status) {
-    if (mbar_try(mbar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        if (mbar_try(mbar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            set_dev_error(status, RVQ_DEV_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// The MMA thread's wait: polls without a suspend hint (its waits are short
-// and on its critical path), same bound and abort protocol as mbar_wait.
-__device__ __forceinline__ bool mbar_try_now(uint32_t mbar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.b32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t mbar, uint32_t parity,
-                                               volatile int *abort_flag, uint32_t *status) {
-    if (mbar_try_now(mbar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        if (mbar_try_now(mbar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            set_dev_error(status, RVQ_DEV_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ uint32_t bf16_bits(float f) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&b);
-}
-
-// Three fp16x2 codeword words summed in fp16, rounded once to bf16x2.
-__device__ __forceinline__ uint32_t sum3_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+// Three fp16x2 codeword words summed in fp16 (the down GEMM's fp16 weights).
+__device__ __forceinline__ uint32_t sum3_f16x2(uint32_t a, uint32_t b, uint32_t c) {
     const __half2 s = __hadd2(__hadd2(*reinterpret_cast<const __half2 *>(&a),
                                       *reinterpret_cast<const __half2 *>(&b)),
                               *reinterpret_cast<const __half2 *>(&c));
-    const float2 f = __half22float2(s);
+    return *reinterpret_cast<const uint32_t *>(&s);
+}
+
+// The same sum rounded once to bf16x2 (the gate/up GEMMs' bf16 weights).
+__device__ __forceinline__ uint32_t sum3_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+    const uint32_t s = sum3_f16x2(a, b, c);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&s));
     return pack_bf16x2(f.x, f.y);
+}
+
+// h = silu(g) u as fp16 bits for the down GEMM; |h| beyond the fp16 range
+// saturates to +-65504 and is reported (*over = true); NaN stays NaN.
+__device__ __forceinline__ uint16_t h_to_f16(float hv, bool &over) {
+    if (fabsf(hv) > 65504.0f) {
+        over = true;
+        hv = copysignf(65504.0f, hv);
+    }
+    return __half_as_ushort(__float2half_rn(hv));
 }
 
 // Rotate a 32-byte vector left by l bytes (l in 0..31).  The packed code
@@ -298,31 +185,6 @@ __device__ __forceinline__ void derotate(uint32_t (&w)[8], int l) {
     for (int i = 0; i < 8; ++i) a[i] = (wl & 4) ? b[(i + 4) & 7] : b[i];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = __funnelshift_l(a[(i + 7) & 7], a[i], bl);
-}
-
-// Eight 32-bit columns of this warp's 32 TMEM lanes (one register per column).
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-            taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-        : "memory");
-}
-
-// 128-bit shared load through a 32-bit shared address (no generic address
-// arithmetic).  Not volatile: its address depends on code bytes loaded after
-// every codebook swap, which keeps it behind the swap's barrier.
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
-                 : "memory");
 }
 
 // Tiled TMA load of one box (64 bf16 columns from col x kTmaRows rows from
@@ -548,7 +410,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 if (!mbar_wait(bar(BAR_ACC_EMPTY + ab), (use & 1u) ^ 1u, abort_flag, job.status))
                     break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t idesc = idesc_bf16(PF_MROWS, I.npad);
+                const uint32_t idesc =
+                    pair ? idesc_bf16(PF_MROWS, I.npad) : idesc_f16(PF_MROWS, I.npad);
                 bool ok = true;
                 for (int ks = 0; ks < KS; ++ks, ++kg) {
                     if (!mbar_wait_spin(bar(BAR_FULL + (kg & (PF_NBAR - 1))),
@@ -767,14 +630,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     // row of token t: its position in the grouped order
                     uint16_t *hrow = reinterpret_cast<uint16_t *>(job.out) +
                                      (size_t)(I.o + I.j0 + 32 * c) * job.rows + R;
+                    bool over = false;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const int p = __shfl_sync(0xffffffffu, pl[c], t);
                         const float u = __shfl_xor_sync(0xffffffffu, a[t], 4);
                         const float g = a[t];
                         const float hv = __fdividef(g * u, 1.0f + __expf(-g));
-                        if (q < 4 && p >= 0) hrow[(size_t)t * job.rows] = (uint16_t)bf16_bits(hv);
+                        if (q < 4 && p >= 0) hrow[(size_t)t * job.rows] = h_to_f16(hv, over);
                     }
+                    if (__any_sync(0xffffffffu, over) && lane == 0)
+                        set_dev_error(job.status, RVQ_DEV_ERR_NONFINITE);
                 } else {
                     float *yrow = reinterpret_cast<float *>(job.out) + R;
 #pragma unroll
@@ -908,10 +774,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                             const uint4 w0 = lds128(cbl + k0 * kCbLine);
                             const uint4 w1 = lds128(cbl + (256 + k1) * kCbLine);
                             const uint4 w2 = lds128(cbl + (512 + k2) * kCbLine);
-                            o[4 * c + 0] = sum3_bf16x2(w0.x, w1.x, w2.x);
-                            o[4 * c + 1] = sum3_bf16x2(w0.y, w1.y, w2.y);
-                            o[4 * c + 2] = sum3_bf16x2(w0.z, w1.z, w2.z);
-                            o[4 * c + 3] = sum3_bf16x2(w0.w, w1.w, w2.w);
+                            // gate/up: bf16 weights; down: fp16 (see the file header)
+                            if (pair) {
+                                o[4 * c + 0] = sum3_bf16x2(w0.x, w1.x, w2.x);
+                                o[4 * c + 1] = sum3_bf16x2(w0.y, w1.y, w2.y);
+                                o[4 * c + 2] = sum3_bf16x2(w0.z, w1.z, w2.z);
+                                o[4 * c + 3] = sum3_bf16x2(w0.w, w1.w, w2.w);
+                            } else {
+                                o[4 * c + 0] = sum3_f16x2(w0.x, w1.x, w2.x);
+                                o[4 * c + 1] = sum3_f16x2(w0.y, w1.y, w2.y);
+                                o[4 * c + 2] = sum3_f16x2(w0.z, w1.z, w2.z);
+                                o[4 * c + 3] = sum3_f16x2(w0.w, w1.w, w2.w);
+                            }
                         }
                         tmem_st8(ta + tst + 8 * hq, o);
                     }
@@ -982,9 +856,9 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
     CUtensorMap tmap;
     memset(&tmap, 0, sizeof(tmap));
     if (job.mode == PF_MODE_PLAIN) {
-        if (job.x_dtype != RVQ_BF16 || job.x_div != 1 || job.x_stride < job.cols ||
+        if (job.x_dtype != PF_H_F16 || job.x_div != 1 || job.x_stride < job.cols ||
             ((uintptr_t)job.x & 15u) != 0 || job.n_pairs < 1) {
-            set_error("prefill: down input must be bf16 rows of pitch >= %d, 16-byte aligned",
+            set_error("prefill: down input must be fp16 h rows of pitch >= %d, 16-byte aligned",
                       job.cols);
             return RVQ_EINVAL;
         }
@@ -997,7 +871,7 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
         const cuuint64_t strides[1] = {(cuuint64_t)job.x_stride * 2u};
         const cuuint32_t box[2] = {(cuuint32_t)PF_KC, (cuuint32_t)kTmaRows};
         const cuuint32_t estr[2] = {1u, 1u};
-        const CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+        const CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                                   const_cast<void *>(job.x), dims, strides, box, estr,
                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -583,11 +583,12 @@ rvq_status launch_route_nt(const float *logits, int n, int E, int k, int32_t *id
 rvq_status launch_route(const float *logits, int n, int E, int k, int32_t *idx, float *w,
                         int32_t *offsets, int32_t *pairs, uint32_t *status, cudaStream_t stream,
                         bool pdl, const LutJob *plan, int4 *pd) {
-    if (plan && (n > 64 || !pd || plan->tc_min_tokens > 0)) {
-        set_error("route: the fused pair plan needs n <= 64, pd and no tensor-core dispatch");
+    if (plan && (n > kRouteSingleBlockTokens || !pd || plan->tc_min_tokens > 0)) {
+        set_error("route: the fused pair plan needs n <= %d, pd and no tensor-core dispatch",
+                  kRouteSingleBlockTokens);
         return RVQ_EINVAL;
     }
-    if (n <= 64)
+    if (n <= kRouteSingleBlockTokens)
         return launch_route_nt<256, true>(logits, n, E, k, idx, w, offsets, pairs, status, stream,
                                           pdl, plan, pd);
     // larger batches: the selection spreads over the grid, the grouping stays in one block

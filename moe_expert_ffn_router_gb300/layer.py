@@ -8,7 +8,8 @@ import torch
 from . import (RVQ_WS_STATUS_BYTES, moe_bank_init, moe_bank_record_bytes, moe_bank_validate,
                moe_bank_write_expert, moe_cache_bank, moe_cache_create, moe_cache_destroy,
                moe_cache_stats, moe_combine, moe_expert_ffn, moe_layer_forward,
-               moe_layer_forward_prenorm, moe_layer_forward_streamed, moe_rms_norm, moe_route,
+               moe_layer_forward_host, moe_layer_forward_prenorm, moe_layer_forward_streamed,
+               moe_rms_norm, moe_route,
                moe_router_logits,
                moe_workspace_bytes, rvq_ws_clear, rvq_ws_status)
 
@@ -95,6 +96,21 @@ class MoeLayer:
         moe_layer_forward(self.bank, self.wr, self.bias, x, n, self.k, b["logits"], b["idx"],
                           b["w"], b["offsets"], b["pairs"], b["out"], b["ws"], events=events,
                           tc_min_tokens=tc_min_tokens, residual=residual)
+        return b
+
+    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, bufs: dict | None = None,
+                     tc_min_tokens: int = 0) -> dict:
+        """The layer with its input read from and its output written to host
+        tensors (pinned for asynchronous copies), through the library's
+        host-buffer call; asynchronous on the current stream."""
+        n = x_host.shape[0]
+        b = bufs or self.buffers(n)
+        xd = b.get("x_dev")
+        if xd is None or xd.dtype != x_host.dtype or xd.shape != (n, self.d):
+            xd = b["x_dev"] = torch.empty((n, self.d), dtype=x_host.dtype, device=self.device)
+        moe_layer_forward_host(self.bank, self.wr, self.bias, x_host, n, self.k, xd, b["logits"],
+                               b["idx"], b["w"], b["offsets"], b["pairs"], b["out"], out_host,
+                               b["ws"], tc_min_tokens=tc_min_tokens)
         return b
 
     def forward_steps(self, x: torch.Tensor) -> dict:

@@ -2,6 +2,9 @@
 -> weighted combine + residual) against the oracle, plus device-side fault
 reporting.  Routing is compared bit-exact with the oracle routing the GPU's
 own fp32 logits; floats within 1e-4 x RMS."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -56,11 +59,18 @@ def check_layer(sl, L, x_bits, tokens=None, steps=False):
     np.testing.assert_allclose(w, rw, rtol=2e-6, atol=1e-9)
     roff, rpairs = oracle.group(ridx, L.E)
     assert np.array_equal(off, roff) and np.array_equal(pairs, rpairs)
-    # expert outputs and combine on a subset of tokens (all by default)
-    tokens = range(n) if tokens is None else tokens
+    # expert outputs and combine on a subset of tokens (all by default); the
+    # oracle layers run on a thread pool (the C oracle releases the GIL), with
+    # the sampled tokens' experts generated first
+    tokens = list(range(n) if tokens is None else tokens)
     for t in tokens:
-        r = oracle.moe_layer(sl.expert, sl.wr, x64[t:t + 1], s.k, s.d, s.f,
-                             route_logits=logits[t:t + 1])
+        for e in idx[t]:
+            sl.expert(int(e))
+    with ThreadPoolExecutor(max_workers=max(1, min(len(tokens), os.cpu_count() or 1))) as ex:
+        refs = list(ex.map(lambda t: oracle.moe_layer(sl.expert, sl.wr, x64[t:t + 1], s.k, s.d,
+                                                      s.f, route_logits=logits[t:t + 1]),
+                           tokens))
+    for t, r in zip(tokens, refs):
         assert np.array_equal(r["idx"][0], idx[t])
         delta_ref = r["out"][0] - x64[t]
         assert_rms_close(out[t] - x64[t], delta_ref, 1e-4, f"token {t} out-x")
@@ -146,11 +156,41 @@ def test_bad_offsets_are_reported():
     assert bits & rvq.DEV_ERR_INDEX and rc == 5
 
 
-@pytest.mark.parametrize("n,sample", [(1, [0]), (8, [0, 5]), (64, [3, 60])])
+@pytest.mark.parametrize("n,sample", [(1, [0]), (8, [0, 5]),
+                                      (64, [0, 9, 18, 27, 36, 45, 54, 63])])
 def test_k3_shaped_layer_full_size(n, sample):
     """d=7168, f=2048, 256 experts, top-16, 4.2 GB bank: all outputs of the
-    sampled tokens against the oracle; routing of every token bit-exact."""
+    sampled tokens against the oracle; routing of every token bit-exact.  At
+    64 tokens the lookup tables serve two tokens of an expert at a time, and
+    an expert with an odd token count gives its last token a one-token item:
+    the sample covers pairs of both kinds."""
     drop_layers()
     sl, L = layer(2)
-    check_layer(sl, L, sl.tokens_bf16(n), tokens=sample)
+    b = check_layer(sl, L, sl.tokens_bf16(n), tokens=sample)
+    if n == 64:
+        off, pairs = b["offsets"].cpu().numpy(), b["pairs"].cpu().numpy()
+        kinds = set()
+        for e in range(L.E):
+            seg = pairs[off[e]:off[e + 1]]
+            for j, p in enumerate(seg):
+                if p // L.k in sample:
+                    kinds.add("odd remainder" if len(seg) % 2 and j == len(seg) - 1 else "pair")
+        assert kinds == {"odd remainder", "pair"}, kinds
     sl.forget()
+
+
+def test_host_buffer_layer_call_equals_device_call():
+    """moe_layer_forward_host (input copied from pinned host memory, output
+    copied back) gives bit for bit the device-buffer layer's outputs."""
+    sl, L = layer(1)
+    n = 3
+    bits = sl.tokens_bf16(n)
+    x_host = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    out_host = torch.full((n, L.d), float("nan"), dtype=torch.float32).pin_memory()
+    hb = L.forward_host(x_host, out_host)
+    torch.cuda.synchronize()
+    assert L.status(n) == (0, 0)
+    ref = L.forward(bf16_dev(bits))
+    torch.cuda.synchronize()
+    assert torch.equal(out_host, ref["out"].cpu())
+    assert torch.equal(hb["x_dev"].cpu().view(torch.int16), x_host.view(torch.int16))

@@ -3,6 +3,8 @@ tiles decoded to bf16 and multiplied on tcgen05.  Held to 2e-2 x RMS per pair
 output against the double-precision oracle; experts left on the lookup-table
 path in a mixed dispatch stay at 1e-4 x RMS.  Routing is the GPU's own (bit-
 exactness of routing is covered by test_gpu_router / test_gpu_layer)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -241,3 +243,48 @@ def test_stalled_pipeline_times_out_and_recovers():
     assert rvq.rvq_ws_status(ws) == (0, 0)                      # the read cleared it
     # the context is healthy: a full tensor-core layer is still correct
     test_tensor_core_path_all_experts_d2048()
+
+
+def test_prefill_multipass_groups_every_pair_d2048():
+    """Groups larger than one pass of the tensor-core kernel (passes of at
+    most 192 tokens): 1024 tokens of the d = 2048 layer with a Zipf router
+    bias strong enough (beta 0.5) that the three largest groups hold 760, 593
+    and 487 tokens, i.e. four, four and three passes with ragged last ones.
+    Every pair of those three groups (1,840 pairs, first, middle and last
+    passes alike) is compared with the oracle expert FFN at 2e-2 x RMS; the
+    oracle calls run on a thread pool (the C oracle releases the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    sl, L, bias = layer(1, 0.5)
+    n = 1024
+    bits = sl.tokens_bf16(n)
+    x = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    b = route(L, x, n)
+    y = run_ffn(L, x, n, b, tc_min_tokens=1)
+    assert np.isfinite(y).all()
+    offs = b["offsets"].cpu().numpy()
+    pairs = b["pairs"].cpu().numpy()
+    idx = b["idx"].cpu().numpy()
+    counts = np.diff(offs)
+    top3 = np.argsort(counts, kind="stable")[-3:]
+    # (the oracle's routing of the same tokens gives 760, 593 and 487)
+    assert counts[top3].min() > 2 * 192 and counts[top3].max() > 3 * 192, counts[top3]
+    x64 = bf16_bits_to_f64(bits)
+    s = sl.shape
+    experts = {int(e): sl.expert(int(e)) for e in top3}
+    work = [(int(p), int(e)) for e in top3 for p in pairs[offs[e]:offs[e + 1]]]
+
+    def err(item):
+        p, e = item
+        t, slot = divmod(p, s.k)
+        assert int(idx[t, slot]) == e
+        ref = oracle.expert_ffn(*experts[e], s.d, s.f, x64[t])
+        d = float(np.abs(y[p] - ref).max())
+        r = float(np.sqrt(np.mean(ref * ref)))
+        return d / r, p, e
+
+    with ThreadPoolExecutor(max_workers=max(1, min(16, (os.cpu_count() or 1)))) as ex:
+        res = list(ex.map(err, work))
+    assert len(res) == int(counts[top3].sum())
+    worst = max(res)
+    assert worst[0] <= TC_TOL, f"pair {worst[1]} (expert {worst[2]}): max err {worst[0]:.3e} x RMS"
+    sl.forget()
