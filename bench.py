@@ -387,6 +387,9 @@ def run_gpu(args, rank, world, local_rank):
                     "peak_source": peak_kind, "traffic": None,
                     "algorithmic_flops_per_launch": int(gu_flops),
                     "avg_launch_us": round(avg[DOMINANT_TC] * 1e3, 2),
+                    "timing": "a second pass over the timed steps with an event between "
+                              "kernels (serialised, programmatic dependent launch off); "
+                              "launch latency included",
                     "ffn_tflops": round(ffn_tflops, 1),
                     "ffn_frac": round(ffn_tflops / peak, 4)}
     else:
@@ -402,7 +405,10 @@ def run_gpu(args, rank, world, local_rank):
                     "traffic": load_traffic(DOMINANT) if (s.E == 256 and batch == 1
                                                           and n_layers == 1) else None,
                     "algorithmic_bytes_per_launch": int(gu_bytes),
-                    "avg_launch_us": round(avg[DOMINANT] * 1e3, 2)}
+                    "avg_launch_us": round(avg[DOMINANT] * 1e3, 2),
+                    "timing": "a second pass over the timed steps with an event between "
+                              "kernels (serialised, programmatic dependent launch off); "
+                              "launch latency included"}
 
     # ---- end to end through host buffers ----
     pinned_in = torch.from_numpy(pool_bits.view(np.int16).copy()).reshape(-1, batch, s.d)

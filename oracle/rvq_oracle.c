@@ -5,7 +5,10 @@
  * and the benchmark's CPU-baseline / reference leg may load this library.  It
  * shares no code, header, table or helper with the CUDA path.
  *
- * Plain C11, libc + libm, double precision throughout, no blocking, no
+ * Plain C11, libc + libm, double precision throughout (one exception: the
+ * offline encoder, oracle_rvq_encode, takes its distances in fp32 fused
+ * multiply-adds and its means as int64 fixed-point sums, the reproducible
+ * steps its codes are compared bit for bit against), no blocking, no
  * fusion: each function is the plain definition of one step, written so it
  * can be checked against the source pages by eye.  Sources (web pages on the
  * WASTE inference engine):
