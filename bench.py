@@ -535,7 +535,7 @@ def oracle_baseline(config, shape, batch, layers, uniq_mean, tokens_bf16):
     # one core: two pairs of the first token
     t_one = ob.run([0], pairs=2, threads=1)
     step_one = t_one / 2 * pairs_batch * layers
-    weights = uniq_mean * 3 * s.d * s.f
+    weights = uniq_mean * layers * 3 * s.d * s.f   # every layer's distinct experts
     return {"value": round(weights / step_all / 1e9, 6), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "single_thread": {"value": round(weights / step_one / 1e9, 6), "cores": 1,
@@ -957,7 +957,6 @@ def main():
                     choices=sorted(WORKLOADS) + sorted(STREAM_WORKLOADS) +
                     sorted(ENCODE_WORKLOADS) + sorted(GEMV_WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--oracle-tokens", type=int, default=4)
     ap.add_argument("--tc-min-tokens", type=int, default=None,
                     help="experts with at least this many tokens take the tensor-core path "
                          "(default: 1 for the prefill workload, 0 = lookup tables only, otherwise)")
@@ -1011,12 +1010,9 @@ def main():
         s = r["shape"]
         cpu = None
         if not args.no_cpu_baseline:
-            tok_s = oracle_sample(r["config"], args.oracle_tokens, shape=r["shape"])
-            v = r["uniq_mean"] * 3 * s.d * s.f / (tok_s * r["batch"] * r["layers"]) / 1e9
-            cpu = {"value": round(v, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{args.oracle_tokens} tokens through the whole oracle layer "
-                             f"({tok_s:.2f} s per token), scaled to the {r['batch']}-token "
-                             f"batch, {r['layers']} layer(s) and their distinct experts"}
+            src = W.ExpertSource(r["config"], 0, s)
+            cpu = oracle_baseline(r["config"], s, r["batch"], r["layers"],
+                                  r["uniq_mean"] / r["layers"], src.tokens_bf16(r["batch"]))
         line = {
             "metric": METRIC, "value": round(r["value"], 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4),

@@ -146,8 +146,10 @@ void oracle_router_logits(const float *wr, const float *bias, const double *x,
 }
 
 /* Strict order used for selection: larger logit first, equal logits by the
- * lower expert index (reading: the pages give no tie rule). */
-static const float *g_sort_row;
+ * lower expert index (reading: the pages give no tie rule).  The row being
+ * sorted is per thread, so concurrent calls (a thread pool in the tests and
+ * the benchmark's baseline) do not share it. */
+static _Thread_local const float *g_sort_row;
 static int cmp_expert(const void *a, const void *b)
 {
     int32_t ia = *(const int32_t *)a, ib = *(const int32_t *)b;
