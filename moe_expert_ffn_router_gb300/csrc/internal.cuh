@@ -180,9 +180,6 @@ struct LutJob {
     // -1 when not resident; NULL: record e
     const int32_t *slot_of;
     int32_t n_records;
-    // tensor-core table builds: 1 makes the builder first wait for an mbarrier
-    // arrival that nothing makes (self-test of the bounded-wait path)
-    int32_t selftest_stall;
 };
 
 __host__ __device__ inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
@@ -192,10 +189,6 @@ rvq_status launch_lut_gemv(const LutJob &job, cudaStream_t stream, bool pdl);
 // one partial slot per chunk group).  pd: per sorted pair {expert | -1, entry}.
 rvq_status launch_lut_plan_pairs(const LutJob &job, int4 *pd, cudaStream_t stream, bool pdl);
 rvq_status launch_lut_gemv_il(const LutJob &job, const int4 *pd, cudaStream_t stream, bool pdl);
-// The decode GEMV with tensor-core table builds (lut_tc.cu): same work,
-// layouts and outputs as launch_lut_gemv_il.  pd may be NULL for a single
-// matrix (job.base NULL: codes_ptr / cb_ptr, pair p = entry p).
-rvq_status launch_lut_gemv_tc(const LutJob &job, const int4 *pd, cudaStream_t stream, bool pdl);
 // Descriptors for one or two LUT-GEMV jobs sharing the same grouping.
 rvq_status launch_lut_plan(const LutJob &ja, const LutJob *jb, cudaStream_t stream, bool pdl);
 rvq_status launch_lut_build(const float *cb, const void *x, int xdt, int n, int cols,

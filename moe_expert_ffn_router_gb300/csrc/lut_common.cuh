@@ -1,5 +1,5 @@
-// Lookup-table helpers shared by the decode GEMV kernels (lut_gemv.cu,
-// lut_tc.cu): code bytes -> shared-memory table addresses and fp32 sums.
+// Lookup-table helpers of the decode GEMV kernels (lut_gemv.cu): code bytes
+// -> shared-memory table addresses and fp32 sums.
 #pragma once
 
 #include <stdint.h>
@@ -62,38 +62,6 @@ __device__ __forceinline__ float tile_lookups1_ilp(const uint4 (&c)[6], const ui
         }
     const float2 a0 = upk2(fadd2(acc[0], acc[1])), a1 = upk2(fadd2(acc[2], acc[3]));
     return (a0.x + a0.y) + (a1.x + a1.y);
-}
-
-// The same lookups with 8 in flight per group (fewer registers; enough when
-// 16 or more warps of the SM look up at once).
-__device__ __forceinline__ float tile_lookups1_g8(const uint4 (&c)[6], const uint32_t (&aux2)[16],
-                                                  const uint8_t *lut) {
-    uint64_t acc[2] = {0, 0};
-#pragma unroll
-    for (int s = 0; s < 3; ++s)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int qh = 0; qh < 2; ++qh) {
-                float v[8];
-#pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const int q = 2 * qh + qq;
-                    const uint32_t w = word_of(c[s * 2 + h], q);
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const int t = h * 16 + q * 4 + b;
-                        const uint32_t idx =
-                            prmt(w, aux2[t >> 1], 0x7600u | (b << 4) | (4 + (t & 1)));
-                        v[qq * 4 + b] =
-                            *reinterpret_cast<const float *>(lut + s * kLutStageBytes + idx);
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i & 1] = fadd2(acc[i & 1], pk2(v[2 * i], v[2 * i + 1]));
-            }
-    const float2 a = upk2(fadd2(acc[0], acc[1]));
-    return a.x + a.y;
 }
 
 }  // namespace rvq

@@ -1,5 +1,5 @@
-// tcgen05 / mbarrier helpers shared by the tensor-core kernels (prefill GEMM,
-// decode table builds).  Inline PTX; sm_100 family.
+// tcgen05 / mbarrier helpers of the tensor-core kernels (the prefill GEMM).
+// Inline PTX; sm_100 family.
 #pragma once
 
 #include <cuda_bf16.h>

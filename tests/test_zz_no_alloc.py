@@ -50,7 +50,8 @@ def test_noalloc_matches_workspace_gemv_on_two_calls():
         y_ref = _with_workspace(packed, cbp, rows, cols, x, n)
         y = torch.full((n, rows), float("nan"), dtype=torch.float32, device=DEV)
         rvq.rvq_gemv_noalloc(packed, cbp, rows, cols, x, n, y)
-        torch.cuda.synchronize()
+        # the call's device status, read from the fixed array (waits for the stream)
+        assert rvq.rvq_gemv_noalloc_status() == (0, 0)
         assert_rms_close(y.cpu().numpy(), y_ref.cpu().numpy(), 1e-4, f"noalloc {rows}x{cols}")
 
 
@@ -62,3 +63,25 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
         rvq.rvq_gemv_noalloc(dummy, dummy, rows, cols, dummy, n, dummy)
     assert ei.value.status == "RVQ_ENOMEM"
     assert "scratch" in str(ei.value)
+
+
+def test_noalloc_rejects_bad_arguments_before_launching():
+    """Argument checks run before the status block is cleared or anything is
+    queued: a rejected call leaves the last call's output untouched."""
+    rows, cols, n = 256, 512, 1
+    packed, cbp = _matrix(rows, cols, 3)
+    x = torch.from_numpy(synth.normal_f32(77, n * cols).reshape(n, cols)).to(DEV)
+    y = torch.empty((n, rows), dtype=torch.float32, device=DEV)
+    rvq.rvq_gemv_noalloc(packed, cbp, rows, cols, x, n, y)
+    torch.cuda.synchronize()
+    before = y.clone()
+    xbad = torch.empty(n * cols + 4, dtype=torch.float32, device=DEV)[1:1 + n * cols].view(n, cols)
+    with pytest.raises(rvq.RvqError) as ei:
+        rvq.rvq_gemv_noalloc(packed, cbp, rows, cols, xbad, n, y)
+    assert ei.value.status == "RVQ_EALIGN"
+    with pytest.raises(rvq.RvqError) as ei:
+        rvq.rvq_gemv_noalloc(packed, cbp, rows + 1, cols, x, n, y)
+    assert ei.value.status == "RVQ_EINVAL"
+    torch.cuda.synchronize()
+    assert torch.equal(y, before)
+    assert rvq.rvq_gemv_noalloc_status() == (0, 0)
