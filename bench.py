@@ -99,7 +99,7 @@ def router_launches(n, E, d):
 
 def load_traffic(name):
     """DRAM bytes per launch of `name` from the committed ncu summary, or None
-    when the kernel source changed since that capture."""
+    when a source the kernel is built from changed since that capture."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "lut_gemv_traffic.json")
     if not os.path.exists(p):
@@ -107,8 +107,13 @@ def load_traffic(name):
     rec = json.load(open(p)).get(name)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
+    h = hashlib.sha1()
+    for rel in rec["sources"]:
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    if h.hexdigest() != rec["sources_sha1"]:
         return None
     return int(rec["dram_bytes_per_launch"])
 
