@@ -112,6 +112,9 @@ FfnPlan plan_ffn(int d, int f, int n_pairs, int E, int n_tokens) {
     off = align256(off + (size_t)n_pairs * f * 2);
     P.off_ypair = off;
     off = align256(off + (size_t)n_pairs * d * 4);
+    P.off_x16 = off;
+    P.n_tokens = n_tokens;
+    off = align256(off + (size_t)n_tokens * d * 2);
     P.off_wsplit = off;
     if (router_tc_supported(n_tokens, E, d)) off = align256(off + router_tc_split_bytes(E, d));
     P.total = off;
@@ -584,8 +587,8 @@ rvq_status rvq::run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype x
 }
 
 // Tensor-core (prefill) path for experts with at least tc_min_tokens tokens:
-// gate/up GEMMs with the SwiGLU epilogue into h (bf16), then the down GEMM
-// writing y fp32 [pair][d] for those experts' pairs.
+// the tokens to fp16, gate/up GEMMs with the SwiGLU epilogue into h (fp16),
+// then the down GEMM writing y fp32 [pair][d] for those experts' pairs.
 rvq_status rvq::run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype xdt, int32_t n,
                       int32_t k, const int32_t *offsets_dev, const int32_t *pairs_dev,
                       void *ws_dev, const FfnPlan &P, float *y_pair, int32_t tc_min_tokens,
@@ -593,6 +596,13 @@ rvq_status rvq::run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtyp
                       int32_t n_records) {
     const RecordLayout L = record_layout(bank->d, bank->f);
     uint8_t *ws = (uint8_t *)ws_dev;
+    if (P.n_tokens < n) {
+        set_error("tensor-core FFN: workspace plan for %d tokens, called with %d", P.n_tokens, n);
+        return RVQ_EINVAL;
+    }
+    // both GEMMs run on fp16 operands: the tokens are converted once
+    uint16_t *x16 = (uint16_t *)(ws + P.off_x16);
+    RVQ_TRY(launch_tokens_f16(x_dev, (int)xdt, n, bank->d, x16, (uint32_t *)ws_dev, st, pdl));
     PfJob g = {};
     g.base = bank->base;
     g.slot_of = slot_of;
@@ -611,8 +621,8 @@ rvq_status rvq::run_ffn_tc(const rvq_moe_bank *bank, const void *x_dev, rvq_dtyp
     g.min_tokens = tc_min_tokens;
     g.offsets = offsets_dev;
     g.pairs = pairs_dev;
-    g.x = x_dev;
-    g.x_dtype = (int)xdt;
+    g.x = x16;
+    g.x_dtype = PF_H_F16;
     g.x_stride = bank->d;
     g.x_div = k;
     g.out = ws + P.off_h16;
@@ -666,7 +676,7 @@ rvq_status moe_expert_ffn_ex(const rvq_moe_bank *bank, const void *x_dev, rvq_dt
     RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_expert_ffn"));
     CHECK_ARG(offsets_dev && pairs_dev && y_pair_dev, "moe_expert_ffn: null pointer");
     CHECK_ALIGN(y_pair_dev, "moe_expert_ffn: y_pair");
-    const FfnPlan P = plan_ffn(bank->d, bank->f, n * k, bank->n_experts);
+    const FfnPlan P = plan_ffn(bank->d, bank->f, n * k, bank->n_experts, n);
     cudaStream_t st = (cudaStream_t)stream;
     if (tc_min_tokens != 1) {  // some experts take the lookup-table path
         RVQ_TRY(run_ffn(bank, x_dev, xdt, n, k, offsets_dev, pairs_dev, ws_dev, P, st, nullptr,
@@ -910,7 +920,7 @@ rvq_status rvq_selftest_prefill_timeout(const rvq_moe_bank *bank, void *ws_dev, 
               "rvq_selftest_prefill_timeout: workspace %zu < %zu", ws_bytes,
               moe_workspace_bytes(bank, 1, 1));
     const int E = bank->n_experts;
-    const FfnPlan P = plan_ffn(bank->d, bank->f, 1, E);
+    const FfnPlan P = plan_ffn(bank->d, bank->f, 1, E, 1);
     uint8_t *ws = (uint8_t *)ws_dev;
     cudaStream_t st = (cudaStream_t)stream;
     // one token routed to expert 0: offsets and pairs in the gate partial
@@ -941,7 +951,7 @@ rvq_status rvq_selftest_prefill_timeout(const rvq_moe_bank *bank, void *ws_dev, 
     g.offsets = offsets;
     g.pairs = offsets + E + 1;
     g.x = x;
-    g.x_dtype = RVQ_BF16;
+    g.x_dtype = PF_H_F16;
     g.x_stride = bank->d;
     g.x_div = 1;
     g.out = ws + P.off_h16;

@@ -226,7 +226,7 @@ rvq_status launch_write_header(uint8_t *record, const rvq_expert_header &h, cuda
 // ------------------------------------------------- tensor-core (prefill) job
 constexpr int PF_MODE_SWIGLU = 0;  // gate/up: A rows interleave gate and up; out = h fp16
 constexpr int PF_MODE_PLAIN = 1;   // down: out = y fp32
-constexpr int PF_H_F16 = 2;        // PfJob x_dtype of a down launch: fp16 h rows
+constexpr int PF_H_F16 = 2;        // PfJob x_dtype: fp16 B rows (tokens for gate/up, h for down)
 struct PfJob {
     const uint8_t *base;       // bank
     uint64_t record_bytes;
@@ -238,7 +238,7 @@ struct PfJob {
     int32_t E, n_pairs;
     int32_t min_tokens;        // experts with fewer tokens are not this launch's work
     const int32_t *offsets, *pairs;
-    const void *x;             // B rows: x[entry / x_div] (gate/up) or h[grouped position] (down, bf16)
+    const void *x;             // fp16 B rows: x16[entry / x_div] (gate/up) or h[grouped position] (down)
     int32_t x_dtype;
     int64_t x_stride;
     int32_t x_div;
@@ -282,6 +282,10 @@ __device__ __forceinline__ int4 pair_desc(const LutJob &job, int e, int ne, int 
     return d;
 }
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl);
+// tokens x [n][d] (RVQ_F32 or RVQ_BF16) -> fp16 x16 [n][d] for the prefill
+// GEMMs; |x| beyond the fp16 range saturates and sets RVQ_DEV_ERR_NONFINITE
+rvq_status launch_tokens_f16(const void *x, int xdt, int n, int d, uint16_t *x16,
+                             uint32_t *status, cudaStream_t stream, bool pdl);
 // offline residual k-means encoder (encode.cu)
 size_t encode_workspace_bytes(int rows, int cols);
 rvq_status launch_rvq_encode(const float *w, int rows, int cols, int iters, uint8_t *codes,
@@ -306,6 +310,8 @@ struct FfnPlan {
     int nslot_gu, nslot_d;
     size_t off_gpart, off_upart, off_h, off_dpart, off_desc_gu, off_desc_d;
     size_t off_h16, off_ypair;  // tensor-core path: h fp16, y fp32 [pair][d]
+    size_t off_x16;             // tensor-core path: the tokens as fp16 [n_tokens][d]
+    int n_tokens;               // tokens the x16 region holds
     size_t off_wsplit;          // tensor-core router: Wr as three bf16 terms (0 bytes if unused)
     size_t total;
 };

@@ -7,13 +7,15 @@
 // decode of the pages ("WASTE Inference Engine", section "Residual Vector
 // Quantization (RVQ)") -- and multiplied on the tensor cores.
 //
-// Precision: the codewords are staged as fp16 and summed in fp16.  Gate and
-// up take that sum rounded once to bf16, against the bf16 tokens.  Down takes
-// the fp16 sum as it is, against h = silu(g) u rounded to fp16: with both
-// down operands in bf16 (the weight sum rounded twice, h to 8 bits) one pair
-// in about two thousand exceeded 2e-2 x RMS of the fp64 oracle in the tail,
-// fp16 operands keep the worst pair near 1.5e-2.  |h| above the fp16 range
-// (65504) saturates and is reported as RVQ_DEV_ERR_NONFINITE.
+// Precision: both GEMMs run on fp16 operands with fp32 accumulation.  The
+// codewords are staged as fp16 and each weight is their fp16 sum; the tokens
+// are converted to fp16 once per launch pair (tokens_f16_kernel), and
+// h = silu(g) u is rounded to fp16.  fp16 keeps three more mantissa bits than
+// bf16: with bf16 down operands (the weight sum rounded twice, h to 8 bits)
+// one pair in about two thousand exceeded 2e-2 x RMS of the fp64 oracle, and
+// a weight summed in fp16 needs no conversion before the MMA.  Values beyond
+// the fp16 range (|x| or |h| > 65504) saturate and are reported as
+// RVQ_DEV_ERR_NONFINITE.
 //
 // GEMM orientation (swap-AB): A = 128 weight rows x 64 K (16-bit, in tensor
 // memory: row = TMEM lane, two K values per 32-bit column), B = up to 192
@@ -42,8 +44,8 @@
 // Warp roles (512 threads):
 //  warp 0      TMEM owner; lane 0 issues the MMAs (4 per M tile and K step)
 //              and commits
-//  warps 1-2   gate/up B producers: cp.async gathers of token rows into the
-//              B slot (fp32 inputs: converted to bf16 and stored)
+//  warps 1-2   gate/up B producers: cp.async gathers of fp16 token rows into
+//              the B slot
 //  warp 3      gate/up B relay (lane 0): once a slot's rows have landed,
 //              fences them into the async proxy and signals the K step (the
 //              fence costs the MMA thread nothing)
@@ -72,12 +74,12 @@
 // bound by the decode warps (~1,100-1,300 cycles for 32 rows x 64 K each).
 //
 // Decoding is bound by shared-memory gathers of codewords, so the codebooks
-// sit in shared memory as fp16 (summed in fp16, then rounded once to bf16) in
-// a bank-private layout: line (stage s, codeword k) is 128 bytes, and 16-byte
-// group q of every line serves lane q of each quarter-warp.  For gate/up,
-// groups 0-3 hold gate's codebook and 4-7 up's (lanes with r % 8 < 4 decode
-// gate rows); for down all eight hold down's.  A quarter-warp thus reads
-// eight codewords from eight distinct bank groups whatever the codes are.
+// sit in shared memory as fp16 in a bank-private layout: line (stage s,
+// codeword k) is 128 bytes, and 16-byte group q of every line serves lane q
+// of each quarter-warp.  For gate/up, groups 0-3 hold gate's codebook and 4-7
+// up's (lanes with r % 8 < 4 decode gate rows); for down all eight hold
+// down's.  A quarter-warp thus reads eight codewords from eight distinct bank
+// groups whatever the codes are.
 //
 // Every wait is bounded (1 s); on expiry the CTA records RVQ_DEV_ERR_TIMEOUT,
 // every role leaves its loop, the MMAs in flight are drained and TMEM is freed.
@@ -137,7 +139,7 @@ static_assert(kSlotB % 1024 == 0 && OFF_ST % 1024 == 0, "swizzled slots start on
 
 constexpr int kLoaders = 64;                     // gate/up B producer threads (warps 1-2)
 constexpr int kTmaRows = 32;                     // token rows per down B TMA box
-constexpr int kLoaderRows = 3;                   // token rows per producer thread (192 / 64)
+constexpr int kLoaderRows = PF_NMAX / 8;         // token rows per producer thread (8 threads a row)
 constexpr int kDecodeWarps = 8;                  // A producer warps (8-15)
 // full[] arrivals: the decode warps of the K step (down: one half of them;
 // gate/up: all eight, four per M tile) + the B side (the relay, or the TMA
@@ -145,7 +147,7 @@ constexpr int kDecodeWarps = 8;                  // A producer warps (8-15)
 constexpr uint32_t kFullCount = kDecodeWarps / 2 + 1;
 constexpr uint32_t kFullCountPair = kDecodeWarps + 1;
 
-// Three fp16x2 codeword words summed in fp16 (the down GEMM's fp16 weights).
+// Three fp16x2 codeword words summed in fp16: two fp16 weights.
 __device__ __forceinline__ uint32_t sum3_f16x2(uint32_t a, uint32_t b, uint32_t c) {
     const __half2 s = __hadd2(__hadd2(*reinterpret_cast<const __half2 *>(&a),
                                       *reinterpret_cast<const __half2 *>(&b)),
@@ -153,15 +155,9 @@ __device__ __forceinline__ uint32_t sum3_f16x2(uint32_t a, uint32_t b, uint32_t 
     return *reinterpret_cast<const uint32_t *>(&s);
 }
 
-// The same sum rounded once to bf16x2 (the gate/up GEMMs' bf16 weights).
-__device__ __forceinline__ uint32_t sum3_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
-    const uint32_t s = sum3_f16x2(a, b, c);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&s));
-    return pack_bf16x2(f.x, f.y);
-}
-
-// h = silu(g) u as fp16 bits for the down GEMM; |h| beyond the fp16 range
-// saturates to +-65504 and is reported (*over = true); NaN stays NaN.
+// A value as fp16 bits for the GEMMs (h = silu(g) u, or a token); beyond the
+// fp16 range it saturates to +-65504 and is reported (*over = true); NaN
+// stays NaN.
 __device__ __forceinline__ uint16_t h_to_f16(float hv, bool &over) {
     if (fabsf(hv) > 65504.0f) {
         over = true;
@@ -410,8 +406,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 if (!mbar_wait(bar(BAR_ACC_EMPTY + ab), (use & 1u) ^ 1u, abort_flag, job.status))
                     break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t idesc =
-                    pair ? idesc_bf16(PF_MROWS, I.npad) : idesc_f16(PF_MROWS, I.npad);
+                const uint32_t idesc = idesc_f16(PF_MROWS, I.npad);
                 bool ok = true;
                 for (int ks = 0; ks < KS; ++ks, ++kg) {
                     if (!mbar_wait_spin(bar(BAR_FULL + (kg & (PF_NBAR - 1))),
@@ -497,25 +492,32 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 }
             }
         } else if (warp < 3) {
+            // gate/up: fp16 token rows x16[entry / x_div], gathered by cp.async.
+            // Eight consecutive threads copy the eight 16-byte chunks of one row,
+            // so a warp instruction touches four 128-byte lines (one L1 tag
+            // lookup each) instead of 32.
             const int lt = tid - 32;
-            const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
+            const int c = lt & 7;                 // the 16-byte chunk this thread copies
+            const int r0 = lt >> 3;               // rows r0, r0 + 8, ...
+            const uint32_t sw = (uint32_t)((c ^ r0) << 4);  // 128-byte swizzle (row & 7 = r0)
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
                 const PfItem I = pf_item(job, Q, MT, it);
                 if (!I.valid) continue;
-                const uint8_t *src[kLoaderRows];
+                // token row of each of this thread's rows (-1: none)
+                int row[kLoaderRows];
 #pragma unroll
                 for (int r = 0; r < kLoaderRows; ++r) {
-                    const int j = lt + kLoaders * r;
-                    src[r] = nullptr;
+                    const int j = r0 + 8 * r;
+                    row[r] = -1;
                     if (j < I.n) {
                         const int p = job.pairs[I.o + I.j0 + j];
                         if (p >= 0 && p < job.n_pairs)
-                            src[r] = reinterpret_cast<const uint8_t *>(job.x) +
-                                     ((int64_t)(p / job.x_div) * job.x_stride) * esz;
+                            row[r] = p / job.x_div;
                         else
                             set_dev_error(job.status, RVQ_DEV_ERR_INDEX);
                     }
                 }
+                const uint8_t *xb = reinterpret_cast<const uint8_t *>(job.x) + c * 16;
                 bool ok = true;
                 for (int ks = 0; ks < KS; ++ks, ++kg) {
                     // the slot's previous K step (5 back) has been consumed
@@ -527,44 +529,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                             break;
                         }
                     }
-                    const uint32_t sb = sbase + OFF_ST + slot * kSlotB;
+                    const uint32_t sb = sbase + OFF_ST + slot * kSlotB + r0 * 128 + sw;
                     const uint32_t landed = bar(BAR_LANDED + (kg & (PF_NBAR - 1)));
-                    if (esz == 2) {
+                    const uint8_t *xk = xb + ks * PF_KC * 2;
 #pragma unroll
-                        for (int r = 0; r < kLoaderRows; ++r) {
-                            const int j = lt + kLoaders * r;
-                            if (src[r] != nullptr) {
-                                const uint8_t *s = src[r] + ks * PF_KC * 2;
-#pragma unroll
-                                for (int c = 0; c < 8; ++c)
-                                    cp_async16(sb + j * 128 + ((c ^ (j & 7)) << 4), s + c * 16);
-                            }
-                        }
-                        // arrives once this thread's copies have landed
-                        asm volatile(
-                            "cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(landed)
-                            : "memory");
-                    } else {
-                        uint8_t *bt = smem + OFF_ST + slot * kSlotB;
-#pragma unroll
-                        for (int r = 0; r < kLoaderRows; ++r) {
-                            const int j = lt + kLoaders * r;
-                            if (src[r] != nullptr) {
-                                const float4 *s =
-                                    reinterpret_cast<const float4 *>(src[r] + ks * PF_KC * 4);
-                                for (int c = 0; c < 8; ++c) {
-                                    const float4 f0 = s[2 * c], f1 = s[2 * c + 1];
-                                    *reinterpret_cast<uint4 *>(bt + j * 128 +
-                                                               ((c ^ (j & 7)) << 4)) =
-                                        make_uint4(pack_bf16x2(f0.x, f0.y),
-                                                   pack_bf16x2(f0.z, f0.w),
-                                                   pack_bf16x2(f1.x, f1.y),
-                                                   pack_bf16x2(f1.z, f1.w));
-                                }
-                            }
-                        }
-                        mbar_arrive(landed);
-                    }
+                    for (int r = 0; r < kLoaderRows; ++r)
+                        if (row[r] >= 0)
+                            cp_async16(sb + r * 8 * 128, xk + (int64_t)row[r] * job.x_stride * 2);
+                    // arrives once this thread's copies have landed
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(landed)
+                                 : "memory");
                     slot = slot == PF_NSLOT - 1 ? 0 : slot + 1;
                 }
                 if (!ok) break;
@@ -774,18 +748,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                             const uint4 w0 = lds128(cbl + k0 * kCbLine);
                             const uint4 w1 = lds128(cbl + (256 + k1) * kCbLine);
                             const uint4 w2 = lds128(cbl + (512 + k2) * kCbLine);
-                            // gate/up: bf16 weights; down: fp16 (see the file header)
-                            if (pair) {
-                                o[4 * c + 0] = sum3_bf16x2(w0.x, w1.x, w2.x);
-                                o[4 * c + 1] = sum3_bf16x2(w0.y, w1.y, w2.y);
-                                o[4 * c + 2] = sum3_bf16x2(w0.z, w1.z, w2.z);
-                                o[4 * c + 3] = sum3_bf16x2(w0.w, w1.w, w2.w);
-                            } else {
-                                o[4 * c + 0] = sum3_f16x2(w0.x, w1.x, w2.x);
-                                o[4 * c + 1] = sum3_f16x2(w0.y, w1.y, w2.y);
-                                o[4 * c + 2] = sum3_f16x2(w0.z, w1.z, w2.z);
-                                o[4 * c + 3] = sum3_f16x2(w0.w, w1.w, w2.w);
-                            }
+                            o[4 * c + 0] = sum3_f16x2(w0.x, w1.x, w2.x);
+                            o[4 * c + 1] = sum3_f16x2(w0.y, w1.y, w2.y);
+                            o[4 * c + 2] = sum3_f16x2(w0.z, w1.z, w2.z);
+                            o[4 * c + 3] = sum3_f16x2(w0.w, w1.w, w2.w);
                         }
                         tmem_st8(ta + tst + 8 * hq, o);
                     }
@@ -809,6 +775,39 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
 }
 
+// x [n][d] (fp32 or bf16) -> fp16, eight values per thread and step.
+__global__ void __launch_bounds__(256) tokens_f16_kernel(const void *x, int xdt, int64_t n8,
+                                                          uint4 *x16, uint32_t *status) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    bool over = false;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float v[8];
+        if (xdt == RVQ_BF16) {
+            const uint4 w = reinterpret_cast<const uint4 *>(x)[i];
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] = __uint_as_float(u[j] << 16);
+                v[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+            }
+        } else {
+            const float4 a = reinterpret_cast<const float4 *>(x)[2 * i];
+            const float4 b = reinterpret_cast<const float4 *>(x)[2 * i + 1];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = (uint32_t)h_to_f16(v[2 * j], over) |
+                   ((uint32_t)h_to_f16(v[2 * j + 1], over) << 16);
+        x16[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (over) set_dev_error(status, RVQ_DEV_ERR_NONFINITE);
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (the
 // library does not link the driver library itself).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -827,6 +826,30 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }  // namespace
 
 void *tensor_map_encoder_entry() { return reinterpret_cast<void *>(tensor_map_encoder()); }
+
+rvq_status launch_tokens_f16(const void *x, int xdt, int n, int d, uint16_t *x16,
+                             uint32_t *status, cudaStream_t stream, bool pdl) {
+    if ((xdt != RVQ_F32 && xdt != RVQ_BF16) || n < 1 || d < 8 || d % 8 != 0 ||
+        ((uintptr_t)x & 15u) != 0 || ((uintptr_t)x16 & 15u) != 0) {
+        set_error("tokens to fp16: dtype %d, n %d, d %d not supported", xdt, n, d);
+        return RVQ_EINVAL;
+    }
+    const int64_t n8 = (int64_t)n * d / 8;
+    const int64_t want = (n8 + 255) / 256;
+    const int blocks = (int)(want < 4 * num_sms() ? want : 4 * num_sms());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, tokens_f16_kernel, x, xdt, n8,
+                                reinterpret_cast<uint4 *>(x16), status));
+    return RVQ_OK;
+}
 
 rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) {
     static std::atomic<int> attr_done[64];  // per device; setting twice is harmless
@@ -850,16 +873,20 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
                   job.tile_rows, job.E);
         return RVQ_EINVAL;
     }
-    // down: B = the pass's contiguous bf16 h rows, loaded by TMA (a 2D map
+    if (job.x_dtype != PF_H_F16 || ((uintptr_t)job.x & 15u) != 0 || (job.x_stride * 2) % 16 != 0 ||
+        job.x_stride < job.cols || job.x_div < 1 || job.n_pairs < 1) {
+        set_error("prefill: B input must be fp16 rows of pitch >= %d (16-byte multiple), "
+                  "16-byte aligned", job.cols);
+        return RVQ_EINVAL;
+    }
+    // down: B = the pass's contiguous fp16 h rows, loaded by TMA (a 2D map
     // over h: cols x n_pairs rows, pitch x_stride, boxes of 64 columns x
     // kTmaRows rows, 128-byte swizzle; rows past the end read as zero)
     CUtensorMap tmap;
     memset(&tmap, 0, sizeof(tmap));
     if (job.mode == PF_MODE_PLAIN) {
-        if (job.x_dtype != PF_H_F16 || job.x_div != 1 || job.x_stride < job.cols ||
-            ((uintptr_t)job.x & 15u) != 0 || job.n_pairs < 1) {
-            set_error("prefill: down input must be fp16 h rows of pitch >= %d, 16-byte aligned",
-                      job.cols);
+        if (job.x_div != 1) {
+            set_error("prefill: down input must be h rows in grouped order");
             return RVQ_EINVAL;
         }
         const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();

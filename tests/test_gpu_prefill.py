@@ -1,5 +1,5 @@
 """GPU parity for the prefill (tensor-core) path of the expert FFN: RVQ code
-tiles decoded to bf16 and multiplied on tcgen05.  Held to 2e-2 x RMS per pair
+tiles decoded to fp16 and multiplied on tcgen05 with fp16 tokens.  Held to 2e-2 x RMS per pair
 output against the double-precision oracle; experts left on the lookup-table
 path in a mixed dispatch stay at 1e-4 x RMS.  Routing is the GPU's own (bit-
 exactness of routing is covered by test_gpu_router / test_gpu_layer)."""
@@ -83,10 +83,9 @@ def test_tensor_core_path_all_experts_d2048():
 
 
 def test_tensor_core_path_fp32_input():
-    """fp32 activations on the tensor-core path: the kernel's loaders convert
-    the token rows to bf16 instead of copying bf16 rows.  The values are
-    bf16-representable, so the conversion is exact and the bf16 tolerance
-    applies unchanged (general fp32 inputs add their own bf16 rounding)."""
+    """fp32 activations on the tensor-core path: the token conversion reads
+    fp32 rows instead of bf16 rows.  The values are bf16-representable, so
+    the fp16 conversion is exact and the tolerance applies unchanged."""
     sl, L, _ = layer(1)
     n = 24
     x32 = synth.bf16_to_f32(sl.tokens_bf16(n))
