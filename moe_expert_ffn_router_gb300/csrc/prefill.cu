@@ -123,7 +123,11 @@ constexpr int OFF_FLAG = OFF_TMEM + 4;
 constexpr int OFF_Q = OFF_BAR + 256;             // pass prefix [E + 1]
 constexpr int kMaxE = 256;
 constexpr int OFF_W = OFF_Q + 4 * (kMaxE + 2);   // cost prefix [E + 1] (int64)
-constexpr int kPfSmem = OFF_W + 8 * (kMaxE + 1) + 1024;  // + slack to align the base to 1 KiB
+constexpr int kItemTable = 256;                  // items of a CTA described in shared memory
+constexpr int OFF_IT = (OFF_W + 8 * (kMaxE + 1) + 15) & ~15;  // item table [kItemTable] (int4)
+constexpr int OFF_EPI = OFF_IT + 16 * kItemTable;     // down epilogue: pair ids of a chunk [4][32]
+constexpr int kPfSmem = OFF_EPI + 4 * 32 * 4 + 1024;  // + slack to align the base to 1 KiB
+static_assert(OFF_IT % 16 == 0 && OFF_EPI % 16 == 0, "item table alignment");
 static_assert(OFF_FLAG + 4 <= OFF_Q, "control block overlaps the pass prefix");
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
@@ -278,6 +282,26 @@ __device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, in
     return I;
 }
 
+// An item as one table entry: {o, rec, j0, e | n << 12 | mt << 21 | valid << 31}.
+__device__ __forceinline__ int4 pf_pack(const PfItem &I) {
+    return make_int4(I.o, I.rec, I.j0,
+                     (int)((uint32_t)I.e | ((uint32_t)I.n << 12) | ((uint32_t)I.mt << 21) |
+                           ((uint32_t)I.valid << 31)));
+}
+__device__ __forceinline__ PfItem pf_unpack(int4 v) {
+    PfItem I;
+    I.o = v.x;
+    I.rec = v.y;
+    I.j0 = v.z;
+    const uint32_t w = (uint32_t)v.w;
+    I.e = (int)(w & 0xFFFu);
+    I.n = (int)((w >> 12) & 0x1FFu);
+    I.mt = (int)((w >> 21) & 0x3FFu);
+    I.valid = (w >> 31) != 0;
+    I.npad = (I.n + 15) & ~15;
+    return I;
+}
+
 // kPair: gate/up launch (two M tiles per item, SwiGLU epilogue); otherwise down.
 template <bool kPair>
 __global__ void __launch_bounds__(PF_THREADS, 1)
@@ -381,6 +405,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int64_t T = W[job.E];
     const int it0 = pf_first_item(job, Q, W, MT, (int64_t)blockIdx.x * T / gridDim.x);
     const int it1 = pf_first_item(job, Q, W, MT, (int64_t)(blockIdx.x + 1) * T / gridDim.x);
+    // the first kItemTable items described once, one per thread, so that no
+    // role walks the offsets and record headers (dependent global loads)
+    // between items
+    int4 *itab = reinterpret_cast<int4 *>(smem + OFF_IT);
+    if (tid < kItemTable && it0 + tid < it1) itab[tid] = pf_pack(pf_item(job, Q, MT, it0 + tid));
+    __syncthreads();
+    auto item = [&](int it) -> PfItem {
+        return it - it0 < kItemTable ? pf_unpack(itab[it - it0]) : pf_item(job, Q, MT, it);
+    };
 
     if (warp == 0) {
         // ================= MMA issuer =================
@@ -391,7 +424,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // so the bounded wait expires and every role gives up
             if (job.selftest_stall) mbar_wait(bar(BAR_NEVER), 0, abort_flag, job.status);
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
-                const PfItem I = pf_item(job, Q, MT, it);
+                const PfItem I = item(it);
                 if (!I.valid) {
                     // a bad or missing record (header mismatch, no cache slot):
                     // every role skips the item; the MMA thread reports it
@@ -465,7 +498,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // thread loads kTmaRows-row boxes per K step
             if (warp == 1 && lane == 0) {
                 for (int it = it0; it < it1 && !*abort_flag; ++it) {
-                    const PfItem I = pf_item(job, Q, MT, it);
+                    const PfItem I = item(it);
                     if (!I.valid) continue;
                     const int nbox = (I.npad + kTmaRows - 1) / kTmaRows;
                     const uint32_t bytes = (uint32_t)nbox * kTmaRows * (PF_KC * 2);
@@ -501,7 +534,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const int r0 = lt >> 3;               // rows r0, r0 + 8, ...
             const uint32_t sw = (uint32_t)((c ^ r0) << 4);  // 128-byte swizzle (row & 7 = r0)
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
-                const PfItem I = pf_item(job, Q, MT, it);
+                const PfItem I = item(it);
                 if (!I.valid) continue;
                 // token row of each of this thread's rows (-1: none)
                 int row[kLoaderRows];
@@ -549,7 +582,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // (their arrivals release them); the fence orders them before the
             // MMA's async-proxy reads, which acquire through full[]
             for (int it = it0; it < it1 && !*abort_flag; ++it) {
-                const PfItem I = pf_item(job, Q, MT, it);
+                const PfItem I = item(it);
                 if (!I.valid) continue;
                 bool ok = true;
                 for (int ks = 0; ks < KS; ++ks, ++kg) {
@@ -566,26 +599,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
     } else if (warp < 8) {
         // ================= epilogue =================
+        // Compact on purpose: it runs once per item, and a fully unrolled
+        // epilogue (~45 KB of code) stalled the next item on instruction fetch.
         const int ew = warp - 4;                 // TMEM lanes 32 ew .. 32 ew + 31
         const int ar = ew * 32 + lane;           // A row
         const int q = lane & 7;
+        const bool up = swiglu && q >= 4;        // gate/up: this lane holds up's accumulator
         // weight row of this lane within the M tile (gate/up: gate lanes q < 4)
         const int rin = swiglu ? (ar >> 3) * 4 + (q & 3) : ar;
         const uint32_t tl = tmem + ((uint32_t)(ew * 32) << 16) + kTmemD;
         uint32_t nacc = 0;
+        bool over = false;
         for (int it = it0; it < it1; ++it) {
-            const PfItem I = pf_item(job, Q, MT, it);
+            const PfItem I = item(it);
             if (!I.valid) continue;
-            // the item's pair ids, one per lane and 32-token chunk, fetched
-            // before the accumulator is ready; -1 marks no token
-            constexpr int kChunks = PF_NMAX / 32;
-            int pl[kChunks];
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                const int j = 32 * c + lane;
-                int p = j < I.n ? job.pairs[I.o + I.j0 + j] : -1;
-                pl[c] = (p >= 0 && p < job.n_pairs) ? p : -1;
-            }
+            const int32_t *pp = job.pairs + I.o + I.j0;
+            // the pair id of the item's token j (-1: none)
+            auto pair_at = [&](int j) -> int {
+                const int p = j < I.n ? pp[j] : -1;
+                return (p >= 0 && p < job.n_pairs) ? p : -1;
+            };
+            const int nch = (I.n + 31) / 32;     // 32-token chunks of the accumulator
+            // down: the pair id of each token (its y row), fetched before the
+            // accumulator is ready (gate/up writes h by grouped position)
+            int p0 = swiglu ? -1 : pair_at(lane);
             const uint32_t ab = pair ? 0u : (nacc & 1u), use = pair ? nacc : (nacc >> 1);
             if (!mbar_wait(bar(BAR_ACC_FULL + ab), use & 1u, abort_flag, job.status)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -593,43 +630,70 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // released as soon as it is drained
 #pragma unroll 1
             for (int mu = 0; mu < (pair ? 2 : 1); ++mu) {
-            const uint32_t acc = pair ? (uint32_t)mu : ab;
-            const int R = ((pair ? 2 * I.mt + mu : I.mt)) * job.tile_rows + rin;
+                const uint32_t acc = pair ? (uint32_t)mu : ab;
+                const int R = ((pair ? 2 * I.mt + mu : I.mt)) * job.tile_rows + rin;
+                int pc = p0;
+#pragma unroll 1
+                for (int c = 0; c < nch; ++c) {
+                    const int pn = !swiglu && c + 1 < nch ? pair_at(32 * (c + 1) + lane) : -1;
+                    float a[32];
+                    tmem_ld32(tl + acc * PF_NMAX + 32 * c, a);
+                    if (swiglu) {
+                        // h rows in the grouped order; a gate lane and its up
+                        // partner (lane ^ 4) hold g and u of the same weight row:
+                        // the gate lane takes token t, the up lane token t + 1
+                        uint16_t *hrow = reinterpret_cast<uint16_t *>(job.out) +
+                                         (size_t)(I.o + I.j0 + 32 * c) * job.rows + R;
+                        const int nt = I.n - 32 * c;     // tokens of this chunk
+                        // two phases, so that the 16 exchanges and SwiGLUs overlap
+                        // instead of forming one chain per token pair
+                        float oth[16];
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                if (32 * c >= I.n) break;
-                float a[32];
-                tmem_ld32(tl + acc * PF_NMAX + 32 * c, a);
-                if (swiglu) {
-                    // row of token t: its position in the grouped order
-                    uint16_t *hrow = reinterpret_cast<uint16_t *>(job.out) +
-                                     (size_t)(I.o + I.j0 + 32 * c) * job.rows + R;
-                    bool over = false;
+                        for (int i = 0; i < 16; ++i)
+                            oth[i] = __shfl_xor_sync(0xffffffffu, up ? a[2 * i] : a[2 * i + 1], 4);
+                        // columns past the chunk's tokens hold padding: not converted
+                        const int t0 = up ? 1 : 0;
+                        uint16_t hb[16];
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const int p = __shfl_sync(0xffffffffu, pl[c], t);
-                        const float u = __shfl_xor_sync(0xffffffffu, a[t], 4);
-                        const float g = a[t];
-                        const float hv = __fdividef(g * u, 1.0f + __expf(-g));
-                        if (q < 4 && p >= 0) hrow[(size_t)t * job.rows] = h_to_f16(hv, over);
+                        for (int i = 0; i < 16; ++i) {
+                            const float g = up ? oth[i] : a[2 * i];
+                            const float u = up ? a[2 * i + 1] : oth[i];
+                            const float hv = __fdividef(g * u, 1.0f + __expf(-g));
+                            hb[i] = h_to_f16(2 * i + t0 < nt ? hv : 0.0f, over);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (2 * i + t0 < nt) hrow[(size_t)(2 * i + t0) * job.rows] = hb[i];
+                    } else {
+                        // the chunk's 32 pair ids to every lane through a per-warp
+                        // scratch (broadcast reads) rather than 32 shuffles
+                        int *pw = reinterpret_cast<int *>(smem + OFF_EPI) + 32 * ew;
+                        pw[lane] = pc;
+                        __syncwarp();
+                        int pv[32];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int4 v = reinterpret_cast<const int4 *>(pw)[i];
+                            pv[4 * i] = v.x;
+                            pv[4 * i + 1] = v.y;
+                            pv[4 * i + 2] = v.z;
+                            pv[4 * i + 3] = v.w;
+                        }
+                        __syncwarp();
+                        float *yrow = reinterpret_cast<float *>(job.out) + R;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (pv[t] >= 0) yrow[(size_t)pv[t] * job.rows] = a[t];
                     }
-                    if (__any_sync(0xffffffffu, over) && lane == 0)
-                        set_dev_error(job.status, RVQ_DEV_ERR_NONFINITE);
-                } else {
-                    float *yrow = reinterpret_cast<float *>(job.out) + R;
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const int p = __shfl_sync(0xffffffffu, pl[c], t);
-                        if (p >= 0) yrow[(size_t)p * job.rows] = a[t];
-                    }
+                    pc = pn;
                 }
-            }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + acc));
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + acc));
             }
             ++nacc;
         }
+        if (__any_sync(0xffffffffu, over) && lane == 0) set_dev_error(job.status, RVQ_DEV_ERR_NONFINITE);
     } else {
         // ================= A producers (decode into TMEM) =================
         const int dt = tid - 256;
@@ -647,11 +711,36 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kTmemA;
         const int RB = job.rows / 32;
         const int G = KS / 4;                    // 32-chunk groups along K
+        // this row's code planes of 32-chunk group 0 of an item: 6 x 16 bytes
+        // (stage s, half h) at cp + (2 s + h) * 512; group g adds g * RB tiles
+        auto planes_of = [&](const PfItem &J) -> const uint8_t * {
+            const int R = (pair ? 2 * J.mt + u : J.mt) * job.tile_rows + rin;
+            return job.base + (uint64_t)J.rec * job.record_bytes + job.codes_off[mat] +
+                   (size_t)(R >> 5) * kTileBytes + (R & 31) * 16;
+        };
+        // the first valid item at or after `from` (it1: none)
+        auto next_valid = [&](int from, PfItem &J) -> int {
+            for (; from < it1; ++from) {
+                J = item(from);
+                if (J.valid) break;
+            }
+            return from;
+        };
         int cur_e = -1;
         uint32_t kg = 0, ncb = 0;
-        for (int it = it0; it < it1 && !*abort_flag; ++it) {
-            const PfItem I = pf_item(job, Q, MT, it);
-            if (!I.valid) continue;
+        PfItem I;
+        int it = next_valid(it0, I);
+        // the planes of the item's first group, loaded one group ahead (across
+        // items too: the next item's first group loads during this item's last)
+        uint4 nxt[6];
+        if (it < it1) {
+            const uint8_t *cp0 = planes_of(I);
+#pragma unroll
+            for (int v = 0; v < 6; ++v) nxt[v] = *reinterpret_cast<const uint4 *>(cp0 + v * 512);
+        }
+        while (it < it1 && !*abort_flag) {
+            PfItem In;
+            const int itn = next_valid(it + 1, In);
             const uint8_t *rec = job.base + (uint64_t)I.rec * job.record_bytes;
             if (I.e != cur_e) {
                 // every A producer is done with the previous codebooks
@@ -690,11 +779,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // step 4 g + half + 2) in bytes 16..23 (gate/up: half 0, every
             // chunk j at byte j).
             const int rot = (l - 8 * half) & 31;
-            // this row's code planes of 32-chunk group g: 6 x 16 bytes (stage s, half h)
-            const uint8_t *cp = rec + job.codes_off[mat] + (size_t)(R >> 5) * kTileBytes + l * 16;
-            uint4 nxt[6];
-#pragma unroll
-            for (int v = 0; v < 6; ++v) nxt[v] = *reinterpret_cast<const uint4 *>(cp + v * 512);
+            const uint8_t *cp = planes_of(I);
+            const uint8_t *cpn = itn < it1 ? planes_of(In) : nullptr;
             bool ok = true;
             for (int g = 0; g < G && ok; ++g) {
                 uint32_t U[3][8];
@@ -711,12 +797,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 }
 #pragma unroll
                 for (int s = 0; s < 3; ++s) derotate(U[s], rot);
-                // the next group's planes load while this one decodes
-                if (g + 1 < G) {
-                    const uint8_t *cpn = cp + (size_t)(g + 1) * RB * kTileBytes;
+                // the next group's planes (or the next item's first) load while
+                // this one decodes
+                const uint8_t *cg = g + 1 < G ? cp + (size_t)(g + 1) * RB * kTileBytes : cpn;
+                if (cg != nullptr) {
 #pragma unroll
                     for (int v = 0; v < 6; ++v)
-                        nxt[v] = *reinterpret_cast<const uint4 *>(cpn + v * 512);
+                        nxt[v] = *reinterpret_cast<const uint4 *>(cg + v * 512);
                 }
 #pragma unroll
                 for (int j = 0; j < nj; ++j) {
@@ -763,6 +850,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             if (!ok) break;
             kg += KS;
+            it = itn;
+            I = In;
         }
     }
 
@@ -867,8 +956,8 @@ rvq_status launch_prefill_gemm(const PfJob &job, cudaStream_t stream, bool pdl) 
     // gate/up items take two M tiles
     const int tile_mult = job.mode == PF_MODE_SWIGLU ? 2 * job.tile_rows : job.tile_rows;
     if ((job.mode != PF_MODE_SWIGLU && job.mode != PF_MODE_PLAIN) || job.tile_rows != want_rows ||
-        job.rows % tile_mult || job.cols % (4 * PF_KC) || job.E < 1 || job.E > kMaxE ||
-        job.min_tokens < 1) {
+        job.rows % tile_mult || job.rows / tile_mult > 1023 || job.cols % (4 * PF_KC) ||
+        job.E < 1 || job.E > kMaxE || job.min_tokens < 1) {
         set_error("prefill: rows %d / cols %d / tile %d / E %d not supported", job.rows, job.cols,
                   job.tile_rows, job.E);
         return RVQ_EINVAL;
