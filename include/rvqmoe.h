@@ -373,12 +373,14 @@ rvq_status moe_expert_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
 
 /* As moe_expert_ffn, with per-expert dispatch to the tensor-core path.
  * Experts whose group holds at least tc_min_tokens tokens are computed by
- * the prefill path: their codes are decoded tile by tile to bf16 on chip
- * (W = C1[c1] + C2[c2] + C3[c3] from shared-memory codebooks, rounded to bf16,
- * held in tensor memory as the MMA's A operand) and multiplied with bf16
- * activations on the tensor cores (tcgen05, fp32 accumulators in TMEM):
- * gate and up GEMMs, h = silu(g) * u rounded to bf16, down GEMM.  Results of
- * those experts carry bf16 rounding (the tests hold them to 2e-2 x RMS).
+ * the prefill path: their codes are decoded tile by tile to fp16 on chip
+ * (W = C1[c1] + C2[c2] + C3[c3] from fp16 shared-memory codebooks, summed in
+ * fp16, held in tensor memory as the MMA's A operand) and multiplied with the
+ * tokens converted to fp16 on the tensor cores (tcgen05, fp32 accumulators in
+ * TMEM): gate and up GEMMs, h = silu(g) * u rounded to fp16, down GEMM.
+ * Results of those experts carry 16-bit rounding (the tests hold them to
+ * 2e-2 x RMS).  A token or h value beyond the fp16 range (65504) saturates
+ * and sets RVQ_DEV_ERR_NONFINITE.
  * tc_min_tokens <= 0: every expert takes the lookup-table path (identical to
  * moe_expert_ffn); 1: every expert takes the tensor-core path.  A bounded
  * device wait that expires sets RVQ_DEV_ERR_TIMEOUT. */

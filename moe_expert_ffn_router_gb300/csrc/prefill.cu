@@ -18,34 +18,37 @@
 // RVQ_DEV_ERR_NONFINITE.
 //
 // GEMM orientation (swap-AB): A = 128 weight rows x 64 K (16-bit, in tensor
-// memory: row = TMEM lane, two K values per 32-bit column), B = up to 192
+// memory: row = TMEM lane, two K values per 32-bit column), B = up to NMAX
 // tokens of one expert's group x 64 K (K-major, 128-byte swizzle, shared
 // memory), D = W x^T (128 rows x N tokens, fp32, TMEM).  The decode warps
 // write their rows of A straight into tensor memory (tcgen05.st), so A costs
 // no shared-memory stores or operand reads, and every MMA reads B once.
 //
-// A work item is (expert, pass of <= 192 tokens, M tiles of 128 A rows):
-//  * gate/up launch: an M tile holds 64 weight rows of gate and the same 64
-//    rows of up, interleaved in fours (A row r holds weight row
+// A work item is (expert, pass of <= NMAX tokens, M tiles of 128 A rows):
+//  * gate/up launch (NMAX 160): an M tile holds 64 weight rows of gate and the
+//    same 64 rows of up, interleaved in fours (A row r holds weight row
 //    64 m + 4 (r / 8) + r % 4, of gate if r % 8 < 4, of up otherwise), so a
 //    row's gate and up accumulators sit four TMEM lanes apart and the epilogue
 //    pairs them with one shuffle: h = silu(g) * u -> fp16, row = the token's
 //    position in the expert-grouped order, so each pass's rows are contiguous.
 //    An item takes two M tiles (2 m, 2 m + 1) that share every K step's
-//    gathered token rows: 8 MMAs per B slot, half the L2 -> SM row traffic
-//    (the rows were the bound: ~7.7 cycles per gathered row per K step).
-//  * down launch: the A rows are down rows [128 m, 128 m + 128); B is the
-//    pass's contiguous h rows, loaded by TMA; the epilogue writes fp32 y
-//    [pair][d].
+//    gathered token rows (8 MMAs per B slot).
+//  * down launch (NMAX 192): the A rows are down rows [128 m, 128 m + 128); B
+//    is the pass's contiguous h rows, loaded by TMA; the epilogue writes fp32
+//    y [pair][d].
 // Items are split into contiguous ranges of equal estimated cost over a
 // persistent grid (one CTA per SM), so consecutive items of a CTA mostly share
-// the expert and its codebooks.
+// the expert and its codebooks.  The first 256 items of a CTA are described
+// once, in shared memory, by all threads at the start: walking the offsets
+// and record headers between items (dependent global loads) cost each role
+// ~3,500 cycles per item.
 //
 // Warp roles (512 threads):
 //  warp 0      TMEM owner; lane 0 issues the MMAs (4 per M tile and K step)
 //              and commits
 //  warps 1-2   gate/up B producers: cp.async gathers of fp16 token rows into
-//              the B slot
+//              the B slot, eight threads per 128-byte row (a warp instruction
+//              touches four lines, not 32)
 //  warp 3      gate/up B relay (lane 0): once a slot's rows have landed,
 //              fences them into the async proxy and signals the K step (the
 //              fence costs the MMA thread nothing)
@@ -55,23 +58,27 @@
 //  warps 8-15  A producers: decode code bytes into TMEM (lane quarter =
 //              warp % 4); down: warps 8-11 take the even K steps, 12-15 the
 //              odd ones; gate/up: warps 8-11 the item's first M tile, 12-15
-//              its second, every K step
+//              its second, every K step.  Each warp loads its rows' code
+//              planes one 32-chunk group ahead, across items too.
 // K step t of the CTA's sequence uses an A stage (down: t % 4, TMEM columns
-// 384 + 32 s; gate/up: t % 2, columns 384 + 64 s + 32 u for M tile u), B slot
-// t % 5 (shared memory; five slots keep up to 120 KiB of token rows in flight
-// against the L2 latency of the row gathers) and the full/empty mbarrier pair
-// t % 8.  full[t % 8] completes once the decode warps of the K step and the B
-// side (the relay, or the TMA producer's expect_tx arrival and its bytes)
-// have arrived, so the MMA thread waits once and commits once per K step.
-// A decode warp reuses a stage after empty[t - stages], a B producer a slot
+// 384 + 32 s; gate/up: t % 3, columns 320 + 64 s + 32 u for M tile u), B slot
+// t % 5 (shared memory; five slots keep the token rows in flight against the
+// L2 latency of the row gathers) and the full/empty mbarrier pair t % 8.
+// full[t % 8] completes once the decode warps of the K step and the B side
+// (the relay, or the TMA producer's expect_tx arrival and its bytes) have
+// arrived, so the MMA thread waits once and commits once per K step.  A
+// decode warp reuses a stage after empty[t - stages], a B producer a slot
 // after empty[(t - 5) % 8].  Down: two accumulators (TMEM columns 0 and 192,
 // guarded by acc_full / acc_empty) let the epilogue of one item overlap the
-// main loop of the next.  Gate/up: the item's M tiles use both, each released
-// by the epilogue as soon as it is drained (the next item's first M tile
-// starts while the second still drains).
-// Measured limits: a single M=128 MMA occupies the tensor pipe for at least
-// ~80 cycles whatever N <= 160; with paired M tiles the gate/up K step is
-// bound by the decode warps (~1,100-1,300 cycles for 32 rows x 64 K each).
+// main loop of the next.  Gate/up: the item's M tiles use both (columns 0 and
+// 160), each released by the epilogue as soon as it is drained (the next
+// item's first M tile starts while the second still drains).
+// Measured limits (per-K-step clock traces of the 2048-token chunk): the MMA
+// thread sets the K step.  Eight M=128 MMAs of a gate/up K step take ~900
+// cycles with the decode switched off (~110 per instruction, most passes
+// having fewer than 160 tokens) and ~1,140 with it on: the decode warps'
+// shared-memory reads and TMEM stores slow the tensor pipe; the decode
+// itself takes ~800 cycles and runs ahead in the three stages.
 //
 // Decoding is bound by shared-memory gathers of codewords, so the codebooks
 // sit in shared memory as fp16 in a bank-private layout: line (stage s,
@@ -96,7 +103,9 @@ namespace rvq {
 namespace {
 
 constexpr int PF_THREADS = 512;
-constexpr int PF_NMAX = 192;                     // tokens per pass (MMA N)
+constexpr int PF_NMAX = 192;                     // tokens per pass (MMA N), down
+constexpr int PF_NMAX_PAIR = 160;                // gate/up: two accumulators of 160 columns leave
+                                                 // TMEM room for three A stages
 constexpr int PF_KC = 64;                        // K columns per stage (one 128-byte swizzle row)
 constexpr int PF_NST = 4;                        // A stages (TMEM)
 constexpr int PF_NSLOT = 5;                      // B slots (shared memory)
@@ -131,19 +140,20 @@ static_assert(OFF_IT % 16 == 0 && OFF_EPI % 16 == 0, "item table alignment");
 static_assert(OFF_FLAG + 4 <= OFF_Q, "control block overlaps the pass prefix");
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemD = 0;                   // accumulator b: columns [PF_NMAX b, + PF_NMAX)
-constexpr uint32_t kTmemA = 2 * PF_NMAX;         // A stage s: columns [kTmemA + 32 s, + 32)
-static_assert(kTmemA + PF_NST * (PF_KC / 2) <= kTmemCols, "TMEM columns");
+constexpr uint32_t kTmemD = 0;                   // accumulator b: columns [NMAX b, + NMAX)
+// down: A stage s at columns [2 PF_NMAX + 32 s, + 32)
+static_assert(2 * PF_NMAX + PF_NST * (PF_KC / 2) <= kTmemCols, "TMEM columns");
 // gate/up items pair two M tiles on one B slot: accumulator of M tile u at
-// columns [PF_NMAX u, + PF_NMAX), A stage s of M tile u at kTmemA + 64 s + 32 u
-constexpr int PF_NST_PAIR = 2;
-static_assert(kTmemA + PF_NST_PAIR * PF_KC <= kTmemCols, "TMEM columns (paired M tiles)");
+// columns [PF_NMAX_PAIR u, + PF_NMAX_PAIR), A stage s of M tile u at
+// 2 PF_NMAX_PAIR + 64 s + 32 u
+constexpr int PF_NST_PAIR = 3;
+static_assert(2 * PF_NMAX_PAIR + PF_NST_PAIR * PF_KC <= kTmemCols, "TMEM columns (paired M tiles)");
 static_assert(PF_NBAR >= PF_NSLOT + 1 && PF_NBAR >= PF_NST + 1, "a barrier pair outlives its stage");
 static_assert(kSlotB % 1024 == 0 && OFF_ST % 1024 == 0, "swizzled slots start on 1 KiB");
 
 constexpr int kLoaders = 64;                     // gate/up B producer threads (warps 1-2)
 constexpr int kTmaRows = 32;                     // token rows per down B TMA box
-constexpr int kLoaderRows = PF_NMAX / 8;         // token rows per producer thread (8 threads a row)
+constexpr int kLoaderRows = PF_NMAX_PAIR / 8;    // token rows per producer thread (8 threads a row)
 constexpr int kDecodeWarps = 8;                  // A producer warps (8-15)
 // full[] arrivals: the decode warps of the K step (down: one half of them;
 // gate/up: all eight, four per M tile) + the B side (the relay, or the TMA
@@ -222,15 +232,20 @@ __device__ __forceinline__ int64_t pf_cost(const PfJob &job, int npad) {
     return job.mode == PF_MODE_SWIGLU ? (int64_t)210 + npad / 2 : (int64_t)116 + npad / 8;
 }
 
+// Tokens per pass of the launch.
+__device__ __forceinline__ int pf_nmax(const PfJob &job) {
+    return job.mode == PF_MODE_SWIGLU ? PF_NMAX_PAIR : PF_NMAX;
+}
+
 // Passes of expert e (0 when its group is below min_tokens) and their cost.
 __device__ __forceinline__ void pf_expert_cost(const PfJob &job, int ne, int MT, int &passes,
                                                int64_t &cost) {
-    passes = ne >= job.min_tokens && ne > 0 ? (ne + PF_NMAX - 1) / PF_NMAX : 0;
+    const int NM = pf_nmax(job);
+    passes = ne >= job.min_tokens && ne > 0 ? (ne + NM - 1) / NM : 0;
     cost = 0;
     if (passes > 0) {
-        const int last = ne - (passes - 1) * PF_NMAX;
-        cost = (int64_t)MT *
-               ((passes - 1) * pf_cost(job, PF_NMAX) + pf_cost(job, (last + 15) & ~15));
+        const int last = ne - (passes - 1) * NM;
+        cost = (int64_t)MT * ((passes - 1) * pf_cost(job, NM) + pf_cost(job, (last + 15) & ~15));
     }
 }
 
@@ -245,9 +260,10 @@ __device__ int pf_first_item(const PfJob &job, const int32_t *Q, const int64_t *
         if (W[mid] <= t) lo = mid; else hi = mid;
     }
     const int ne = job.offsets[lo + 1] - job.offsets[lo];
-    const int P = (ne + PF_NMAX - 1) / PF_NMAX;
-    const int64_t cf = pf_cost(job, PF_NMAX);
-    const int64_t cl = pf_cost(job, (ne - (P - 1) * PF_NMAX + 15) & ~15);
+    const int NM = pf_nmax(job);
+    const int P = (ne + NM - 1) / NM;
+    const int64_t cf = pf_cost(job, NM);
+    const int64_t cl = pf_cost(job, (ne - (P - 1) * NM + 15) & ~15);
     int64_t rem = t - W[lo];
     const int64_t pq = rem / ((int64_t)MT * cf);
     const int pi = (int)(pq < (int64_t)P - 1 ? pq : (int64_t)P - 1);
@@ -270,8 +286,9 @@ __device__ __forceinline__ PfItem pf_item(const PfJob &job, const int32_t *Q, in
     I.e = lo;
     I.o = job.offsets[lo];
     const int ne = job.offsets[lo + 1] - I.o;
-    I.j0 = (pi - Q[lo]) * PF_NMAX;
-    I.n = min(PF_NMAX, ne - I.j0);
+    const int NM = pf_nmax(job);
+    I.j0 = (pi - Q[lo]) * NM;
+    I.n = min(NM, ne - I.j0);
     I.npad = (I.n + 15) & ~15;
     I.rec = record_of(job, lo);
     const rvq_expert_header *h = I.rec < 0 ? nullptr :
@@ -322,6 +339,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     constexpr bool swiglu = kPair;
     const int MT = job.rows / job.tile_rows / (pair ? 2 : 1);  // items per pass
     constexpr int NST = pair ? PF_NST_PAIR : PF_NST;           // A stages: K step t uses t % NST
+    constexpr int NMAX = pair ? PF_NMAX_PAIR : PF_NMAX;        // tokens per pass
+    constexpr uint32_t kTmemA = 2 * NMAX;                      // first A stage column
     const int KS = job.cols / PF_KC;             // a multiple of 4
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -452,7 +471,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     // start-address field: +1 per 16 bytes (32 bytes per 16 K)
                     const uint64_t bd = bdesc0 + slot * (uint32_t)(kSlotB >> 4);
                     if (pair) {
-                        const uint32_t ta = tmem + kTmemA + (kg & (PF_NST_PAIR - 1)) * PF_KC;
+                        const uint32_t ta = tmem + kTmemA + (kg % PF_NST_PAIR) * PF_KC;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_bf16_ts(tmem + kTmemD, ta + kk * 8, bd + 2 * kk, idesc,
@@ -467,11 +486,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         }
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ts(tmem + kTmemD + PF_NMAX, ta + 32 + kk * 8, bd + 2 * kk,
+                            mma_bf16_ts(tmem + kTmemD + NMAX, ta + 32 + kk * 8, bd + 2 * kk,
                                         idesc, (ks > 0 || kk > 0) ? 1u : 0u);
                     } else {
                         const uint32_t ta = tmem + kTmemA + (kg & (PF_NST - 1)) * (PF_KC / 2);
-                        const uint32_t td = tmem + kTmemD + ab * PF_NMAX;
+                        const uint32_t td = tmem + kTmemD + ab * NMAX;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_bf16_ts(td, ta + kk * 8, bd + 2 * kk, idesc,
@@ -637,7 +656,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 for (int c = 0; c < nch; ++c) {
                     const int pn = !swiglu && c + 1 < nch ? pair_at(32 * (c + 1) + lane) : -1;
                     float a[32];
-                    tmem_ld32(tl + acc * PF_NMAX + 32 * c, a);
+                    tmem_ld32(tl + acc * NMAX + 32 * c, a);
                     if (swiglu) {
                         // h rows in the grouped order; a gate lane and its up
                         // partner (lane ^ 4) hold g and u of the same weight row:
@@ -809,7 +828,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 for (int j = 0; j < nj; ++j) {
                     // this K step, its A stage and its first code word
                     const uint32_t kt = pair ? kg + 4 * g + j : kg + 4 * g + 2 * j + half;
-                    const uint32_t st = kt & (uint32_t)(NST - 1);
+                    const uint32_t st = kt % (uint32_t)NST;
                     const int w0 = pair ? 2 * j : 4 * j;
                     const uint32_t tst = pair ? st * PF_KC + 32 * u : st * (PF_KC / 2);
                     // the stage's previous K step (NST back) has been consumed
