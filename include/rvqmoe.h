@@ -167,8 +167,11 @@ rvq_status rvq_gemv(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
  * rvq_gemv_noalloc_status: synchronous; waits for `stream`, then reads the
  * device status word of the array (what rvq_ws_status reads from a
  * workspace) and returns RVQ_OK, RVQ_EDEVICE, RVQ_ECORRUPT or RVQ_ETIMEOUT,
- * storing the raw bits in *bits_out if not NULL and clearing them.  The GEMV
- * sets a bit only when one of its bounded waits expires (RVQ_ETIMEOUT).
+ * storing the raw bits in *bits_out if not NULL and clearing them.  The
+ * single-matrix GEMV reads no expert records, offsets or pair lists and has
+ * no bounded waits, so its launches detect no device-side error and the word
+ * reads 0 after them; the call is there so that a caller never has to assume
+ * that (and reads any bit a later kernel of the path might set).
  * ------------------------------------------------------------------------ */
 #define RVQ_NOALLOC_SCRATCH_BYTES 4194304u /* 4 MiB */
 rvq_status rvq_gemv_noalloc(const uint8_t *packed_codes_dev, const float *packed_cb_dev,
