@@ -45,7 +45,7 @@
 //
 // Warp roles (512 threads):
 //  warp 0      TMEM owner; lane 0 issues the MMAs (4 per M tile and K step)
-//              and commits
+//              and commits; gate/up: M tile 0 only
 //  warps 1-2   gate/up B producers: cp.async gathers of fp16 token rows into
 //              the B slot, eight threads per 128-byte row (a warp instruction
 //              touches four lines, not 32)
@@ -54,7 +54,10 @@
 //              fence costs the MMA thread nothing)
 //  warp 1 l.0  down B producer: tiled TMA loads of the pass's h rows (async
 //              proxy, completion counted on the K step's full barrier)
-//  warps 4-7   epilogue: TMEM -> registers -> global (lane quarter = warp % 4)
+//  warps 4-7   epilogue: TMEM -> registers -> global (lane quarter = warp % 4);
+//              gate/up: warp 7 lane 0 issues M tile 1's MMAs of an item before
+//              the warp drains it (a second issuing thread: one thread issues
+//              a tcgen05.mma only about every 115 cycles)
 //  warps 8-15  A producers: decode code bytes into TMEM (lane quarter =
 //              warp % 4); down: warps 8-11 take the even K steps, 12-15 the
 //              odd ones; gate/up: warps 8-11 the item's first M tile, 12-15
@@ -123,13 +126,13 @@ constexpr int BAR_EMPTY = BAR_FULL + PF_NBAR;    // [PF_NBAR]
 constexpr int BAR_LANDED = BAR_EMPTY + PF_NBAR;  // [PF_NBAR] B rows of the K step in shared memory
 constexpr int BAR_ACC_FULL = BAR_LANDED + PF_NBAR;    // [2]
 constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;       // [2]
-constexpr int BAR_DONE = BAR_ACC_EMPTY + 2;
-constexpr int BAR_CB = BAR_DONE + 1;             // A producers: codebook swap rendezvous
+constexpr int BAR_DONE = BAR_ACC_EMPTY + 2;      // [2]: each MMA issuer's final drain
+constexpr int BAR_CB = BAR_DONE + 2;             // A producers: codebook swap rendezvous
 constexpr int BAR_NEVER = BAR_CB + 1;            // self-test: a phase nothing completes
 constexpr int kNumBars = BAR_NEVER + 1;
 constexpr int OFF_TMEM = OFF_BAR + 8 * kNumBars;
 constexpr int OFF_FLAG = OFF_TMEM + 4;
-constexpr int OFF_Q = OFF_BAR + 256;             // pass prefix [E + 1]
+constexpr int OFF_Q = OFF_BAR + 512;             // pass prefix [E + 1]
 constexpr int kMaxE = 256;
 constexpr int OFF_W = OFF_Q + 4 * (kMaxE + 2);   // cost prefix [E + 1] (int64)
 constexpr int kItemTable = 256;                  // items of a CTA described in shared memory
@@ -400,7 +403,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (lane == 0) {
             for (int s = 0; s < PF_NBAR; ++s) {
                 mbar_init(bar(BAR_FULL + s), pair ? kFullCountPair : kFullCount);
-                mbar_init(bar(BAR_EMPTY + s), 1);
+                // gate/up: each M tile's MMA issuer commits (two arrivals)
+                mbar_init(bar(BAR_EMPTY + s), pair ? 2 : 1);
                 mbar_init(bar(BAR_LANDED + s), kLoaders);
             }
             for (int b = 0; b < 2; ++b) {
@@ -408,6 +412,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 mbar_init(bar(BAR_ACC_EMPTY + b), 4);
             }
             mbar_init(bar(BAR_DONE), 1);
+            mbar_init(bar(BAR_DONE + 1), 1);
             mbar_init(bar(BAR_CB), kDecodeWarps);
             mbar_init(bar(BAR_NEVER), 1);
             *abort_flag = 0;
@@ -434,11 +439,52 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         return it - it0 < kItemTable ? pf_unpack(itab[it - it0]) : pf_item(job, Q, MT, it);
     };
 
+    // The MMAs of one item on accumulator `acc` (TMEM columns acc * NMAX),
+    // issued by one thread: gate/up M tile u == acc (its A stage columns
+    // + 32 u), down the item's alternating accumulator.  One thread issues a
+    // tcgen05.mma about every 115 cycles whatever N <= 192 (a microbenchmark;
+    // two threads on separate accumulators issue twice as many), so gate/up
+    // gives each M tile its own issuing thread: warp 0 lane 0 (tile 0) and
+    // warp 7 lane 0 (tile 1, between its epilogue drains).  Returns false once
+    // the kernel aborts.
+    const uint64_t bdesc0 = smem_desc(sbase + OFF_ST);
+    auto issue_item = [&](const PfItem &I, uint32_t &kg, uint32_t &slot, uint32_t acc,
+                          uint32_t acc_use, uint32_t u) -> bool {
+        if (!mbar_wait(bar(BAR_ACC_EMPTY + acc), (acc_use & 1u) ^ 1u, abort_flag, job.status))
+            return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t idesc = idesc_f16(PF_MROWS, I.npad);
+        const uint32_t td = tmem + kTmemD + acc * NMAX;
+        for (int ks = 0; ks < KS; ++ks, ++kg) {
+            if (!mbar_wait(bar(BAR_FULL + (kg & (PF_NBAR - 1))), (kg / PF_NBAR) & 1u, abort_flag,
+                           job.status))
+                return false;
+            // (the B producers fenced their slot writes into the async proxy)
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // start-address field: +1 per 16 bytes (32 bytes per 16 K)
+            const uint64_t bd = bdesc0 + slot * (uint32_t)(kSlotB >> 4);
+            const uint32_t ta = pair ? tmem + kTmemA + (kg % NST) * PF_KC + 32 * u
+                                     : tmem + kTmemA + (kg % NST) * (PF_KC / 2);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ts(td, ta + kk * 8, bd + 2 * kk, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(BAR_EMPTY + (kg & (PF_NBAR - 1))));
+            slot = slot == PF_NSLOT - 1 ? 0 : slot + 1;
+        }
+        mma_commit(bar(BAR_ACC_FULL + acc));
+        return true;
+    };
+    // every MMA an issuer queued has completed before TMEM is released
+    auto issuer_drain = [&](int which) {
+        mma_commit(bar(BAR_DONE + which));
+        int no_abort = 0;
+        mbar_wait(bar(BAR_DONE + which), 0, &no_abort, job.status);
+    };
+
     if (warp == 0) {
         // ================= MMA issuer =================
         if (lane == 0) {
             uint32_t kg = 0, slot = 0, nacc = 0;  // K steps, B slot, items consumed
-            const uint64_t bdesc0 = smem_desc(sbase + OFF_ST);
             // self-test of the failure path: wait for an arrival nothing makes,
             // so the bounded wait expires and every role gives up
             if (job.selftest_stall) mbar_wait(bar(BAR_NEVER), 0, abort_flag, job.status);
@@ -450,63 +496,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     if (I.n > 0) set_dev_error(job.status, RVQ_DEV_ERR_CORRUPT);
                     continue;
                 }
-                // down: two accumulators alternate over items; gate/up: an item
-                // uses both (one per M tile), each released by the epilogue on
-                // its own, so the next item starts on M tile 0 while the
-                // epilogue still drains M tile 1
+                // down: two accumulators alternate over items; gate/up: this
+                // thread issues M tile 0 on accumulator 0 (warp 7 issues M
+                // tile 1 on accumulator 1), each released by the epilogue on
+                // its own
                 const uint32_t ab = pair ? 0u : (nacc & 1u), use = pair ? nacc : (nacc >> 1);
-                if (!mbar_wait(bar(BAR_ACC_EMPTY + ab), (use & 1u) ^ 1u, abort_flag, job.status))
-                    break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t idesc = idesc_f16(PF_MROWS, I.npad);
-                bool ok = true;
-                for (int ks = 0; ks < KS; ++ks, ++kg) {
-                    if (!mbar_wait_spin(bar(BAR_FULL + (kg & (PF_NBAR - 1))),
-                                        (kg / PF_NBAR) & 1u, abort_flag, job.status)) {
-                        ok = false;
-                        break;
-                    }
-                    // (the B producers fenced their slot writes into the async proxy)
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    // start-address field: +1 per 16 bytes (32 bytes per 16 K)
-                    const uint64_t bd = bdesc0 + slot * (uint32_t)(kSlotB >> 4);
-                    if (pair) {
-                        const uint32_t ta = tmem + kTmemA + (kg % PF_NST_PAIR) * PF_KC;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ts(tmem + kTmemD, ta + kk * 8, bd + 2 * kk, idesc,
-                                        (ks > 0 || kk > 0) ? 1u : 0u);
-                        if (ks == 0) {
-                            if (!mbar_wait_spin(bar(BAR_ACC_EMPTY + 1), (use & 1u) ^ 1u,
-                                                abort_flag, job.status)) {
-                                ok = false;
-                                break;
-                            }
-                            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ts(tmem + kTmemD + NMAX, ta + 32 + kk * 8, bd + 2 * kk,
-                                        idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-                    } else {
-                        const uint32_t ta = tmem + kTmemA + (kg & (PF_NST - 1)) * (PF_KC / 2);
-                        const uint32_t td = tmem + kTmemD + ab * NMAX;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ts(td, ta + kk * 8, bd + 2 * kk, idesc,
-                                        (ks > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bar(BAR_EMPTY + (kg & (PF_NBAR - 1))));
-                    slot = slot == PF_NSLOT - 1 ? 0 : slot + 1;
-                }
-                if (!ok) break;
-                mma_commit(bar(BAR_ACC_FULL + ab));
+                if (!issue_item(I, kg, slot, ab, use, 0)) break;
                 ++nacc;
             }
-            // drain: every MMA issued has completed before TMEM is released
-            mma_commit(bar(BAR_DONE));
-            int no_abort = 0;
-            mbar_wait(bar(BAR_DONE), 0, &no_abort, job.status);
+            issuer_drain(0);
         }
         __syncwarp();
     } else if (warp < 4) {
@@ -629,9 +627,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const uint32_t tl = tmem + ((uint32_t)(ew * 32) << 16) + kTmemD;
         uint32_t nacc = 0;
         bool over = false;
+        // gate/up: warp 7 lane 0 also issues M tile 1's MMAs of each item
+        // (between draining the previous item and draining this one)
+        const bool issuer = pair && warp == 7;
+        uint32_t kg1 = 0, slot1 = 0;
+        bool issue_ok = true;
         for (int it = it0; it < it1; ++it) {
             const PfItem I = item(it);
             if (!I.valid) continue;
+            if (issuer) {
+                if (lane == 0 && issue_ok && !*abort_flag)
+                    issue_ok = issue_item(I, kg1, slot1, 1, nacc, 1);
+                __syncwarp();
+            }
             const int32_t *pp = job.pairs + I.o + I.j0;
             // the pair id of the item's token j (-1: none)
             auto pair_at = [&](int j) -> int {
@@ -643,13 +651,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // accumulator is ready (gate/up writes h by grouped position)
             int p0 = swiglu ? -1 : pair_at(lane);
             const uint32_t ab = pair ? 0u : (nacc & 1u), use = pair ? nacc : (nacc >> 1);
-            if (!mbar_wait(bar(BAR_ACC_FULL + ab), use & 1u, abort_flag, job.status)) break;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // gate/up: the item's two M tiles, accumulators 0 and 1, each
-            // released as soon as it is drained
+            // drained once its own issuer's MMAs are done and released as soon
+            // as it is drained
+            bool acc_ok = true;
 #pragma unroll 1
             for (int mu = 0; mu < (pair ? 2 : 1); ++mu) {
                 const uint32_t acc = pair ? (uint32_t)mu : ab;
+                if (!mbar_wait(bar(BAR_ACC_FULL + acc), use & 1u, abort_flag, job.status)) {
+                    acc_ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const int R = ((pair ? 2 * I.mt + mu : I.mt)) * job.tile_rows + rin;
                 int pc = p0;
 #pragma unroll 1
@@ -710,9 +723,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + acc));
             }
+            if (!acc_ok) break;
             ++nacc;
         }
         if (__any_sync(0xffffffffu, over) && lane == 0) set_dev_error(job.status, RVQ_DEV_ERR_NONFINITE);
+        if (issuer && lane == 0) issuer_drain(1);
+        __syncwarp();
     } else {
         // ================= A producers (decode into TMEM) =================
         const int dt = tid - 256;
