@@ -244,11 +244,37 @@ def test_stalled_pipeline_times_out_and_recovers():
     test_tensor_core_path_all_experts_d2048()
 
 
+def test_tokens_beyond_fp16_range_are_reported():
+    """The tensor-core path computes on fp16 operands: a token value beyond
+    the fp16 range (65,504) saturates and is reported as RVQ_DEV_ERR_NONFINITE
+    in the workspace status, and the context stays usable.  The lookup-table
+    path (fp32) takes the same input without a report."""
+    sl, L, _ = layer(1)
+    n = 8
+    bits = sl.tokens_bf16(n).copy()
+    bits[3, 17] = 0x47C3                     # bf16 99,840 (1.5234375 x 2^16)
+    x = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    b = route(L, x, n)
+    y = torch.empty((n * L.k, L.d), dtype=torch.float32, device=DEV)
+    rvq.moe_expert_ffn_ex(L.bank, x, n, L.k, b["offsets"], b["pairs"], y, b["ws"], 1)
+    torch.cuda.synchronize()
+    rc, flags = rvq.rvq_ws_status(b["ws"])
+    assert rc == 5 and flags & rvq.DEV_ERR_NONFINITE, (rc, flags)   # RVQ_EDEVICE
+    assert rvq.rvq_ws_status(b["ws"]) == (0, 0)                     # the read cleared it
+    rvq.moe_expert_ffn_ex(L.bank, x, n, L.k, b["offsets"], b["pairs"], y, b["ws"], 0)
+    torch.cuda.synchronize()
+    assert rvq.rvq_ws_status(b["ws"]) == (0, 0)
+    # the context is healthy: an in-range batch on the tensor cores is correct
+    test_tensor_core_path_all_experts_d2048()
+
+
 def test_prefill_multipass_groups_every_pair_d2048():
-    """Groups larger than one pass of the tensor-core kernel (passes of at
-    most 192 tokens): 1024 tokens of the d = 2048 layer with a Zipf router
-    bias strong enough (beta 0.5) that the three largest groups hold 760, 593
-    and 487 tokens, i.e. four, four and three passes with ragged last ones.
+    """Groups larger than one pass of the tensor-core kernels (gate/up passes
+    of at most 160 tokens, down passes of at most 192): 1024 tokens of the
+    d = 2048 layer with a Zipf router bias strong enough (beta 0.5) that the
+    three largest groups hold 760, 593 and 487 tokens, i.e. five, four and
+    four gate/up passes (four, four and three down passes) with ragged last
+    ones.
     Every pair of those three groups (1,840 pairs, first, middle and last
     passes alike) is compared with the oracle expert FFN at 2e-2 x RMS; the
     oracle calls run on a thread pool (the C oracle releases the GIL)."""
