@@ -69,19 +69,21 @@
 // L2 latency of the row gathers) and the full/empty mbarrier pair t % 8.
 // full[t % 8] completes once the decode warps of the K step and the B side
 // (the relay, or the TMA producer's expect_tx arrival and its bytes) have
-// arrived, so the MMA thread waits once and commits once per K step.  A
-// decode warp reuses a stage after empty[t - stages], a B producer a slot
-// after empty[(t - 5) % 8].  Down: two accumulators (TMEM columns 0 and 192,
+// arrived, so each MMA-issuing thread waits once and commits once per K step
+// (gate/up: empty[] takes both issuers' commits).  A decode warp reuses a
+// stage after empty[t - stages], a B producer a slot after
+// empty[(t - 5) % 8].  Down: two accumulators (TMEM columns 0 and 192,
 // guarded by acc_full / acc_empty) let the epilogue of one item overlap the
 // main loop of the next.  Gate/up: the item's M tiles use both (columns 0 and
 // 160), each released by the epilogue as soon as it is drained (the next
 // item's first M tile starts while the second still drains).
-// Measured limits (per-K-step clock traces of the 2048-token chunk): the MMA
-// thread sets the K step.  Eight M=128 MMAs of a gate/up K step take ~900
-// cycles with the decode switched off (~110 per instruction, most passes
-// having fewer than 160 tokens) and ~1,140 with it on: the decode warps'
-// shared-memory reads and TMEM stores slow the tensor pipe; the decode
-// itself takes ~800 cycles and runs ahead in the three stages.
+// Measured limits (per-warp clock traces of the 2048-token chunk): a decode
+// warp takes ~700-780 cycles per gate/up K step, and issuing a tcgen05.mma
+// occupies the issuing thread's sub-partition for ~85-115 cycles.  The decode
+// warps on the sub-partitions that also run an issuer or the loaders start
+// each step late, so the K step settles at ~1,150 cycles (~750 with the
+// decode switched off).  Down is bound by its single issuer (4 MMAs and one
+// wait, fence and commit per K step, ~650 cycles), its decode running ahead.
 //
 // Decoding is bound by shared-memory gathers of codewords, so the codebooks
 // sit in shared memory as fp16 in a bank-private layout: line (stage s,
