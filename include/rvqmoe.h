@@ -450,6 +450,37 @@ rvq_status moe_layer_forward_host(const rvq_moe_bank *bank, const float *wr_dev,
                                   int32_t *pairs_dev, float *out_dev, float *out_host, void *ws_dev,
                                   size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream);
 
+/* A CUDA graph of one layer call, for loops that run the same layer on the
+ * same buffers step after step (decode).  moe_layer_graph_create records the
+ * launches of moe_layer_forward_ex (x is also the residual; no event marks)
+ * once, by stream capture on `stream`, and instantiates them; each
+ * moe_layer_graph_launch then runs the whole layer as one graph launch on the
+ * stream it is given, without the per-kernel host launch cost.
+ *  - x_host and out_host both non-NULL: the graph also holds the copy of
+ *    x_host (n x d of xdt) into x_dev before the layer and of out_dev (fp32
+ *    n x d) into out_host after it, as moe_layer_forward_host; both NULL: the
+ *    layer reads x_dev as it is when the graph runs.  One of them NULL: EINVAL.
+ *  - The graph records pointers, not contents: every buffer must outlive the
+ *    graph, and each launch reads what they hold when it runs.
+ *  - Creating queues no work.  `stream` must be a stream that can be captured
+ *    (not the legacy default stream): otherwise RVQ_ECUDA, nothing recorded.
+ *  - Arguments are checked as in moe_layer_forward_host before the capture
+ *    starts (EINVAL / EALIGN / ENOMEM; *graph_out is set to NULL on error).
+ * moe_layer_graph_destroy frees the graph (NULL: no-op); it must not run
+ * while a launch of it is pending on a stream that has not been synchronised.
+ * The pages have no counterpart: this is how the library replays its launch
+ * sequence on the GPU. */
+typedef struct rvq_layer_graph rvq_layer_graph;
+rvq_status moe_layer_graph_create(const rvq_moe_bank *bank, const float *wr_dev,
+                                  const float *bias_dev, const void *x_host, rvq_dtype xdt,
+                                  int32_t n, int32_t k, void *x_dev, float *logits_dev,
+                                  int32_t *topk_idx_dev, float *topk_w_dev, int32_t *offsets_dev,
+                                  int32_t *pairs_dev, float *out_dev, float *out_host, void *ws_dev,
+                                  size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream,
+                                  rvq_layer_graph **graph_out);
+rvq_status moe_layer_graph_launch(const rvq_layer_graph *graph, rvq_stream_t stream);
+rvq_status moe_layer_graph_destroy(rvq_layer_graph *graph);
+
 /* A pre-norm layer of a stack in one call: xn = bf16(h / sqrt(mean(h^2) +
  * eps)) row by row (the values moe_rms_norm gives), then moe_layer_forward_ex
  * with x = xn (bf16) and residual = h: out = h + sum_slot w * expert(xn).

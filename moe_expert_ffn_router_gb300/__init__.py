@@ -99,6 +99,11 @@ _SIGS = {
                                     _vp, _vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp]),
     "moe_layer_forward_host": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
+    "moe_layer_graph_create": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp, _vp, _sz, _i32, _vp,
+                                      ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_layer_graph_launch": (_i32, [_vp, _vp]),
+    "moe_layer_graph_destroy": (_i32, [_vp]),
     "moe_layer_forward_prenorm": (_i32, [_BANKP, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
     "moe_rms_norm": (_i32, [_vp, _i32, _i32, _i32, ctypes.c_float, _vp, _i32, _vp]),
@@ -372,6 +377,52 @@ def moe_layer_forward_host(bank, wr, bias, x_host, n, k, x_dev, logits, topk_idx
                                        _p(offsets), _p(pairs), _p(out),
                                        ctypes.c_void_p(out_host.data_ptr()), _p(ws), _nbytes(ws),
                                        int(tc_min_tokens), _stream(stream)))
+
+
+class LayerGraph:
+    """A CUDA graph of one layer call (moe_layer_graph_create): launch() runs
+    the whole layer as one graph launch; close() frees it.  Holds references
+    to the buffers it records, so they outlive it."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep
+
+    def launch(self, stream=None):
+        _check("moe_layer_graph_launch", _lib.moe_layer_graph_launch(self._h, _stream(stream)))
+
+    def close(self):
+        if self._h is not None:
+            _check("moe_layer_graph_destroy", _lib.moe_layer_graph_destroy(self._h))
+            self._h = None
+            self._keep = None
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.moe_layer_graph_destroy(self._h)
+
+
+def moe_layer_graph_create(bank, wr, bias, n, k, x_dev, logits, topk_idx, topk_w, offsets, pairs,
+                           out, ws, tc_min_tokens=0, x_host=None, out_host=None, stream=None):
+    """Records one layer call (optionally with the copies of x_host in and of
+    out back to out_host) as a CUDA graph; stream must be capturable (not the
+    legacy default stream).  Returns a LayerGraph."""
+    if (x_host is None) != (out_host is None):
+        raise ValueError("x_host and out_host go together")
+    if x_host is not None:
+        assert not x_host.is_cuda and not out_host.is_cuda and x_host.dtype == x_dev.dtype
+        assert x_host.is_contiguous() and out_host.is_contiguous()
+        assert out_host.dtype == torch.float32 and out_host.numel() >= n * out.shape[-1]
+    h = ctypes.c_void_p()
+    _check("moe_layer_graph_create",
+           _lib.moe_layer_graph_create(
+               ctypes.byref(bank), _p(wr), _p(bias),
+               None if x_host is None else ctypes.c_void_p(x_host.data_ptr()), _dt(x_dev), n, k,
+               _p(x_dev), _p(logits), _p(topk_idx), _p(topk_w), _p(offsets), _p(pairs), _p(out),
+               None if out_host is None else ctypes.c_void_p(out_host.data_ptr()), _p(ws),
+               _nbytes(ws), int(tc_min_tokens), _stream(stream), ctypes.byref(h)))
+    return LayerGraph(h, (bank, wr, bias, x_dev, logits, topk_idx, topk_w, offsets, pairs, out,
+                          ws, x_host, out_host))
 
 
 def moe_layer_forward_prenorm(bank, wr, bias, h, n, k, eps, xn, logits, topk_idx, topk_w, offsets,

@@ -7,6 +7,8 @@
 
 #include <vector>
 
+#include <new>
+
 #include "internal.cuh"
 
 namespace rvq {
@@ -831,29 +833,136 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
     return mark(7);
 }
 
+// The checks of a layer call whose input and output may live in host memory
+// (both host pointers or neither, per `host_needed`), before anything is queued.
+static rvq_status check_layer_io(const rvq_moe_bank *bank, const float *wr_dev, const void *x_host,
+                                 rvq_dtype xdt, int32_t n, int32_t k, const void *x_dev,
+                                 const float *logits_dev, const int32_t *topk_idx_dev,
+                                 const float *topk_w_dev, const int32_t *offsets_dev,
+                                 const int32_t *pairs_dev, const float *out_dev,
+                                 const float *out_host, void *ws_dev, size_t ws_bytes,
+                                 bool host_needed, const char *who) {
+    CHECK_ARG(bank && x_dev && out_dev, "%s: null pointer", who);
+    if (host_needed)
+        CHECK_ARG(x_host && out_host, "%s: null host pointer", who);
+    else
+        CHECK_ARG((x_host == nullptr) == (out_host == nullptr),
+                  "%s: x_host and out_host must be given together", who);
+    CHECK_ARG(n >= 1 && bank->d > 0, "%s: n %d", who, n);
+    CHECK_ARG(xdt == RVQ_F32 || xdt == RVQ_BF16, "%s: dtype %d", who, (int)xdt);
+    CHECK_ALIGN(x_dev, who);
+    RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, who));
+    CHECK_ARG(wr_dev && logits_dev && topk_idx_dev && topk_w_dev && offsets_dev && pairs_dev,
+              "%s: null pointer", who);
+    CHECK_ALIGN(out_dev, who);
+    if (xdt == RVQ_BF16)
+        CHECK_ARG((const void *)out_dev != x_dev, "%s: bf16 x cannot alias out", who);
+    return RVQ_OK;
+}
+
+// x_host -> x_dev, the layer, out_dev -> out_host (the copies only when the
+// host pointers are given), all queued on st.
+static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
+                                 const float *bias_dev, const void *x_host, rvq_dtype xdt,
+                                 int32_t n, int32_t k, void *x_dev, float *logits_dev,
+                                 int32_t *topk_idx_dev, float *topk_w_dev, int32_t *offsets_dev,
+                                 int32_t *pairs_dev, float *out_dev, float *out_host, void *ws_dev,
+                                 size_t ws_bytes, int32_t tc_min_tokens, cudaStream_t st) {
+    const size_t esz = xdt == RVQ_BF16 ? 2 : 4;
+    const size_t xbytes = (size_t)n * bank->d * esz, obytes = (size_t)n * bank->d * 4;
+    if (x_host) RVQ_CUDA(cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, st));
+    RVQ_TRY(moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
+                                 topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
+                                 nullptr, xdt, tc_min_tokens, nullptr, (rvq_stream_t)st));
+    if (out_host) RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
+    return RVQ_OK;
+}
+
 rvq_status moe_layer_forward_host(const rvq_moe_bank *bank, const float *wr_dev,
                                   const float *bias_dev, const void *x_host, rvq_dtype xdt,
                                   int32_t n, int32_t k, void *x_dev, float *logits_dev,
                                   int32_t *topk_idx_dev, float *topk_w_dev, int32_t *offsets_dev,
                                   int32_t *pairs_dev, float *out_dev, float *out_host, void *ws_dev,
                                   size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream) {
-    CHECK_ARG(bank && x_host && out_host && x_dev && out_dev, "moe_layer_forward_host: null pointer");
-    CHECK_ARG(n >= 1 && bank->d > 0, "moe_layer_forward_host: n %d", n);
-    CHECK_ARG(xdt == RVQ_F32 || xdt == RVQ_BF16, "moe_layer_forward_host: dtype %d", (int)xdt);
-    CHECK_ALIGN(x_dev, "moe_layer_forward_host: x_dev");
     // every argument of the layer call is checked before the first copy
-    RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_layer_forward_host"));
-    CHECK_ARG(wr_dev && logits_dev && topk_idx_dev && topk_w_dev && offsets_dev && pairs_dev,
-              "moe_layer_forward_host: null pointer");
-    CHECK_ALIGN(out_dev, "moe_layer_forward_host: out_dev");
-    const size_t esz = xdt == RVQ_BF16 ? 2 : 4;
-    const size_t xbytes = (size_t)n * bank->d * esz, obytes = (size_t)n * bank->d * 4;
+    RVQ_TRY(check_layer_io(bank, wr_dev, x_host, xdt, n, k, x_dev, logits_dev, topk_idx_dev,
+                           topk_w_dev, offsets_dev, pairs_dev, out_dev, out_host, ws_dev, ws_bytes,
+                           true, "moe_layer_forward_host"));
+    return queue_layer_io(bank, wr_dev, bias_dev, x_host, xdt, n, k, x_dev, logits_dev,
+                          topk_idx_dev, topk_w_dev, offsets_dev, pairs_dev, out_dev, out_host,
+                          ws_dev, ws_bytes, tc_min_tokens, (cudaStream_t)stream);
+}
+
+}  // extern "C"
+
+// An instantiated graph of one layer call (moe_layer_graph_create).
+struct rvq_layer_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+rvq_status moe_layer_graph_create(const rvq_moe_bank *bank, const float *wr_dev,
+                                  const float *bias_dev, const void *x_host, rvq_dtype xdt,
+                                  int32_t n, int32_t k, void *x_dev, float *logits_dev,
+                                  int32_t *topk_idx_dev, float *topk_w_dev, int32_t *offsets_dev,
+                                  int32_t *pairs_dev, float *out_dev, float *out_host, void *ws_dev,
+                                  size_t ws_bytes, int32_t tc_min_tokens, rvq_stream_t stream,
+                                  rvq_layer_graph **graph_out) {
+    CHECK_ARG(graph_out, "moe_layer_graph_create: null graph_out");
+    *graph_out = nullptr;
+    RVQ_TRY(check_layer_io(bank, wr_dev, x_host, xdt, n, k, x_dev, logits_dev, topk_idx_dev,
+                           topk_w_dev, offsets_dev, pairs_dev, out_dev, out_host, ws_dev, ws_bytes,
+                           false, "moe_layer_graph_create"));
     cudaStream_t st = (cudaStream_t)stream;
-    RVQ_CUDA(cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, st));
-    RVQ_TRY(moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
-                                 topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
-                                 nullptr, xdt, tc_min_tokens, nullptr, stream));
-    RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
+    // relaxed: the launch helpers may set function attributes on first use
+    RVQ_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed));
+    const rvq_status rc = queue_layer_io(bank, wr_dev, bias_dev, x_host, xdt, n, k, x_dev,
+                                         logits_dev, topk_idx_dev, topk_w_dev, offsets_dev,
+                                         pairs_dev, out_dev, out_host, ws_dev, ws_bytes,
+                                         tc_min_tokens, st);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(st, &g);  // the capture always ends here
+    if (rc != RVQ_OK || ce != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        if (rc != RVQ_OK) return rc;
+        set_error("moe_layer_graph_create: stream capture failed: %s", cudaGetErrorString(ce));
+        return RVQ_ECUDA;
+    }
+    cudaGraphExec_t ex = nullptr;
+    const cudaError_t ie = cudaGraphInstantiate(&ex, g, 0);
+    if (ie != cudaSuccess) {
+        cudaGraphDestroy(g);
+        set_error("moe_layer_graph_create: cudaGraphInstantiate: %s", cudaGetErrorString(ie));
+        return RVQ_ECUDA;
+    }
+    rvq_layer_graph *lg = new (std::nothrow) rvq_layer_graph{g, ex};
+    if (!lg) {
+        cudaGraphExecDestroy(ex);
+        cudaGraphDestroy(g);
+        set_error("moe_layer_graph_create: out of host memory");
+        return RVQ_ENOMEM;
+    }
+    *graph_out = lg;
+    return RVQ_OK;
+}
+
+rvq_status moe_layer_graph_launch(const rvq_layer_graph *graph, rvq_stream_t stream) {
+    CHECK_ARG(graph, "moe_layer_graph_launch: null graph");
+    RVQ_CUDA(cudaGraphLaunch(graph->exec, (cudaStream_t)stream));
+    return RVQ_OK;
+}
+
+rvq_status moe_layer_graph_destroy(rvq_layer_graph *graph) {
+    if (!graph) return RVQ_OK;
+    const cudaError_t a = cudaGraphExecDestroy(graph->exec);
+    const cudaError_t b = cudaGraphDestroy(graph->graph);
+    delete graph;
+    if (a != cudaSuccess || b != cudaSuccess) {
+        set_error("moe_layer_graph_destroy: %s", cudaGetErrorString(a != cudaSuccess ? a : b));
+        return RVQ_ECUDA;
+    }
     return RVQ_OK;
 }
 

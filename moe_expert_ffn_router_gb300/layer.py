@@ -9,6 +9,7 @@ from . import (RVQ_WS_STATUS_BYTES, moe_bank_init, moe_bank_record_bytes, moe_ba
                moe_bank_write_expert, moe_cache_bank, moe_cache_create, moe_cache_destroy,
                moe_cache_stats, moe_combine, moe_expert_ffn, moe_layer_forward,
                moe_layer_forward_host, moe_layer_forward_prenorm, moe_layer_forward_streamed,
+               moe_layer_graph_create,
                moe_rms_norm, moe_route,
                moe_router_logits,
                moe_workspace_bytes, rvq_ws_clear, rvq_ws_status)
@@ -112,6 +113,22 @@ class MoeLayer:
                                b["idx"], b["w"], b["offsets"], b["pairs"], b["out"], out_host,
                                b["ws"], tc_min_tokens=tc_min_tokens)
         return b
+
+    def graph(self, x_dev: torch.Tensor, bufs: dict, x_host: torch.Tensor | None = None,
+              out_host: torch.Tensor | None = None, tc_min_tokens: int = 0):
+        """A CUDA graph of this layer on x_dev and bufs (optionally with the
+        copy of x_host into x_dev before it and of the output to out_host
+        after it), recorded on a side stream; launch() runs it on the current
+        stream."""
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream())
+        g = moe_layer_graph_create(self.bank, self.wr, self.bias, x_dev.shape[0], self.k, x_dev,
+                                   bufs["logits"], bufs["idx"], bufs["w"], bufs["offsets"],
+                                   bufs["pairs"], bufs["out"], bufs["ws"],
+                                   tc_min_tokens=tc_min_tokens, x_host=x_host, out_host=out_host,
+                                   stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
 
     def forward_steps(self, x: torch.Tensor) -> dict:
         """Same layer through the separate calls (router, route, FFN, combine)."""

@@ -98,6 +98,38 @@ def test_bank_init_checks():
     assert lib.moe_workspace_bytes(ctypes.byref(bank), 1, 8) > 256
 
 
+def test_layer_graph_checks_before_capturing():
+    """moe_layer_graph_create checks its arguments as the host-buffer layer
+    call does, before any stream capture starts, and leaves *graph_out NULL;
+    launching or destroying a NULL graph is refused / a no-op."""
+    bank = rvq.RvqMoeBank()
+    rb = rvq.moe_bank_record_bytes(2048, 1024)
+    assert lib.moe_bank_init(ctypes.byref(bank), A256, rb * 64, 64, 2048, 1024, 0) == 0
+    ws = lib.moe_workspace_bytes(ctypes.byref(bank), 4, 8)
+    out = ctypes.c_void_p(12345)
+    args = [ctypes.byref(bank), A16, None, None, 1, 4, 8, A16, A16, A16, A16, A16, A16, A16 + 0x100,
+            None, A256, ws, 0, None, ctypes.byref(out)]
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        out.value = 12345
+        rc = lib.moe_layer_graph_create(*a)
+        assert out.value is None          # *graph_out cleared on every refusal
+        return rc
+    EINVAL, EALIGN, ENOMEM = 1, 2, 3
+    assert lib.moe_layer_graph_create(*args[:-1], None) == EINVAL     # no graph_out
+    assert call(a3=A16) == EINVAL                   # x_host without out_host
+    assert call(a14=A16) == EINVAL                  # out_host without x_host
+    assert call(a7=A16 + 2) == EALIGN               # x_dev
+    assert call(a16=ws - 1) == ENOMEM               # workspace too small
+    assert call(a5=0) == EINVAL                     # no tokens
+    assert call(a4=7) == EINVAL                     # dtype
+    assert call(a13=A16) == EINVAL                  # bf16 x aliasing out
+    assert lib.moe_layer_graph_launch(None, None) == EINVAL
+    assert lib.moe_layer_graph_destroy(None) == 0
+
+
 def test_workspace_sizes_grow_with_batch():
     bank = rvq.RvqMoeBank()
     rb = rvq.moe_bank_record_bytes(7168, 2048)

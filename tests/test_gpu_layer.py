@@ -194,3 +194,59 @@ def test_host_buffer_layer_call_equals_device_call():
     torch.cuda.synchronize()
     assert torch.equal(out_host, ref["out"].cpu())
     assert torch.equal(hb["x_dev"].cpu().view(torch.int16), x_host.view(torch.int16))
+
+
+def test_layer_graph_replays_the_direct_call():
+    """A layer recorded as a CUDA graph (moe_layer_graph_create) and launched
+    step after step gives bit for bit what the direct layer call gives on the
+    same inputs: routing, pair plan, expert FFN and combine, for lookup-table
+    decode batches, through host buffers, and with tensor-core dispatch."""
+    sl, L = layer(1)
+    pool = sl.tokens_bf16(3 * 40)
+    # decode batch on device buffers: new tokens copied into x_dev between launches
+    n = 4
+    x_dev = torch.empty((n, L.d), dtype=torch.bfloat16, device=DEV)
+    b = L.buffers(n)
+    g = L.graph(x_dev, b)
+    for step in range(3):
+        bits = pool[step * n:(step + 1) * n]
+        x_dev.copy_(bf16_dev(bits))
+        g.launch()
+        torch.cuda.synchronize()
+        got = b["out"].clone()
+        idx = b["idx"].clone()
+        ref = L.forward(bf16_dev(bits))
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref["out"]), step
+        assert torch.equal(idx, ref["idx"]), step
+    assert L.status(n) == (0, 0)
+    g.close()
+    # the same batch through pinned host buffers recorded in the graph
+    x_host = torch.empty((n, L.d), dtype=torch.bfloat16).pin_memory()
+    out_host = torch.full((n, L.d), float("nan"), dtype=torch.float32).pin_memory()
+    x2 = torch.empty((n, L.d), dtype=torch.bfloat16, device=DEV)
+    b2 = L.buffers(n)
+    g2 = L.graph(x2, b2, x_host=x_host, out_host=out_host)
+    for step in range(2):
+        bits = pool[40 + step * n:40 + (step + 1) * n]
+        x_host.view(torch.int16).copy_(torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)))
+        g2.launch()
+        torch.cuda.synchronize()
+        ref = L.forward(bf16_dev(bits))
+        torch.cuda.synchronize()
+        assert torch.equal(out_host, ref["out"].cpu()), step
+    g2.close()
+    # a prefill-sized batch with every expert on the tensor cores
+    n = 40
+    x3 = torch.empty((n, L.d), dtype=torch.bfloat16, device=DEV)
+    b3 = L.buffers(n)
+    g3 = L.graph(x3, b3, tc_min_tokens=1)
+    bits = pool[80:120]
+    x3.copy_(bf16_dev(bits))
+    g3.launch()
+    torch.cuda.synchronize()
+    ref = L.forward(bf16_dev(bits), tc_min_tokens=1)
+    torch.cuda.synchronize()
+    assert torch.equal(b3["out"], ref["out"])
+    assert L.status(n) == (0, 0)
+    g3.close()
