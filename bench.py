@@ -395,6 +395,15 @@ def run_gpu(args, rank, world, local_rank):
         for j, name in enumerate(kernels):
             per[name].append(evs[j].elapsed_time(evs[j + 1]))
     avg = {k: float(np.mean(v)) for k, v in per.items() if k != "unused"}
+    # decode batches on lookup tables: the routing launch writes the pair plan
+    # and the down GEMV reduces its own SwiGLU inputs, so those two event
+    # intervals hold no launch
+    fused = tc_min == 0 and batch <= 16
+    fused_swiglu = fused and s.d // 256 <= 32 and batch <= 4
+    if fused:
+        avg.pop("lut_plan", None)
+    if fused_swiglu:
+        avg.pop("swiglu_reduce", None)
     if tc_min > 0:
         # useful FLOPs: 2 per multiply-add, gate + up (2 d f) then down (d f)
         # for each of the n k routed (token, expert) pairs
@@ -476,8 +485,10 @@ def run_gpu(args, rank, world, local_rank):
                          + router_launches(batch, s.E, s.d) - 1
                          # a stack's pre-norm: inside the router launch for one token
                          + (1 if n_layers > 1 and batch > 1 else 0)
-                         # decode batches on lookup tables: the pair plan inside the routing launch
-                         - (1 if tc_min == 0 and batch <= 16 else 0)) * args.steps * n_layers,
+                         # decode batches on lookup tables: the pair plan inside the routing
+                         # launch, the SwiGLU reduction inside the down GEMV
+                         - (1 if fused else 0) - (1 if fused_swiglu else 0))
+                        * args.steps * n_layers,
                config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
     del L, stack, built
     return res
@@ -864,7 +875,11 @@ def run_stream(args, rank, world, local_rank):
         "clocks": sampler.summary(t0w, t1w),
         # per layer: norm, router, top-k, pair plan, 2 GEMVs, SwiGLU, combine (+ the
         # lookahead router of the next layer)
-        "gpu_launches": args.steps * (wl.n_layers * 8 + (wl.n_layers - 1 if lookahead else 0)),
+        # per layer: norm, router logits, route, pair plan, gate/up GEMV,
+        # SwiGLU reduction (inside the down GEMV up to 4 tokens), down GEMV,
+        # combine; lookahead adds the next layer's router
+        "gpu_launches": args.steps * (wl.n_layers * (7 if batch <= 4 and s.d // 256 <= 32 else 8)
+                                      + (wl.n_layers - 1 if lookahead else 0)),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -572,9 +572,17 @@ rvq_status rvq::run_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype x
         RVQ_TRY(mark(0));
         RVQ_TRY(launch_lut_gemv_il(gu, pd, st, pdl));
         RVQ_TRY(mark(1));
-        RVQ_TRY(launch_swiglu_reduce(gpart, upart, np, P.nslot_gu, bank->f, h, st, pdl));
+        if (P.nslot_gu <= kIlSwigluMaxSlots && n <= kIlSwigluMaxTokens) {
+            // the down launch reduces its tables' inputs h from the gate/up
+            // partials itself (no separate SwiGLU launch)
+            dn.sw_g = gpart;
+            dn.sw_u = upart;
+            dn.sw_nslot = P.nslot_gu;
+        } else {
+            RVQ_TRY(launch_swiglu_reduce(gpart, upart, np, P.nslot_gu, bank->f, h, st, pdl));
+        }
         RVQ_TRY(mark(2));
-        dn.early_start = 1;  // the plan is three launches back (or more); only h is new
+        dn.early_start = 1;  // the plan is two or more launches back; only the inputs are new
         RVQ_TRY(launch_lut_gemv_il(dn, pd, st, pdl));
         return mark(3);
     }

@@ -171,8 +171,9 @@ struct LutJob {
     // record header check
     int32_t check_header;
     int32_t layer, d, f;
-    // interleaved GEMV: 1 when only the inputs x come from the immediately
-    // preceding kernel (the pair plan was written two or more launches back),
+    // interleaved GEMV: 1 when only the inputs (x, or the gate/up partials of
+    // a fused SwiGLU) come from the immediately preceding kernel (the pair
+    // plan was written two or more launches back),
     // so the first table's codebook and code tiles are requested before the
     // dependency wait
     int32_t early_start;
@@ -180,7 +181,20 @@ struct LutJob {
     // -1 when not resident; NULL: record e
     const int32_t *slot_of;
     int32_t n_records;
+    // interleaved down GEMV with the SwiGLU reduction fused (sw_g != NULL):
+    // a table's inputs h = silu(sum of sw_g) * sum of sw_u over the gate/up
+    // launch's sw_nslot split-K slots ([entry][slot][f] each) are computed by
+    // the block instead of read from x
+    const float *sw_g, *sw_u;
+    int32_t sw_nslot;
 };
+// split-K slots (d / 256) up to which the down GEMV can fuse the reduction
+constexpr int kIlSwigluMaxSlots = 32;
+// tokens up to which it does: the fused reduction costs every table of the
+// down launch a round trip to L2, which outweighs the separate launch it
+// saves from 8 tokens on (K3-shaped layer: batch 1 -5 %, batch 8 +1 %,
+// batch 16 +2 % per step)
+constexpr int kIlSwigluMaxTokens = 4;
 
 __host__ __device__ inline int lut_items(const LutJob &j) { return (j.G / (2 * j.C)) * j.n_pairs * j.S; }
 

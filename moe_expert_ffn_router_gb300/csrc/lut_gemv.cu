@@ -33,7 +33,8 @@
 //  * Items of the same (expert, chunk group) for different token pairs are
 //    adjacent in the item order, so a second token pair re-reads codes from L2.
 //  * Split-K partials (one slot per item column range) are reduced by the
-//    next kernel (SwiGLU for gate/up, the combine for down).
+//    next kernel (SwiGLU for gate/up, the combine for down); the decode
+//    kernel's down launch reduces the gate/up partials itself.
 #include "internal.cuh"
 #include "lut_common.cuh"
 
@@ -539,7 +540,11 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_kernel(const LutJob job) {
 // 32-row tile per warp.  A table serves all units of one (matrix, pair,
 // group) in the block's contiguous unit range.  The next table's inputs (its
 // 256 input values and, when the expert or matrix changes, its codebook) are
-// fetched by one bulk copy onto an mbarrier while the warps stream.
+// fetched by one bulk copy onto an mbarrier while the warps stream.  In the
+// down launch the 256 values are h = silu(g) u of the gate/up launch: every
+// warp reduces a share of them from the split-K partials at the start of the
+// phase (il_swiglu_x) and arrives on the same mbarrier, so no separate SwiGLU
+// launch (and its two kernel boundaries) sits between the two GEMVs.
 constexpr int IL_ROWS = 512;                   // rows per unit = 16 warps x 32
 constexpr int IL_XS = 32 * 8 * 4;              // one table's inputs, fp32 or bf16
 constexpr int kIlSmemBytes = kLutBytes + kCbBytes + IL_XS + 64;
@@ -745,7 +750,9 @@ __device__ __forceinline__ void il_build(uint8_t *lut, int h, const uint8_t *cb_
 __device__ __forceinline__ void il_fetch_cb(const LutJob &job, const IlTab &t, bool same_cb,
                                             uint8_t *cb_s, uint32_t bar) {
     const int esz = job.x_dtype == RVQ_BF16 ? 2 : 4;
-    const uint32_t bytes = 256u * esz + (same_cb ? 0u : (uint32_t)kCbBytes);
+    // (with the SwiGLU reduction fused, the inputs are written by the block)
+    const uint32_t bytes =
+        (job.sw_g ? 0u : 256u * esz) + (same_cb ? 0u : (uint32_t)kCbBytes);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
     if (!same_cb) {
@@ -771,7 +778,58 @@ __device__ __forceinline__ void il_fetch_x(const LutJob &job, const IlTab &t, ui
 __device__ __forceinline__ void il_fetch(const LutJob &job, const IlTab &t, bool same_cb,
                                          uint8_t *cb_s, uint8_t *xs_s, uint32_t bar) {
     il_fetch_cb(job, t, same_cb, cb_s, bar);
-    il_fetch_x(job, t, xs_s, bar);
+    if (!job.sw_g) il_fetch_x(job, t, xs_s, bar);
+}
+
+// Down launch with the SwiGLU reduction fused: table t's 256 inputs
+// h[r] = silu(g[r]) u[r] for rows r = 256 g .. 256 g + 255 of pair entry
+// t.d.y, g and u summed over the gate/up launch's split-K slots (at most 32):
+// eight adjacent lanes per four rows, lane j taking slots j, j + 8, ... (all
+// its loads in flight at once), then three xor-shuffles, a fixed order.
+// Called by all 512 threads; each warp then arrives on `bar`.
+__device__ __forceinline__ void il_swiglu_x(const LutJob &job, const IlTab &t, uint8_t *xs_s,
+                                            int tid, uint32_t bar) {
+    const int j = tid & 7, i4 = tid >> 3;  // slot residue, float4 of rows
+    const int f4 = job.cols / 4, nslot = job.sw_nslot;
+    const int64_t off = (int64_t)t.d.y * nslot * f4 + t.g * 64 + i4;
+    const float4 *gp = reinterpret_cast<const float4 *>(job.sw_g) + off;
+    const float4 *up = reinterpret_cast<const float4 *>(job.sw_u) + off;
+    static_assert(kIlSwigluMaxSlots <= 4 * 8, "four slots per lane of eight");
+    float4 a[4], b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int s = j + 8 * q;
+        a[q] = s < nslot ? __ldg(gp + (int64_t)s * f4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        b[q] = s < nslot ? __ldg(up + (int64_t)s * f4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 g = a[0], u = b[0];
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+        g.x += a[q].x; g.y += a[q].y; g.z += a[q].z; g.w += a[q].w;
+        u.x += b[q].x; u.y += b[q].y; u.z += b[q].z; u.w += b[q].w;
+    }
+#pragma unroll
+    for (int o = 1; o <= 4; o <<= 1) {
+        g.x += __shfl_xor_sync(0xffffffffu, g.x, o);
+        g.y += __shfl_xor_sync(0xffffffffu, g.y, o);
+        g.z += __shfl_xor_sync(0xffffffffu, g.z, o);
+        g.w += __shfl_xor_sync(0xffffffffu, g.w, o);
+        u.x += __shfl_xor_sync(0xffffffffu, u.x, o);
+        u.y += __shfl_xor_sync(0xffffffffu, u.y, o);
+        u.z += __shfl_xor_sync(0xffffffffu, u.z, o);
+        u.w += __shfl_xor_sync(0xffffffffu, u.w, o);
+    }
+    if (j == 0) {
+        float4 o;
+        o.x = g.x / (1.0f + expf(-g.x)) * u.x;
+        o.y = g.y / (1.0f + expf(-g.y)) * u.y;
+        o.z = g.z / (1.0f + expf(-g.z)) * u.z;
+        o.w = g.w / (1.0f + expf(-g.w)) * u.w;
+        reinterpret_cast<float4 *>(xs_s)[i4] = o;
+    }
+    __syncwarp();
+    if ((tid & 31) == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, const int4 *pd) {
@@ -787,15 +845,19 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, co
     const int w1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
     const int RB = job.rows / 32;
     const int nslot = job.G;
+    // arrivals per table: the fetching thread, and with the SwiGLU reduction
+    // fused every warp (each computes a share of the inputs)
+    const bool fused = job.sw_g != nullptr;
     if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(inbar));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(inbar), "r"(fused ? 1u + NW : 1u));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     // The table walk reads the pair plan; with early_start it was written
-    // by a kernel that completed before the preceding one began, so the walk,
-    // the first code tiles and the first codebook need not wait for the
-    // preceding kernel (which writes only the inputs x).
+    // by an earlier kernel that the preceding one waited for before it let
+    // this launch start, so the walk, the first code tiles and the first
+    // codebook need not wait for the preceding kernel (which writes only this
+    // launch's inputs: x, or the gate/up partials of a fused SwiGLU).
     const bool early = job.early_start != 0;
     if (!early) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -861,7 +923,11 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, co
     }
     if (has_cur) {
         // the first table: its inputs, then built by all warps before streaming
-        if (threadIdx.x == 0) il_fetch_x(job, cur, xs_s, inbar);
+        if (fused) {
+            il_swiglu_x(job, cur, xs_s, threadIdx.x, inbar);
+        } else if (threadIdx.x == 0) {
+            il_fetch_x(job, cur, xs_s, inbar);
+        }
         cb_m = cur.m;
         cb_e = cur.d.x;
         alive = il_wait(inbar, inph, job.status);
@@ -889,6 +955,8 @@ __global__ void __launch_bounds__(NT, 1) lut_gemv_il_kernel(const LutJob job, co
         if (has_nxt) {
             cb_m = nxt.m;
             cb_e = nxt.d.x;
+            // the previous table's build is done with the inputs' buffer
+            if (fused) il_swiglu_x(job, nxt, xs_s, threadIdx.x, inbar);
         }
 #pragma unroll
         for (int p2 = 0; p2 < 16; ++p2) {
