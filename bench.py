@@ -82,6 +82,8 @@ ENCODE_METRIC = "offline RVQ encoder: weights encoded per second (3 stages x 256
 KERNELS = ["router_logits", "route", "lut_plan", "lut_gemv_gate_up", "swiglu_reduce",
            "lut_gemv_down", "combine"]
 DOMINANT = "lut_gemv_gate_up"
+L2_BYTES = 129 * 10**6   # GB300 L2
+BANK_COPIES = 4          # rotated bank copies for a single layer whose bank is under 2 x L2
 # event intervals of the layer call when every expert takes the tensor-core path
 KERNELS_TC = ["router_logits", "route", "lut_experts", "prefill_gate_up", "prefill_down",
               "unused", "combine"]
@@ -293,10 +295,19 @@ def run_gpu(args, rank, world, local_rank):
     kernels = KERNELS_TC if tc_min > 0 else KERNELS
     n_layers = W.WORKLOADS[config].n_layers
     encoded = encoded_bank(args.workload)
-    built = [build_layer(config, dev, shape=s, layer=i, encoded=encoded) for i in range(n_layers)]
+    weights_per_expert = 3 * s.d * s.f
+    code_bytes_per_expert = 3 * (3 * s.d * s.f // 8)
+    # a single layer whose bank is under twice the L2 is timed on BANK_COPIES
+    # seeded copies (other seeds, the same shapes), step i on copy i mod
+    # BANK_COPIES, so that a step does not find the previous steps' experts in L2
+    rot = BANK_COPIES if n_layers == 1 and code_bytes_per_expert * s.E < 2 * L2_BYTES else 1
+    built = [build_layer(config, dev, shape=s, layer=i, encoded=encoded)
+             for i in range(max(n_layers, rot))]
     L, src = built[0]
     from moe_expert_ffn_router_gb300.layer import MoeStack
-    stack = MoeStack([b[0] for b in built])
+    stack = MoeStack([b[0] for b in built[:n_layers]])
+    copies = [b[0] for b in built] if n_layers == 1 else [L]
+    copy_bufs = [stack.buffers(batch)[0]] + [Lc.buffers(batch) for Lc in copies[1:]]
     if prefill:
         pool_bits = src.tokens_bf16(2 * batch)          # two chunks, alternating
     else:
@@ -305,20 +316,18 @@ def run_gpu(args, rank, world, local_rank):
     xs = torch.from_numpy(pool_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     xs = xs.reshape(-1, batch, s.d)
     nsteps = xs.shape[0]
-    bufs = stack.buffers(batch)[0]
-    weights_per_expert = 3 * s.d * s.f
-    code_bytes_per_expert = 3 * (3 * s.d * s.f // 8)
+    assert nsteps % rot == 0, "each token-pool entry keeps one bank copy"
     cb_bytes_per_expert = 3 * rvq.RVQ_CODEBOOK_BYTES
 
-    def forward(x, events=None):
+    def forward(x, events=None, r=0):
         # one layer: the layer itself (router -> top-k -> FFN -> combine +
-        # residual); a stack: pre-norm + layer, per layer
+        # residual), on bank copy r; a stack: pre-norm + layer, per layer
         if n_layers == 1:
-            return [L.forward(x, bufs, events=events, tc_min_tokens=tc_min)]
+            return [copies[r].forward(x, copy_bufs[r], events=events, tc_min_tokens=tc_min)]
         return stack.forward(x, events=events, tc_min_tokens=tc_min)
 
     def step(i, events=None):
-        return forward(xs[i % nsteps], events=events)
+        return forward(xs[i % nsteps], events=events, r=i % rot)
 
     # unique experts per step, summed over the layers (from the routing the
     # GPU computed); the pool is replayed identically in the timed loop, so
@@ -330,7 +339,7 @@ def run_gpu(args, rank, world, local_rank):
         per = [len(set(b["idx"].cpu().numpy().reshape(-1).tolist())) for b in bl]
         uniq.append(sum(per))
         uniq0.append(per[0])
-    for Lx in stack.layers:
+    for Lx in stack.layers + copies[1:]:
         rc, bits = Lx.status(batch)
         if rc != 0:
             raise RuntimeError(f"device status {rc} bits {bits:#x}")
@@ -361,8 +370,8 @@ def run_gpu(args, rank, world, local_rank):
     # timed value unless --graph: a graph boundary ends that overlap (the next
     # step's router cannot start behind the previous step's combine), and the
     # replays measured slower (0.103 against 0.093 ms per K3 decode step).
-    graphs = ([L.graph(xs[j], bufs, tc_min_tokens=tc_min) for j in range(nsteps)]
-              if n_layers == 1 else [])
+    graphs = ([copies[j % rot].graph(xs[j], copy_bufs[j % rot], tc_min_tokens=tc_min)
+               for j in range(nsteps)] if n_layers == 1 else [])
     use_graph = bool(graphs) and args.graph
     ms_other = timed(step if use_graph else (lambda i: graphs[i % nsteps].launch())) \
         if graphs else None
@@ -451,14 +460,16 @@ def run_gpu(args, rank, world, local_rank):
 
     def e2e_step(i):
         xbuf.view(torch.int16).copy_(pinned_in[i % nsteps], non_blocking=True)
-        forward(xbuf)
-        pinned_out.copy_(out_last, non_blocking=True)
+        forward(xbuf, r=i % rot)
+        pinned_out.copy_(copy_bufs[i % rot]["out"] if n_layers == 1 else out_last,
+                         non_blocking=True)
 
     if use_graph:
         # the copies in and out recorded in each step's graph
         pin_bf16 = pinned_in.view(torch.bfloat16)
-        graphs = [L.graph(xbuf, bufs, x_host=pin_bf16[j], out_host=pinned_out,
-                          tc_min_tokens=tc_min) for j in range(nsteps)]
+        graphs = [copies[j % rot].graph(xbuf, copy_bufs[j % rot], x_host=pin_bf16[j],
+                                        out_host=pinned_out, tc_min_tokens=tc_min)
+                  for j in range(nsteps)]
         ms_e2e = timed(lambda i: graphs[i % nsteps].launch())
         for g in graphs:
             g.close()
@@ -467,7 +478,7 @@ def run_gpu(args, rank, world, local_rank):
     e2e = {"value": round(job_rate(experts_total * weights_per_expert, world, ms_e2e) / 1e9, 2),
            "unit": UNIT,
            "h2d_bytes_per_step": batch * s.d * 2, "d2h_bytes_per_step": batch * s.d * 4}
-    for Lx in stack.layers:
+    for Lx in stack.layers + copies[1:]:
         rc, bits = Lx.status(batch)
         if rc != 0:
             raise RuntimeError(f"device status {rc} bits {bits:#x}")
@@ -489,8 +500,9 @@ def run_gpu(args, rank, world, local_rank):
                          # launch, the SwiGLU reduction inside the down GEMV
                          - (1 if fused else 0) - (1 if fused_swiglu else 0))
                         * args.steps * n_layers,
-               config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers)
-    del L, stack, built
+               config=config, batch=batch, shape=s, prefill=prefill, layers=n_layers,
+               bank_copies=rot)
+    del L, stack, built, copies, copy_bufs
     return res
 
 
@@ -1072,9 +1084,16 @@ def main():
                        "batch": r["batch"], "layers": r["layers"],
                        "d": s.d, "f": s.f, "experts": s.E, "top_k": s.k,
                        "codes_bytes": 3 * (3 * s.d * s.f // 8) * s.E * r["layers"],
-                       "l2": f"inputs larger than L2: "
-                             f"{3 * (3 * s.d * s.f // 8) * s.E * r['layers'] / 1e9:.2f} "
-                             "GB code bank (L2 129 MB); token pool rotates routing every step",
+                       "l2": (f"inputs larger than L2: "
+                              f"{3 * (3 * s.d * s.f // 8) * s.E * r['layers'] / 1e9:.2f} "
+                              "GB code bank (L2 129 MB); token pool rotates routing every step")
+                             if r["bank_copies"] == 1 else
+                             (f"{r['bank_copies']} seeded copies of the "
+                              f"{3 * (3 * s.d * s.f // 8) * s.E / 1e6:.0f} MB code bank "
+                              f"({r['bank_copies'] * 3 * (3 * s.d * s.f // 8) * s.E / 1e9:.2f} "
+                              "GB, L2 129 MB), step i on copy i mod "
+                              f"{r['bank_copies']}; token pool rotates routing every step"),
+                       "bank_copies": r["bank_copies"],
                        "parallelism": f"replicas{world}",
                        "path": ("tensor cores for every expert group (fp16 operands: "
                                 "bf16 tokens and fp16 codeword sums, fp32 accumulate)")
