@@ -458,15 +458,22 @@ def run_gpu(args, rank, world, local_rank):
     xbuf = torch.empty((batch, s.d), dtype=torch.bfloat16, device=dev)
     out_last = stack.buffers(batch)[-1]["out"]
 
+    pin_bf16 = pinned_in.view(torch.bfloat16)
+
     def e2e_step(i):
+        if n_layers == 1:
+            # the library's host-buffer layer call (moe_layer_forward_host)
+            r = i % rot
+            copies[r].forward_host(pin_bf16[i % nsteps], pinned_out, copy_bufs[r],
+                                   tc_min_tokens=tc_min)
+            return
+        # a stack: its input copied in and its output copied back around it
         xbuf.view(torch.int16).copy_(pinned_in[i % nsteps], non_blocking=True)
-        forward(xbuf, r=i % rot)
-        pinned_out.copy_(copy_bufs[i % rot]["out"] if n_layers == 1 else out_last,
-                         non_blocking=True)
+        forward(xbuf)
+        pinned_out.copy_(out_last, non_blocking=True)
 
     if use_graph:
         # the copies in and out recorded in each step's graph
-        pin_bf16 = pinned_in.view(torch.bfloat16)
         graphs = [copies[j % rot].graph(xbuf, copy_bufs[j % rot], x_host=pin_bf16[j],
                                         out_host=pinned_out, tc_min_tokens=tc_min)
                   for j in range(nsteps)]

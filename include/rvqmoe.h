@@ -433,15 +433,21 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
                                 void **events, rvq_stream_t stream);
 
 /* One whole MoE layer with its input and output in host memory, for callers
- * whose tokens arrive from and leave to the host: one cudaMemcpyAsync of
- * x_host (n x d of xdt) into x_dev, the layer of moe_layer_forward_ex (x is
- * also the residual; no event marks), and one cudaMemcpyAsync of out (fp32
- * n x d) from out_dev back to out_host, all on `stream` and asynchronous:
- * synchronise the stream before reading out_host.  Pinned host buffers let
- * the copies run asynchronously; pageable ones work, with the driver's
- * staging.  x_dev (dev, >= n x d x sizeof(xdt) bytes, 16-byte aligned) and
- * the other device buffers are the caller's, as in moe_layer_forward_ex.
- * Every argument is checked before the first copy (EINVAL / EALIGN / ENOMEM,
+ * whose tokens arrive from and leave to the host.  The call queues, all on
+ * `stream` and asynchronous (synchronise the stream before reading out_host):
+ *  - a copy of x_host (n x d of xdt) into x_dev;
+ *  - the layer of moe_layer_forward_ex (x is also the residual; no event
+ *    marks);
+ *  - a copy of out (fp32 n x d) from out_dev back to out_host.
+ * A host buffer that the device maps (pinned memory, which is mapped on
+ * systems with unified addressing) at a 16-byte aligned address is read or
+ * written by a copy kernel of the call itself.  That kernel waits for the
+ * preceding kernel on the stream like the layer's own kernels, so the step
+ * stays one chain of dependent launches.  Any other host buffer is copied
+ * by cudaMemcpyAsync: pageable memory works, with the driver's staging.
+ * x_dev (dev, >= n x d x sizeof(xdt) bytes, 16-byte aligned) and the other
+ * device buffers are the caller's, as in moe_layer_forward_ex.  Every
+ * argument is checked before the first copy (EINVAL / EALIGN / ENOMEM,
  * nothing queued). */
 rvq_status moe_layer_forward_host(const rvq_moe_bank *bank, const float *wr_dev,
                                   const float *bias_dev, const void *x_host, rvq_dtype xdt,

@@ -870,6 +870,20 @@ static rvq_status check_layer_io(const rvq_moe_bank *bank, const float *wr_dev, 
 
 // x_host -> x_dev, the layer, out_dev -> out_host (the copies only when the
 // host pointers are given), all queued on st.
+// The address at which kernels of this device reach host buffer p, when p is
+// pinned memory the device maps (16-byte aligned); NULL otherwise (pageable
+// memory, or a mapping the device cannot use).
+static void *mapped_host(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // an unknown pointer is not an error here
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer || ((uintptr_t)a.devicePointer & 15u))
+        return nullptr;
+    return a.devicePointer;
+}
+
 static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
                                  const float *bias_dev, const void *x_host, rvq_dtype xdt,
                                  int32_t n, int32_t k, void *x_dev, float *logits_dev,
@@ -878,11 +892,23 @@ static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
                                  size_t ws_bytes, int32_t tc_min_tokens, cudaStream_t st) {
     const size_t esz = xdt == RVQ_BF16 ? 2 : 4;
     const size_t xbytes = (size_t)n * bank->d * esz, obytes = (size_t)n * bank->d * 4;
-    if (x_host) RVQ_CUDA(cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, st));
+    // a host buffer the GPU maps (pinned) is read or written by a copy kernel
+    // inside the call's launch chain; any other one by cudaMemcpyAsync
+    if (x_host) {
+        if (void *xm = mapped_host(x_host))
+            RVQ_TRY(launch_io_copy(xm, x_dev, xbytes, st, true));
+        else
+            RVQ_CUDA(cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, st));
+    }
     RVQ_TRY(moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
                                  topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
                                  nullptr, xdt, tc_min_tokens, nullptr, (rvq_stream_t)st));
-    if (out_host) RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
+    if (out_host) {
+        if (void *om = mapped_host(out_host))
+            RVQ_TRY(launch_io_copy(out_dev, om, obytes, st, true));
+        else
+            RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
+    }
     return RVQ_OK;
 }
 

@@ -56,6 +56,19 @@ __global__ void combine_kernel(const float *__restrict__ ypart, int nslot,
     *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
 }
 
+// A layer call's input or output moved between a host buffer the GPU maps
+// (pinned) and device memory by the GPU itself, 16 bytes per thread and
+// step: as a kernel of the call's launch chain, programmatic dependent launch
+// carries through it (a cudaMemcpyAsync node would end the overlap).
+__global__ void __launch_bounds__(256) io_copy_kernel(const uint4 *__restrict__ src,
+                                                      uint4 *__restrict__ dst, int64_t n16) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
 // nslot == 1 (outputs already reduced, e.g. by the tensor-core path): one
 // thread per (token, column quad) with all k slot loads in flight at once.
 __global__ void __launch_bounds__(256) combine1_kernel(const float *__restrict__ y,
@@ -194,6 +207,30 @@ rvq_status launch_rms_norm(const void *x, int xdt, int n, int d, float eps, void
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     RVQ_CUDA(cudaLaunchKernelEx(&cfg, rms_norm_kernel, x, xdt, d, eps, out, odt));
+    return RVQ_OK;
+}
+
+rvq_status launch_io_copy(const void *src, void *dst, size_t bytes, cudaStream_t stream,
+                          bool pdl) {
+    if (bytes == 0) return RVQ_OK;
+    if ((bytes & 15u) != 0 || ((uintptr_t)src & 15u) != 0 || ((uintptr_t)dst & 15u) != 0) {
+        set_error("io copy: %zu bytes between %p and %p are not 16-byte aligned", bytes, src, dst);
+        return RVQ_EALIGN;
+    }
+    const int64_t n16 = (int64_t)(bytes / 16);
+    const int64_t want = (n16 + 255) / 256;
+    const int blocks = (int)(want < 4 * num_sms() ? want : 4 * num_sms());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, io_copy_kernel, reinterpret_cast<const uint4 *>(src),
+                                reinterpret_cast<uint4 *>(dst), n16));
     return RVQ_OK;
 }
 

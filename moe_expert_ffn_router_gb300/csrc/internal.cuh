@@ -217,6 +217,10 @@ rvq_status launch_rms_norm(const void *x, int xdt, int n, int d, float eps, void
                            cudaStream_t stream, bool pdl);
 rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
                           const void *res, int rdt, float *out, cudaStream_t stream, bool pdl);
+// bytes (a multiple of 16, both ends 16-byte aligned) copied by a kernel,
+// for a host buffer the GPU maps; waits for the preceding kernel of the stream
+rvq_status launch_io_copy(const void *src, void *dst, size_t bytes, cudaStream_t stream,
+                          bool pdl);
 rvq_status launch_router_logits(const float *wr, const float *bias, const void *x, int xdt,
                                 int n, int E, int d, float *logits, cudaStream_t stream);
 // One token: xn = bf16(h / rms(h)) (written by block 0) and its logits, in one

@@ -179,21 +179,30 @@ def test_k3_shaped_layer_full_size(n, sample):
     sl.forget()
 
 
-def test_host_buffer_layer_call_equals_device_call():
-    """moe_layer_forward_host (input copied from pinned host memory, output
-    copied back) gives bit for bit the device-buffer layer's outputs."""
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_layer_call_equals_device_call(pinned):
+    """moe_layer_forward_host gives bit for bit the device-buffer layer's
+    outputs, over several steps on the same buffers.  Pinned buffers (mapped:
+    moved by the call's copy kernels) and pageable ones (cudaMemcpyAsync)."""
     sl, L = layer(1)
     n = 3
-    bits = sl.tokens_bf16(n)
-    x_host = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
-    out_host = torch.full((n, L.d), float("nan"), dtype=torch.float32).pin_memory()
-    hb = L.forward_host(x_host, out_host)
-    torch.cuda.synchronize()
-    assert L.status(n) == (0, 0)
-    ref = L.forward(bf16_dev(bits))
-    torch.cuda.synchronize()
-    assert torch.equal(out_host, ref["out"].cpu())
-    assert torch.equal(hb["x_dev"].cpu().view(torch.int16), x_host.view(torch.int16))
+    pool = sl.tokens_bf16(3 * n)
+    x_host = torch.empty((n, L.d), dtype=torch.bfloat16)
+    out_host = torch.full((n, L.d), float("nan"), dtype=torch.float32)
+    if pinned:
+        x_host, out_host = x_host.pin_memory(), out_host.pin_memory()
+    b = L.buffers(n)
+    for step in range(3):
+        bits = pool[step * n:(step + 1) * n]
+        x_host.view(torch.int16).copy_(torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)))
+        hb = L.forward_host(x_host, out_host, b)
+        torch.cuda.synchronize()
+        assert L.status(n) == (0, 0)
+        got = out_host.clone()
+        ref = L.forward(bf16_dev(bits))
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref["out"].cpu()), step
+        assert torch.equal(hb["x_dev"].cpu().view(torch.int16), x_host.view(torch.int16)), step
 
 
 def test_layer_graph_replays_the_direct_call():
