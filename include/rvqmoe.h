@@ -439,12 +439,13 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
  *  - the layer of moe_layer_forward_ex (x is also the residual; no event
  *    marks);
  *  - a copy of out (fp32 n x d) from out_dev back to out_host.
- * A host buffer that the device maps (pinned memory, which is mapped on
- * systems with unified addressing) at a 16-byte aligned address is read or
- * written by a copy kernel of the call itself.  That kernel waits for the
- * preceding kernel on the stream like the layer's own kernels, so the step
- * stays one chain of dependent launches.  Any other host buffer is copied
- * by cudaMemcpyAsync: pageable memory works, with the driver's staging.
+ * A transfer of up to 1 MiB whose host buffer the device maps (pinned memory,
+ * which is mapped on systems with unified addressing) at a 16-byte aligned
+ * address is made by a copy kernel of the call itself.  That kernel waits for
+ * the preceding kernel on the stream like the layer's own kernels, so the
+ * step stays one chain of dependent launches.  Larger transfers, and any
+ * other host buffer, go through cudaMemcpyAsync: pageable memory works, with
+ * the driver's staging.
  * x_dev (dev, >= n x d x sizeof(xdt) bytes, 16-byte aligned) and the other
  * device buffers are the caller's, as in moe_layer_forward_ex.  Every
  * argument is checked before the first copy (EINVAL / EALIGN / ENOMEM,

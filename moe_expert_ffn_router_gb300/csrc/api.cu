@@ -873,6 +873,9 @@ static rvq_status check_layer_io(const rvq_moe_bank *bank, const float *wr_dev, 
 // The address at which kernels of this device reach host buffer p, when p is
 // pinned memory the device maps (16-byte aligned); NULL otherwise (pageable
 // memory, or a mapping the device cannot use).
+// Largest host transfer a copy kernel makes; larger ones go to the copy engines.
+constexpr size_t kIoKernelMaxBytes = size_t(1) << 20;
+
 static void *mapped_host(const void *p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -895,7 +898,7 @@ static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
     // a host buffer the GPU maps (pinned) is read or written by a copy kernel
     // inside the call's launch chain; any other one by cudaMemcpyAsync
     if (x_host) {
-        if (void *xm = mapped_host(x_host))
+        if (void *xm = xbytes <= kIoKernelMaxBytes ? mapped_host(x_host) : nullptr)
             RVQ_TRY(launch_io_copy(xm, x_dev, xbytes, st, true));
         else
             RVQ_CUDA(cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, st));
@@ -904,7 +907,7 @@ static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
                                  topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
                                  nullptr, xdt, tc_min_tokens, nullptr, (rvq_stream_t)st));
     if (out_host) {
-        if (void *om = mapped_host(out_host))
+        if (void *om = obytes <= kIoKernelMaxBytes ? mapped_host(out_host) : nullptr)
             RVQ_TRY(launch_io_copy(out_dev, om, obytes, st, true));
         else
             RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
