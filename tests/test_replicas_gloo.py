@@ -44,3 +44,11 @@ def test_job_rate_counts_every_rank():
     # 100 units per rank, 2 ranks, slowest rank 15 ms
     assert bench.job_rate(100, 2, 15.0) == pytest.approx(100 * 2 / 0.015)
     assert bench.replica_max_ms(12.5, 1, "cpu") == 12.5
+
+
+def test_committed_traffic_record_matches_the_kernel_sources():
+    """roofline.traffic comes from a committed ncu capture keyed to a hash of
+    the sources the decode GEMV is built from; a source changed since the
+    capture makes bench.py report null.  The committed record must match."""
+    import bench
+    assert bench.load_traffic(bench.DOMINANT) is not None
