@@ -179,18 +179,25 @@ def test_k3_shaped_layer_full_size(n, sample):
     sl.forget()
 
 
-@pytest.mark.parametrize("pinned", [True, False])
-def test_host_buffer_layer_call_equals_device_call(pinned):
+@pytest.mark.parametrize("kind", ["pinned", "pageable", "pinned_unaligned"])
+def test_host_buffer_layer_call_equals_device_call(kind):
     """moe_layer_forward_host gives bit for bit the device-buffer layer's
     outputs, over several steps on the same buffers.  Pinned buffers (mapped:
-    moved by the call's copy kernels) and pageable ones (cudaMemcpyAsync)."""
+    moved by the call's copy kernels), pageable ones and pinned ones off a
+    16-byte boundary (both by cudaMemcpyAsync)."""
     sl, L = layer(1)
     n = 3
     pool = sl.tokens_bf16(3 * n)
     x_host = torch.empty((n, L.d), dtype=torch.bfloat16)
     out_host = torch.full((n, L.d), float("nan"), dtype=torch.float32)
-    if pinned:
+    if kind == "pinned":
         x_host, out_host = x_host.pin_memory(), out_host.pin_memory()
+    elif kind == "pinned_unaligned":
+        # views one element into larger pinned buffers: 2 and 4 bytes off
+        x_host = torch.empty(n * L.d + 1, dtype=torch.bfloat16).pin_memory()[1:].view(n, L.d)
+        out_host = torch.full((n * L.d + 1,), float("nan"),
+                              dtype=torch.float32).pin_memory()[1:].view(n, L.d)
+        assert x_host.data_ptr() % 16 and out_host.data_ptr() % 16
     b = L.buffers(n)
     for step in range(3):
         bits = pool[step * n:(step + 1) * n]
