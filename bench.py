@@ -48,6 +48,7 @@ WORKLOADS = {
     "k3_decode_b16": (2, 16),
     "k3_decode_b32": (2, 32),
     "k3_decode_b64": (2, 64),
+    "k3_decode_b64_e64": (2, 64, 64),  # profiling case: the two-token GEMV on a 1.06 GB bank
     "decode_d2048_b1": (1, 1),
     "decode_d2048_b4": (1, 4),
     "decode_d2048_b16": (1, 16),
