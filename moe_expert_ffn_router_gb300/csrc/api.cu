@@ -868,14 +868,9 @@ static rvq_status check_layer_io(const rvq_moe_bank *bank, const float *wr_dev, 
     return RVQ_OK;
 }
 
-// x_host -> x_dev, the layer, out_dev -> out_host (the copies only when the
-// host pointers are given), all queued on st.
 // The address at which kernels of this device reach host buffer p, when p is
 // pinned memory the device maps (16-byte aligned); NULL otherwise (pageable
 // memory, or a mapping the device cannot use).
-// Largest host transfer a copy kernel makes; larger ones go to the copy engines.
-constexpr size_t kIoKernelMaxBytes = size_t(1) << 20;
-
 static void *mapped_host(const void *p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -887,6 +882,12 @@ static void *mapped_host(const void *p) {
     return a.devicePointer;
 }
 
+// Largest host transfer a copy kernel makes; larger ones go to the copy engines
+// (measured alike for a prefill chunk's tens of MB).
+constexpr size_t kIoKernelMaxBytes = size_t(1) << 20;
+
+// x_host -> x_dev, the layer, out_dev -> out_host (the copies only when the
+// host pointers are given), all queued on st.
 static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
                                  const float *bias_dev, const void *x_host, rvq_dtype xdt,
                                  int32_t n, int32_t k, void *x_dev, float *logits_dev,
@@ -895,8 +896,9 @@ static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
                                  size_t ws_bytes, int32_t tc_min_tokens, cudaStream_t st) {
     const size_t esz = xdt == RVQ_BF16 ? 2 : 4;
     const size_t xbytes = (size_t)n * bank->d * esz, obytes = (size_t)n * bank->d * 4;
-    // a host buffer the GPU maps (pinned) is read or written by a copy kernel
-    // inside the call's launch chain; any other one by cudaMemcpyAsync
+    // up to kIoKernelMaxBytes, a host buffer the GPU maps (pinned) is read or
+    // written by a copy kernel inside the call's launch chain; otherwise the
+    // copy is a cudaMemcpyAsync
     if (x_host) {
         if (void *xm = xbytes <= kIoKernelMaxBytes ? mapped_host(x_host) : nullptr)
             RVQ_TRY(launch_io_copy(xm, x_dev, xbytes, st, true));
