@@ -370,7 +370,7 @@ def run_gpu(args, rank, world, local_rank):
     # dependent launch between them and from one step into the next, are the
     # timed value unless --graph: a graph boundary ends that overlap (the next
     # step's router cannot start behind the previous step's combine), and the
-    # replays measured slower (0.103 against 0.093 ms per K3 decode step).
+    # replays measured slower (0.092-0.099 against 0.089 ms per K3 decode step).
     graphs = ([copies[j % rot].graph(xs[j], copy_bufs[j % rot], tc_min_tokens=tc_min)
                for j in range(nsteps)] if n_layers == 1 else [])
     use_graph = bool(graphs) and args.graph
