@@ -374,6 +374,14 @@ rvq_status moe_expert_ffn(const rvq_moe_bank *bank, const void *x_dev, rvq_dtype
                           const int32_t *pairs_dev, float *y_pair_dev, void *ws_dev,
                           size_t ws_bytes, rvq_stream_t stream);
 
+/* A starting point for tc_min_tokens, measured on GB300 with K3-shaped
+ * experts (d = 7168, f = 2048): at 64 tokens per step a threshold of 6 was
+ * the fastest tried (4 and 8 within 4 %), while at 32 tokens the lookup
+ * tables alone were fastest; a 2048-token prefill chunk is fastest with every
+ * expert on the tensor cores (1).  The crossover depends on the shapes and
+ * on the group sizes of the step. */
+#define RVQMOE_PREFILL_MIN_TOKENS 6
+
 /* As moe_expert_ffn, with per-expert dispatch to the tensor-core path.
  * Experts whose group holds at least tc_min_tokens tokens are computed by
  * the prefill path: their codes are decoded tile by tile to fp16 on chip

@@ -23,6 +23,7 @@ RVQ_CODEBOOK_BYTES = 24576
 RVQ_BANK_MAGIC = 0x31515652
 RVQ_HDR_FLAG_CRC32 = 0x1
 MOE_LAYER_EVENTS = 8
+RVQMOE_PREFILL_MIN_TOKENS = 6
 DEV_ERR_INDEX, DEV_ERR_NONFINITE, DEV_ERR_CORRUPT, DEV_ERR_TIMEOUT = 1, 2, 4, 8
 STATUS = {0: "RVQ_OK", 1: "RVQ_EINVAL", 2: "RVQ_EALIGN", 3: "RVQ_ENOMEM", 4: "RVQ_ECORRUPT",
           5: "RVQ_EDEVICE", 6: "RVQ_ETIMEOUT", 7: "RVQ_ECUDA", 8: "RVQ_ENOTIMPL"}

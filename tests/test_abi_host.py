@@ -23,6 +23,25 @@ def test_every_declared_function_is_exported():
         assert n in names
 
 
+def test_binding_constants_equal_the_header_defines():
+    """Every numeric #define of include/rvqmoe.h that the binding also
+    defines has the same value in both (the binding restates them)."""
+    import re
+    defines = {}
+    for m in re.finditer(r"^#define\s+(\w+)\s+(0x[0-9a-fA-F]+|\d+)u?\b",
+                         open(rvq.HEADER).read(), re.M):
+        defines[m.group(1)] = int(m.group(2), 0)
+    aliases = {"RVQ_DEV_ERR_INDEX": "DEV_ERR_INDEX", "RVQ_DEV_ERR_NONFINITE": "DEV_ERR_NONFINITE",
+               "RVQ_DEV_ERR_CORRUPT": "DEV_ERR_CORRUPT", "RVQ_DEV_ERR_TIMEOUT": "DEV_ERR_TIMEOUT"}
+    checked = 0
+    for name, value in defines.items():
+        py = getattr(rvq, aliases.get(name, name), None)
+        if py is not None:
+            assert py == value, (name, py, value)
+            checked += 1
+    assert checked >= 10, defines
+
+
 def test_status_strings_and_version():
     for code in range(9):
         assert rvq.status_string(code) and rvq.status_string(code) != "unknown status"
