@@ -117,6 +117,28 @@ def test_mixed_dispatch_by_group_size():
                 lambda e: TC_TOL if counts[e] >= thr else LUT_TOL)
 
 
+def test_mixed_dispatch_small_batch_fused_swiglu():
+    """Four tokens, two of them equal: their experts get groups of two
+    (tensor cores at threshold 2) and the rest one token each (lookup
+    tables).  Up to 4 tokens the lookup-table down launch reduces its own
+    SwiGLU inputs, here with the tensor-core pairs skipped; every pair is
+    compared with the oracle."""
+    sl, L, _ = layer(1)
+    base = sl.tokens_bf16(3)
+    bits = np.concatenate([base[:1], base[:1], base[1:]])
+    n = bits.shape[0]
+    assert n == 4
+    x = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    b = route(L, x, n)
+    counts = np.diff(b["offsets"].cpu().numpy())
+    thr = 2
+    assert (counts >= thr).any() and ((counts > 0) & (counts < thr)).any()
+    y = run_ffn(L, x, n, b, tc_min_tokens=thr)
+    idx = b["idx"].cpu().numpy()
+    check_pairs(sl, bf16_bits_to_f64(bits), idx, y, range(n * L.k),
+                lambda e: TC_TOL if counts[e] >= thr else LUT_TOL)
+
+
 def test_prefill_chunk_full_size_zipf():
     """2048 tokens of the K3-shaped layer with the Zipf-skewed router bias
     (tokens per expert ~50-600, several 192-token passes for the largest
