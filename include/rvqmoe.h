@@ -449,9 +449,10 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
  *  - a copy of out (fp32 n x d) from out_dev back to out_host.
  * A transfer of up to 1 MiB whose host buffer the device maps (pinned memory,
  * which is mapped on systems with unified addressing) at a 16-byte aligned
- * address is made by a copy kernel of the call itself.  That kernel waits for
- * the preceding kernel on the stream like the layer's own kernels, so the
- * step stays one chain of dependent launches.  Larger transfers, and any
+ * address is made by the call's own kernels: the input by a copy kernel that
+ * waits for the preceding kernel on the stream like the layer's kernels, the
+ * output by the combine, which writes it to out_host beside out_dev.  The
+ * step thus stays one chain of dependent launches.  Larger transfers, and any
  * other host buffer, go through cudaMemcpyAsync: pageable memory works, with
  * the driver's staging.
  * x_dev (dev, >= n x d x sizeof(xdt) bytes, 16-byte aligned) and the other

@@ -741,15 +741,17 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
                                      int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
                                      void *ws_dev, const void *residual_dev, rvq_dtype rdt,
                                      int32_t tc_min_tokens, void **events, cudaStream_t st,
-                                     const FfnPlan &P);
+                                     const FfnPlan &P, float *out2 = nullptr);
 
-rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
+// moe_layer_forward_ex, with out2 (optional) a second copy of the output that
+// the combine writes (a host buffer the GPU maps).
+static rvq_status layer_forward(const rvq_moe_bank *bank, const float *wr_dev,
                                 const float *bias_dev, const void *x_dev, rvq_dtype xdt, int32_t n,
                                 int32_t k, float *logits_dev, int32_t *topk_idx_dev,
                                 float *topk_w_dev, int32_t *offsets_dev, int32_t *pairs_dev,
                                 float *out_dev, void *ws_dev, size_t ws_bytes,
                                 const void *residual_dev, rvq_dtype rdt, int32_t tc_min_tokens,
-                                void **events, rvq_stream_t stream) {
+                                void **events, rvq_stream_t stream, float *out2) {
     RVQ_TRY(check_ffn_args(bank, x_dev, xdt, n, k, ws_dev, ws_bytes, "moe_layer_forward"));
     if (!residual_dev) {
         residual_dev = x_dev;
@@ -787,7 +789,19 @@ rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
     RVQ_TRY(mark(1));
     return layer_after_router(bank, x_dev, xdt, n, k, logits_dev, topk_idx_dev, topk_w_dev,
                               offsets_dev, pairs_dev, out_dev, ws_dev, residual_dev, rdt,
-                              tc_min_tokens, events, st, P);
+                              tc_min_tokens, events, st, P, out2);
+}
+
+rvq_status moe_layer_forward_ex(const rvq_moe_bank *bank, const float *wr_dev,
+                                const float *bias_dev, const void *x_dev, rvq_dtype xdt, int32_t n,
+                                int32_t k, float *logits_dev, int32_t *topk_idx_dev,
+                                float *topk_w_dev, int32_t *offsets_dev, int32_t *pairs_dev,
+                                float *out_dev, void *ws_dev, size_t ws_bytes,
+                                const void *residual_dev, rvq_dtype rdt, int32_t tc_min_tokens,
+                                void **events, rvq_stream_t stream) {
+    return layer_forward(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
+                         topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
+                         residual_dev, rdt, tc_min_tokens, events, stream, nullptr);
 }
 
 // Routing, expert FFN and combine of a layer whose logits are computed.
@@ -797,7 +811,7 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
                                      int32_t *offsets_dev, int32_t *pairs_dev, float *out_dev,
                                      void *ws_dev, const void *residual_dev, rvq_dtype rdt,
                                      int32_t tc_min_tokens, void **events, cudaStream_t st,
-                                     const FfnPlan &P) {
+                                     const FfnPlan &P, float *out2) {
     const bool pdl = events == nullptr;
     auto mark = [&](int i) -> rvq_status {
         if (events) RVQ_CUDA(cudaEventRecord((cudaEvent_t)events[i], st));
@@ -819,7 +833,7 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
                         events ? events + 3 : nullptr, pdl, 0, nullptr, 0, fuse_plan));
         float *dpart = (float *)((uint8_t *)ws_dev + P.off_dpart);
         RVQ_TRY(launch_combine(dpart, P.nslot_d, topk_w_dev, n, k, bank->d, residual_dev,
-                               (int)rdt, out_dev, st, pdl));
+                               (int)rdt, out_dev, st, pdl, out2));
         return mark(7);
     }
     // with tensor-core dispatch: marks 3 = lookup-table experts done, 4 = after the
@@ -837,7 +851,7 @@ static rvq_status layer_after_router(const rvq_moe_bank *bank, const void *x_dev
     RVQ_TRY(mark(5));
     RVQ_TRY(mark(6));
     RVQ_TRY(launch_combine(ypair, 1, topk_w_dev, n, k, bank->d, residual_dev, (int)rdt, out_dev,
-                           st, pdl));
+                           st, pdl, out2));
     return mark(7);
 }
 
@@ -896,24 +910,22 @@ static rvq_status queue_layer_io(const rvq_moe_bank *bank, const float *wr_dev,
                                  size_t ws_bytes, int32_t tc_min_tokens, cudaStream_t st) {
     const size_t esz = xdt == RVQ_BF16 ? 2 : 4;
     const size_t xbytes = (size_t)n * bank->d * esz, obytes = (size_t)n * bank->d * 4;
-    // up to kIoKernelMaxBytes, a host buffer the GPU maps (pinned) is read or
-    // written by a copy kernel inside the call's launch chain; otherwise the
-    // copy is a cudaMemcpyAsync
+    // up to kIoKernelMaxBytes, a host buffer the GPU maps (pinned) is read by
+    // a copy kernel, or written by the combine, inside the call's launch
+    // chain; otherwise the copy is a cudaMemcpyAsync
     if (x_host) {
         if (void *xm = xbytes <= kIoKernelMaxBytes ? mapped_host(x_host) : nullptr)
             RVQ_TRY(launch_io_copy(xm, x_dev, xbytes, st, true));
         else
             RVQ_CUDA(cudaMemcpyAsync(x_dev, x_host, xbytes, cudaMemcpyHostToDevice, st));
     }
-    RVQ_TRY(moe_layer_forward_ex(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
-                                 topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes,
-                                 nullptr, xdt, tc_min_tokens, nullptr, (rvq_stream_t)st));
-    if (out_host) {
-        if (void *om = obytes <= kIoKernelMaxBytes ? mapped_host(out_host) : nullptr)
-            RVQ_TRY(launch_io_copy(out_dev, om, obytes, st, true));
-        else
-            RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
-    }
+    // a mapped output is written by the combine itself, beside out_dev
+    float *om = out_host && obytes <= kIoKernelMaxBytes ? (float *)mapped_host(out_host) : nullptr;
+    RVQ_TRY(layer_forward(bank, wr_dev, bias_dev, x_dev, xdt, n, k, logits_dev, topk_idx_dev,
+                          topk_w_dev, offsets_dev, pairs_dev, out_dev, ws_dev, ws_bytes, nullptr,
+                          xdt, tc_min_tokens, nullptr, (rvq_stream_t)st, om));
+    if (out_host && !om)
+        RVQ_CUDA(cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st));
     return RVQ_OK;
 }
 

@@ -14,7 +14,7 @@ constexpr int CB_Q = 16;  // column quads per block
 
 __global__ void combine_kernel(const float *__restrict__ ypart, int nslot,
                                const float *__restrict__ w, int n, int k, int d,
-                               const void *res, int rdt, float *out) {
+                               const void *res, int rdt, float *out, float *out2) {
     __shared__ float4 prod[32][CB_Q];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
@@ -54,6 +54,7 @@ __global__ void combine_kernel(const float *__restrict__ ypart, int nslot,
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
+    if (out2) *reinterpret_cast<float4 *>(out2 + (int64_t)t * d + c) = acc;
 }
 
 // A layer call's input or output moved between a host buffer the GPU maps
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(256) io_copy_kernel(const uint4 *__restrict__ 
 __global__ void __launch_bounds__(256) combine1_kernel(const float *__restrict__ y,
                                                        const float *__restrict__ w, int n, int k,
                                                        int d, const void *res, int rdt,
-                                                       float *out) {
+                                                       float *out, float *out2) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int d4 = d >> 2;
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(256) combine1_kernel(const float *__restrict__
         }
     }
     *reinterpret_cast<float4 *>(out + (int64_t)t * d + c) = acc;
+    if (out2) *reinterpret_cast<float4 *>(out2 + (int64_t)t * d + c) = acc;
 }
 
 // Row-wise RMS normalisation without a gain (the layer stack's pre-norm):
@@ -235,7 +237,8 @@ rvq_status launch_io_copy(const void *src, void *dst, size_t bytes, cudaStream_t
 }
 
 rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
-                          const void *res, int rdt, float *out, cudaStream_t stream, bool pdl) {
+                          const void *res, int rdt, float *out, cudaStream_t stream, bool pdl,
+                          float *out2) {
     if (n == 0) return RVQ_OK;
     if (k > 32) {
         set_error("combine: k %d > 32", k);
@@ -251,12 +254,13 @@ rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, 
     if (nslot == 1 && n > 64) {
         cfg.gridDim = dim3((unsigned)((d / 4 + 255) / 256), (unsigned)n);
         cfg.blockDim = dim3(256);
-        RVQ_CUDA(cudaLaunchKernelEx(&cfg, combine1_kernel, ypart, w, n, k, d, res, rdt, out));
+        RVQ_CUDA(cudaLaunchKernelEx(&cfg, combine1_kernel, ypart, w, n, k, d, res, rdt, out, out2));
         return RVQ_OK;
     }
     cfg.gridDim = dim3((unsigned)((d / 4 + CB_Q - 1) / CB_Q), (unsigned)n);
     cfg.blockDim = dim3(CB_Q, (unsigned)k);
-    RVQ_CUDA(cudaLaunchKernelEx(&cfg, combine_kernel, ypart, nslot, w, n, k, d, res, rdt, out));
+    RVQ_CUDA(cudaLaunchKernelEx(&cfg, combine_kernel, ypart, nslot, w, n, k, d, res, rdt, out,
+                                out2));
     return RVQ_OK;
 }
 

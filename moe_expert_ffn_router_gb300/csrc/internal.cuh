@@ -215,8 +215,10 @@ rvq_status launch_slot_reduce(const float *part, int n_entries, int nslot, int r
                               cudaStream_t stream, bool pdl);
 rvq_status launch_rms_norm(const void *x, int xdt, int n, int d, float eps, void *out, int odt,
                            cudaStream_t stream, bool pdl);
+// out2 (optional): a second copy of out, e.g. a host buffer the GPU maps
 rvq_status launch_combine(const float *ypart, int nslot, const float *w, int n, int k, int d,
-                          const void *res, int rdt, float *out, cudaStream_t stream, bool pdl);
+                          const void *res, int rdt, float *out, cudaStream_t stream, bool pdl,
+                          float *out2 = nullptr);
 // bytes (a multiple of 16, both ends 16-byte aligned) copied by a kernel,
 // for a host buffer the GPU maps; waits for the preceding kernel of the stream
 rvq_status launch_io_copy(const void *src, void *dst, size_t bytes, cudaStream_t stream,
